@@ -1,1 +1,245 @@
-"""Sample-guided exact Top-K over ragged FP32 score rows (CUDA, sm_103a)."""
+"""Sample-guided exact Top-K over ragged FP32 score rows (CUDA, sm_103a).
+
+A thin ctypes binding of the C ABI in include/topk.h.  It only marshals
+arguments: every step of the selection runs in the CUDA kernels of
+``lib/libtopk.so``.  PyTorch provides device memory and the current stream.
+There is no CPU fallback: if the library has not been built, every call
+raises.
+
+    import torch, exact_top_sparse_gb300 as ets
+    idx = ets.topk_ragged(scores, row_lens, K=2048)   # [M, K] int32, -1 padded
+"""
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "lib", "libtopk.so")
+
+TOPK_OK = 0
+STATUS_NAMES = {
+    0: "TOPK_OK", -1: "TOPK_ERR_ARG", -2: "TOPK_ERR_ALIGN", -3: "TOPK_ERR_WORKSPACE",
+    -4: "TOPK_ERR_CUDA", -5: "TOPK_ERR_CAPTURE_ALLOC", -6: "TOPK_ERR_UNSUPPORTED_K",
+    -7: "TOPK_ERR_NO_DEVICE",
+}
+K_MAX = 4096
+
+PATH_SENTINEL, PATH_DIRECT, PATH_TAU0, PATH_TAU1, PATH_RECOVERY = 0, 1, 2, 3, 4
+FLAG_LEN_CLAMPED, FLAG_OVERFLOW, FLAG_RECOVERY, FLAG_INTERNAL, FLAG_TIMEOUT = 1, 2, 4, 8, 16
+KIND_AUTO, KIND_DIRECT, KIND_PERSISTENT, KIND_KVSPLIT = 0, 1, 2, 3
+KIND_NAMES = {0: "auto", 1: "direct", 2: "persistent", 3: "kvsplit"}
+
+
+class TopKError(RuntimeError):
+    def __init__(self, code, where):
+        super().__init__("%s: %s (%d)" % (where, STATUS_NAMES.get(code, "unknown"), code))
+        self.code = code
+
+
+class RowDiag(ctypes.Structure):
+    _fields_ = [("tau0", ctypes.c_float), ("tau1", ctypes.c_float),
+                ("count0", ctypes.c_int64), ("count1", ctypes.c_int64),
+                ("path", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+
+
+DIAG_DTYPE = np.dtype([("tau0", "<f4"), ("tau1", "<f4"), ("count0", "<i8"), ("count1", "<i8"),
+                       ("path", "<i4"), ("flags", "<u4")])
+assert DIAG_DTYPE.itemsize == ctypes.sizeof(RowDiag)
+
+
+class Params(ctypes.Structure):
+    _fields_ = [("stride", ctypes.c_int32), ("rho0", ctypes.c_float), ("rho1", ctypes.c_float),
+                ("sample_min_len", ctypes.c_int64), ("direct_max", ctypes.c_int64),
+                ("force_kind", ctypes.c_int32), ("kv_segments", ctypes.c_int32)]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("grid", ctypes.c_int32), ("segments", ctypes.c_int32),
+                ("sm_count", ctypes.c_int32), ("workspace_bytes", ctypes.c_size_t),
+                ("smem_bytes", ctypes.c_size_t)]
+
+
+EXPORTS = ("topk_ragged", "topk_ragged_diag", "topk_ragged_ws", "topk_workspace_bytes",
+           "topk_ragged_host", "topk_plan", "topk_set_params", "topk_get_params",
+           "topk_default_params", "topk_read_status", "topk_release_workspaces",
+           "topk_status_string", "topk_version")
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load (once) and return the CUDA library; raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            "CUDA selector library not found at %s; build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'` "
+            "(there is no CPU fallback)" % path)
+    lib = ctypes.CDLL(path)
+    vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+    lib.topk_ragged.argtypes = [vp, vp, i64, i64, i32, vp, vp]
+    lib.topk_ragged_diag.argtypes = [vp, vp, i64, i64, i32, vp, vp, vp]
+    lib.topk_ragged_ws.argtypes = [vp, vp, i64, i64, i32, vp, vp, sz, vp]
+    lib.topk_workspace_bytes.argtypes = [i64, i64, i32]
+    lib.topk_workspace_bytes.restype = sz
+    lib.topk_ragged_host.argtypes = [vp, vp, i64, i64, i32, vp, i64]
+    lib.topk_plan.argtypes = [i64, i64, i32, ctypes.POINTER(PlanInfo)]
+    lib.topk_set_params.argtypes = [ctypes.POINTER(Params)]
+    lib.topk_get_params.argtypes = [ctypes.POINTER(Params)]
+    lib.topk_default_params.argtypes = [ctypes.POINTER(Params)]
+    lib.topk_default_params.restype = None
+    lib.topk_read_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.topk_release_workspaces.argtypes = []
+    lib.topk_release_workspaces.restype = None
+    lib.topk_status_string.argtypes = [ctypes.c_int]
+    lib.topk_status_string.restype = ctypes.c_char_p
+    lib.topk_version.argtypes = []
+    for name in ("topk_ragged", "topk_ragged_diag", "topk_ragged_ws", "topk_ragged_host",
+                 "topk_plan", "topk_set_params", "topk_get_params", "topk_read_status",
+                 "topk_version"):
+        getattr(lib, name).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _check(code, where):
+    if code != TOPK_OK:
+        raise TopKError(code, where)
+
+
+def _stream_handle(device, stream):
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _inputs(scores, row_lens, K, out):
+    if not (isinstance(scores, torch.Tensor) and scores.is_cuda):
+        raise TypeError("scores must be a CUDA tensor")
+    if scores.dtype != torch.float32 or scores.dim() != 2:
+        raise TypeError("scores must be a 2-D float32 tensor [M, N_alloc]")
+    if scores.stride(1) != 1 or (scores.shape[0] > 1 and scores.stride(0) != scores.shape[1]):
+        raise ValueError("scores must be contiguous (row stride N_alloc)")
+    if not (isinstance(row_lens, torch.Tensor) and row_lens.device == scores.device
+            and row_lens.dtype == torch.int32 and row_lens.dim() == 1
+            and row_lens.shape[0] == scores.shape[0] and row_lens.is_contiguous()):
+        raise TypeError("row_lens must be a contiguous int32 [M] tensor on the scores' device")
+    M, N = scores.shape
+    if out is None:
+        out = torch.empty((M, K), dtype=torch.int32, device=scores.device)
+    elif not (out.device == scores.device and out.dtype == torch.int32
+              and tuple(out.shape) == (M, K) and out.is_contiguous()):
+        raise TypeError("out must be a contiguous int32 [M, K] tensor on the scores' device")
+    return M, N, out
+
+
+def topk_ragged(scores: torch.Tensor, row_lens: torch.Tensor, K: int = 2048,
+                out: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """Exact Top-K of every row's valid prefix; [M, K] int32, unsorted, -1 padded."""
+    lib = load_library()
+    M, N, out = _inputs(scores, row_lens, K, out)
+    with torch.cuda.device(scores.device):
+        rc = lib.topk_ragged(scores.data_ptr(), row_lens.data_ptr(), M, N, K, out.data_ptr(),
+                             _stream_handle(scores.device, stream))
+    _check(rc, "topk_ragged")
+    return out
+
+
+def topk_ragged_diag(scores, row_lens, K: int = 2048, out=None, stream=None):
+    """topk_ragged plus per-row diagnostics (numpy structured array, host copy)."""
+    lib = load_library()
+    M, N, out = _inputs(scores, row_lens, K, out)
+    diag = torch.empty(M * DIAG_DTYPE.itemsize, dtype=torch.uint8, device=scores.device)
+    with torch.cuda.device(scores.device):
+        rc = lib.topk_ragged_diag(scores.data_ptr(), row_lens.data_ptr(), M, N, K,
+                                  out.data_ptr(), diag.data_ptr(),
+                                  _stream_handle(scores.device, stream))
+    _check(rc, "topk_ragged_diag")
+    return out, diag.cpu().numpy().view(DIAG_DTYPE)
+
+
+def workspace_bytes(M: int, N_alloc: int, K: int = 2048) -> int:
+    return int(load_library().topk_workspace_bytes(M, N_alloc, K))
+
+
+def topk_ragged_ws(scores, row_lens, K, workspace: torch.Tensor, out=None, stream=None):
+    """Explicit-workspace form; `workspace` is a zero-initialised CUDA byte tensor."""
+    lib = load_library()
+    M, N, out = _inputs(scores, row_lens, K, out)
+    with torch.cuda.device(scores.device):
+        rc = lib.topk_ragged_ws(scores.data_ptr(), row_lens.data_ptr(), M, N, K, out.data_ptr(),
+                                workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                _stream_handle(scores.device, stream))
+    _check(rc, "topk_ragged_ws")
+    return out
+
+
+def topk_ragged_host(scores: np.ndarray, row_lens: np.ndarray, K: int = 2048,
+                     out: np.ndarray = None, rows_per_chunk: int = 0) -> np.ndarray:
+    """Host-buffer form: host arrays in, host indices out (copies inside the call)."""
+    lib = load_library()
+    if not (isinstance(scores, np.ndarray) and scores.dtype == np.float32 and scores.ndim == 2
+            and scores.flags.c_contiguous):
+        raise TypeError("scores must be a C-contiguous float32 [M, N_alloc] array")
+    row_lens = np.ascontiguousarray(row_lens, dtype=np.int32)
+    M, N = scores.shape
+    if out is None:
+        out = np.empty((M, K), dtype=np.int32)
+    rc = lib.topk_ragged_host(scores.ctypes.data, row_lens.ctypes.data, M, N, K, out.ctypes.data,
+                              rows_per_chunk)
+    _check(rc, "topk_ragged_host")
+    return out
+
+
+def plan(M: int, N_alloc: int, K: int = 2048) -> dict:
+    info = PlanInfo()
+    _check(load_library().topk_plan(M, N_alloc, K, ctypes.byref(info)), "topk_plan")
+    return {"kind": KIND_NAMES[info.kind], "grid": info.grid, "segments": info.segments,
+            "sm_count": info.sm_count, "workspace_bytes": info.workspace_bytes,
+            "smem_bytes": info.smem_bytes}
+
+
+def get_params() -> dict:
+    p = Params()
+    _check(load_library().topk_get_params(ctypes.byref(p)), "topk_get_params")
+    return {f: getattr(p, f) for f, _ in Params._fields_}
+
+
+def default_params() -> dict:
+    p = Params()
+    load_library().topk_default_params(ctypes.byref(p))
+    return {f: getattr(p, f) for f, _ in Params._fields_}
+
+
+def set_params(**kw) -> dict:
+    """Update process-wide parameters; returns the previous values."""
+    old = get_params()
+    new = dict(old)
+    for k, v in kw.items():
+        if k not in new:
+            raise KeyError(k)
+        new[k] = v
+    p = Params(**new)
+    _check(load_library().topk_set_params(ctypes.byref(p)), "topk_set_params")
+    return old
+
+
+def read_status(device=None, stream=None) -> int:
+    """Read and clear the device status word (OR of FLAG_* since the last read)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    flags = ctypes.c_uint32(0)
+    with torch.cuda.device(dev):
+        _check(load_library().topk_read_status(_stream_handle(dev, stream), ctypes.byref(flags)),
+               "topk_read_status")
+    return int(flags.value)
+
+
+def release_workspaces() -> None:
+    load_library().topk_release_workspaces()
+
+
+def version() -> int:
+    return int(load_library().topk_version())

@@ -1,0 +1,452 @@
+// C ABI of the exact Top-K selector: argument checks, the host planner that
+// picks the execution path, the per-(device, stream) workspace cache and the
+// host-buffer pipeline.  The planner reads only sizes and device properties,
+// never device memory, so every call can be captured in a CUDA graph once its
+// workspace exists (the pages' timings are CUDA-graph replays: codexqa.cn
+// article, section "什么叫精确，时间怎么量"; graph-capturable ragged-row dispatch:
+// arxivdaily abstract).
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "../../include/topk.h"
+#include "topk_launch.h"
+
+namespace {
+
+constexpr int kVersion = 10000;  // 1.0.0
+constexpr size_t kHdrBytes = 256;
+constexpr int64_t kMinSegment = 32768;  // floats per KV-split segment, at least
+constexpr int kKvWavesPersistent = 6;   // M >= this many resident waves -> persistent
+constexpr int kKvTargetWaves = 12;      // KV-split aims at this many CTA waves
+
+std::mutex g_mu;
+topk_params g_params;
+bool g_params_init = false;
+
+struct DevInfo {
+  bool ready = false;
+  int sm_count = 0;
+  int occ = 0;
+  size_t optin = 0;
+};
+std::map<int, DevInfo> g_dev;
+
+struct Buf {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+};
+std::map<std::pair<int, uintptr_t>, Buf> g_ws;  // (device, stream) -> workspace
+
+struct HostPipe {
+  float* scores[2] = {nullptr, nullptr};
+  int32_t* lens[2] = {nullptr, nullptr};
+  int32_t* out[2] = {nullptr, nullptr};
+  size_t score_bytes = 0, lens_bytes = 0, out_bytes = 0;
+  cudaStream_t st[2] = {nullptr, nullptr};
+};
+std::map<int, HostPipe> g_pipe;
+
+void defaults(topk_params* p) {
+  p->stride = 128;
+  p->rho0 = 1.5f;
+  p->rho1 = 1.75f;
+  p->sample_min_len = 16384;
+  p->direct_max = 49152;
+  p->force_kind = TOPK_KIND_AUTO;
+  p->kv_segments = 0;
+}
+
+topk_params params_snapshot() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_params_init) {
+    defaults(&g_params);
+    g_params_init = true;
+  }
+  return g_params;
+}
+
+int device_info(DevInfo* out, int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TOPK_ERR_NO_DEVICE;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.ready) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return TOPK_ERR_NO_DEVICE;
+    if (prop.major != 10 || prop.minor != 3) return TOPK_ERR_NO_DEVICE;  // built for sm_103a only
+    if (tk::prepare_device() != cudaSuccess) return TOPK_ERR_CUDA;
+    int occ = 0;
+    if (tk::persistent_occupancy(&occ) != cudaSuccess || occ < 1) return TOPK_ERR_CUDA;
+    d.sm_count = prop.multiProcessorCount;
+    d.occ = occ;
+    d.optin = prop.sharedMemPerBlockOptin;
+    d.ready = true;
+  }
+  *out = d;
+  if (dev_out) *dev_out = dev;
+  return TOPK_OK;
+}
+
+struct Plan {
+  int kind = TOPK_KIND_AUTO;
+  int grid = 0;
+  int segments = 1;
+  size_t ws = 0;
+  size_t smem = 0;
+};
+
+int check_sizes(int64_t M, int64_t N, int32_t K) {
+  if (M < 0 || N < 0 || N > INT32_MAX || M > INT32_MAX) return TOPK_ERR_ARG;
+  if (K < 1) return TOPK_ERR_ARG;
+  if (K > TOPK_K_MAX) return TOPK_ERR_UNSUPPORTED_K;
+  if (M > 0 && N > 0 && M > INT64_MAX / N) return TOPK_ERR_ARG;
+  return TOPK_OK;
+}
+
+int make_plan(int64_t M, int64_t N, int32_t K, const topk_params& p, const DevInfo& d, Plan* pl) {
+  (void)K;
+  const int resident = d.sm_count * d.occ;
+  const bool direct_fits = tk::direct_smem_bytes(N) <= d.optin;
+  int kind = p.force_kind;
+  if (kind == TOPK_KIND_DIRECT && !direct_fits) return TOPK_ERR_ARG;
+  if (kind == TOPK_KIND_AUTO) {
+    if (N <= p.direct_max && direct_fits) kind = TOPK_KIND_DIRECT;
+    else if (M >= (int64_t)kKvWavesPersistent * resident) kind = TOPK_KIND_PERSISTENT;
+    else kind = TOPK_KIND_KVSPLIT;
+  }
+  int segments = 1;
+  if (kind == TOPK_KIND_KVSPLIT) {
+    int64_t P = p.kv_segments;
+    if (P <= 0) {
+      P = ((int64_t)kKvTargetWaves * resident + M - 1) / (M > 0 ? M : 1);
+      int64_t pmax = N / kMinSegment;
+      if (pmax < 1) pmax = 1;
+      if (P > pmax) P = pmax;
+    }
+    if (P < 1) P = 1;
+    if (P > 4096) P = 4096;
+    if (M * P > INT32_MAX) return TOPK_ERR_ARG;
+    if (P == 1 && p.force_kind != TOPK_KIND_KVSPLIT) kind = TOPK_KIND_PERSISTENT;
+    segments = (int)P;
+  }
+  pl->kind = kind;
+  pl->segments = (kind == TOPK_KIND_KVSPLIT) ? segments : 1;
+  pl->ws = kHdrBytes;
+  if (kind == TOPK_KIND_DIRECT) {
+    pl->grid = (int)M;
+    pl->smem = tk::direct_smem_bytes(N);
+  } else if (kind == TOPK_KIND_PERSISTENT) {
+    pl->grid = (int)(M < resident ? M : resident);
+    pl->smem = tk::persistent_smem_bytes();
+  } else {
+    pl->grid = (int)(M * pl->segments);
+    pl->smem = tk::kv_segment_smem_bytes();
+    pl->ws += (size_t)M * tk::kv_row_bytes();
+  }
+  return TOPK_OK;
+}
+
+int validate_ptrs(const float* scores, const int32_t* row_lens, int64_t M, int64_t N,
+                  int32_t* out_idx) {
+  if (M == 0) return TOPK_OK;
+  if (!row_lens || !out_idx) return TOPK_ERR_ARG;
+  if (N > 0 && !scores) return TOPK_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(scores) & 3u) || (reinterpret_cast<uintptr_t>(out_idx) & 3u) ||
+      (reinterpret_cast<uintptr_t>(row_lens) & 3u))
+    return TOPK_ERR_ALIGN;
+  return TOPK_OK;
+}
+
+tk::Params kernel_params(int64_t M, int64_t N, int32_t K, const topk_params& p, const Plan& pl) {
+  tk::Params P;
+  P.M = M;
+  P.N_alloc = N;
+  P.K = K;
+  P.stride = p.stride;
+  P.target0 = (uint32_t)std::ceil((double)p.rho0 * (double)K);
+  P.target1 = (uint32_t)std::ceil((double)p.rho1 * (double)K);
+  if (P.target1 < P.target0) P.target1 = P.target0;
+  P.sample_min_len = p.sample_min_len;
+  P.segments = pl.segments;
+  return P;
+}
+
+int launch(const Plan& pl, const tk::Params& P, const float* scores, const int32_t* row_lens,
+           int32_t* out_idx, topk_row_diag* diag, void* ws, cudaStream_t st) {
+  tk::RowDiag* d = reinterpret_cast<tk::RowDiag*>(diag);
+  cudaError_t e;
+  if (pl.kind == TOPK_KIND_DIRECT) {
+    e = tk::launch_direct(scores, row_lens, out_idx, d, P, st);
+  } else if (pl.kind == TOPK_KIND_PERSISTENT) {
+    e = tk::launch_persistent(scores, row_lens, out_idx, d, static_cast<uint32_t*>(ws), pl.grid,
+                              P, st);
+  } else {
+    e = tk::launch_kvsplit(scores, row_lens, out_idx, d,
+                           static_cast<uint8_t*>(ws) + kHdrBytes, P, st);
+  }
+  return e == cudaSuccess ? TOPK_OK : TOPK_ERR_CUDA;
+}
+
+// Workspace for (current device, stream), grown on demand.  A new buffer is
+// zero-filled (the persistent queue counters must start at zero).
+int cached_workspace(int dev, cudaStream_t st, size_t need, void** ptr) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  Buf& b = g_ws[{dev, reinterpret_cast<uintptr_t>(st)}];
+  if (b.bytes >= need && b.ptr) {
+    *ptr = b.ptr;
+    return TOPK_OK;
+  }
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return TOPK_ERR_CUDA;
+  if (cs != cudaStreamCaptureStatusNone) return TOPK_ERR_CAPTURE_ALLOC;
+  if (b.ptr) {
+    if (cudaStreamSynchronize(st) != cudaSuccess) return TOPK_ERR_CUDA;
+    cudaFree(b.ptr);
+    b.ptr = nullptr;
+    b.bytes = 0;
+  }
+  size_t bytes = need < (1u << 20) ? (1u << 20) : need;
+  void* p = nullptr;
+  if (cudaMalloc(&p, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return TOPK_ERR_CUDA;
+  }
+  if (cudaMemset(p, 0, bytes) != cudaSuccess) {
+    cudaFree(p);
+    return TOPK_ERR_CUDA;
+  }
+  b.ptr = p;
+  b.bytes = bytes;
+  *ptr = p;
+  return TOPK_OK;
+}
+
+int run(const float* scores, const int32_t* row_lens, int64_t M, int64_t N, int32_t K,
+        int32_t* out_idx, topk_row_diag* diag, void* ws, size_t ws_bytes, bool explicit_ws,
+        cudaStream_t st) {
+  int rc = check_sizes(M, N, K);
+  if (rc) return rc;
+  rc = validate_ptrs(scores, row_lens, M, N, out_idx);
+  if (rc) return rc;
+  if (M == 0) return TOPK_OK;
+  if (explicit_ws) {
+    if (!ws) return TOPK_ERR_ARG;
+    if (reinterpret_cast<uintptr_t>(ws) & 255u) return TOPK_ERR_ALIGN;
+  }
+  DevInfo d;
+  int dev = 0;
+  rc = device_info(&d, &dev);
+  if (rc) return rc;
+  const topk_params p = params_snapshot();
+  Plan pl;
+  rc = make_plan(M, N, K, p, d, &pl);
+  if (rc) return rc;
+  if (explicit_ws) {
+    if (ws_bytes < pl.ws) return TOPK_ERR_WORKSPACE;
+  } else {
+    rc = cached_workspace(dev, st, pl.ws, &ws);
+    if (rc) return rc;
+  }
+  return launch(pl, kernel_params(M, N, K, p, pl), scores, row_lens, out_idx, diag, ws, st);
+}
+
+}  // namespace
+
+extern "C" {
+
+int topk_ragged(const float* scores, const int32_t* row_lens, int64_t M, int64_t N_alloc,
+                int32_t K, int32_t* out_idx, struct CUstream_st* stream) {
+  return run(scores, row_lens, M, N_alloc, K, out_idx, nullptr, nullptr, 0, false, stream);
+}
+
+int topk_ragged_diag(const float* scores, const int32_t* row_lens, int64_t M, int64_t N_alloc,
+                     int32_t K, int32_t* out_idx, topk_row_diag* diag,
+                     struct CUstream_st* stream) {
+  if (M > 0 && !diag) return TOPK_ERR_ARG;
+  return run(scores, row_lens, M, N_alloc, K, out_idx, diag, nullptr, 0, false, stream);
+}
+
+int topk_ragged_ws(const float* scores, const int32_t* row_lens, int64_t M, int64_t N_alloc,
+                   int32_t K, int32_t* out_idx, void* workspace, size_t workspace_bytes,
+                   struct CUstream_st* stream) {
+  return run(scores, row_lens, M, N_alloc, K, out_idx, nullptr, workspace, workspace_bytes, true,
+             stream);
+}
+
+size_t topk_workspace_bytes(int64_t M, int64_t N_alloc, int32_t K) {
+  if (check_sizes(M, N_alloc, K) || M == 0) return 0;
+  DevInfo d;
+  if (device_info(&d, nullptr)) return 0;
+  Plan pl;
+  if (make_plan(M, N_alloc, K, params_snapshot(), d, &pl)) return 0;
+  return pl.ws;
+}
+
+int topk_plan(int64_t M, int64_t N_alloc, int32_t K, topk_plan_info* info) {
+  if (!info) return TOPK_ERR_ARG;
+  int rc = check_sizes(M, N_alloc, K);
+  if (rc) return rc;
+  DevInfo d;
+  rc = device_info(&d, nullptr);
+  if (rc) return rc;
+  Plan pl;
+  rc = make_plan(M, N_alloc, K, params_snapshot(), d, &pl);
+  if (rc) return rc;
+  info->kind = pl.kind;
+  info->grid = pl.grid;
+  info->segments = pl.segments;
+  info->sm_count = d.sm_count;
+  info->workspace_bytes = pl.ws;
+  info->smem_bytes = pl.smem;
+  return TOPK_OK;
+}
+
+void topk_default_params(topk_params* p) {
+  if (p) defaults(p);
+}
+
+int topk_set_params(const topk_params* p) {
+  if (!p) return TOPK_ERR_ARG;
+  if (p->stride < 1 || !(p->rho0 >= 1.0f) || !(p->rho1 >= p->rho0) || !(p->rho1 <= 64.0f) ||
+      p->sample_min_len < 0 || p->direct_max < 0 || p->kv_segments < 0 ||
+      p->kv_segments > 4096 || p->force_kind < TOPK_KIND_AUTO || p->force_kind > TOPK_KIND_KVSPLIT)
+    return TOPK_ERR_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_params = *p;
+  g_params_init = true;
+  return TOPK_OK;
+}
+
+int topk_get_params(topk_params* p) {
+  if (!p) return TOPK_ERR_ARG;
+  *p = params_snapshot();
+  return TOPK_OK;
+}
+
+int topk_read_status(struct CUstream_st* stream, uint32_t* flags) {
+  if (!flags) return TOPK_ERR_ARG;
+  DevInfo d;
+  int rc = device_info(&d, nullptr);
+  if (rc) return rc;
+  return tk::read_and_clear_status(stream, flags) == cudaSuccess ? TOPK_OK : TOPK_ERR_CUDA;
+}
+
+int topk_ragged_host(const float* h_scores, const int32_t* h_lens, int64_t M, int64_t N_alloc,
+                     int32_t K, int32_t* h_out, int64_t rows_per_chunk) {
+  int rc = check_sizes(M, N_alloc, K);
+  if (rc) return rc;
+  if (M == 0) return TOPK_OK;
+  if (!h_lens || !h_out || (N_alloc > 0 && !h_scores) || rows_per_chunk < 0) return TOPK_ERR_ARG;
+  DevInfo d;
+  int dev = 0;
+  rc = device_info(&d, &dev);
+  if (rc) return rc;
+  const size_t row_bytes = (size_t)N_alloc * sizeof(float);
+  int64_t rows = rows_per_chunk;
+  if (rows == 0) rows = row_bytes ? (int64_t)((1ull << 30) / row_bytes) : M;
+  if (rows < 1) rows = 1;
+  if (rows > M) rows = M;
+  HostPipe* hp;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    hp = &g_pipe[dev];
+  }
+  const size_t need_s = (size_t)rows * row_bytes, need_l = (size_t)rows * 4,
+               need_o = (size_t)rows * K * 4;
+  for (int i = 0; i < 2; ++i) {
+    if (!hp->st[i] && cudaStreamCreateWithFlags(&hp->st[i], cudaStreamNonBlocking) != cudaSuccess)
+      return TOPK_ERR_CUDA;
+  }
+  if (hp->score_bytes < need_s || hp->lens_bytes < need_l || hp->out_bytes < need_o) {
+    for (int i = 0; i < 2; ++i) {
+      cudaStreamSynchronize(hp->st[i]);
+      cudaFree(hp->scores[i]);
+      cudaFree(hp->lens[i]);
+      cudaFree(hp->out[i]);
+      hp->scores[i] = nullptr;
+      hp->lens[i] = nullptr;
+      hp->out[i] = nullptr;
+    }
+    hp->score_bytes = hp->lens_bytes = hp->out_bytes = 0;
+    for (int i = 0; i < 2; ++i) {
+      if (cudaMalloc(&hp->scores[i], need_s ? need_s : 16) != cudaSuccess ||
+          cudaMalloc(&hp->lens[i], need_l) != cudaSuccess ||
+          cudaMalloc(&hp->out[i], need_o) != cudaSuccess) {
+        cudaGetLastError();
+        return TOPK_ERR_CUDA;
+      }
+    }
+    hp->score_bytes = need_s;
+    hp->lens_bytes = need_l;
+    hp->out_bytes = need_o;
+  }
+  for (int64_t r0 = 0, c = 0; r0 < M; r0 += rows, ++c) {
+    const int64_t n = (M - r0) < rows ? (M - r0) : rows;
+    const int s = (int)(c & 1);
+    cudaStream_t st = hp->st[s];
+    if (row_bytes &&
+        cudaMemcpyAsync(hp->scores[s], h_scores + r0 * N_alloc, (size_t)n * row_bytes,
+                        cudaMemcpyHostToDevice, st) != cudaSuccess)
+      return TOPK_ERR_CUDA;
+    if (cudaMemcpyAsync(hp->lens[s], h_lens + r0, (size_t)n * 4, cudaMemcpyHostToDevice, st) !=
+        cudaSuccess)
+      return TOPK_ERR_CUDA;
+    rc = topk_ragged(hp->scores[s], hp->lens[s], n, N_alloc, K, hp->out[s], st);
+    if (rc) return rc;
+    if (cudaMemcpyAsync(h_out + r0 * K, hp->out[s], (size_t)n * K * 4, cudaMemcpyDeviceToHost,
+                        st) != cudaSuccess)
+      return TOPK_ERR_CUDA;
+  }
+  for (int i = 0; i < 2; ++i)
+    if (cudaStreamSynchronize(hp->st[i]) != cudaSuccess) return TOPK_ERR_CUDA;
+  return TOPK_OK;
+}
+
+void topk_release_workspaces(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int cur = 0;
+  cudaGetDevice(&cur);
+  for (auto& kv : g_ws) {
+    if (!kv.second.ptr) continue;
+    cudaSetDevice(kv.first.first);
+    cudaDeviceSynchronize();
+    cudaFree(kv.second.ptr);
+  }
+  g_ws.clear();
+  for (auto& kv : g_pipe) {
+    cudaSetDevice(kv.first);
+    cudaDeviceSynchronize();
+    for (int i = 0; i < 2; ++i) {
+      cudaFree(kv.second.scores[i]);
+      cudaFree(kv.second.lens[i]);
+      cudaFree(kv.second.out[i]);
+      if (kv.second.st[i]) cudaStreamDestroy(kv.second.st[i]);
+    }
+  }
+  g_pipe.clear();
+  cudaSetDevice(cur);
+}
+
+const char* topk_status_string(int code) {
+  switch (code) {
+    case TOPK_OK: return "ok";
+    case TOPK_ERR_ARG: return "invalid argument";
+    case TOPK_ERR_ALIGN: return "misaligned pointer";
+    case TOPK_ERR_WORKSPACE: return "workspace too small";
+    case TOPK_ERR_CUDA: return "CUDA runtime error";
+    case TOPK_ERR_CAPTURE_ALLOC: return "workspace allocation needed during stream capture";
+    case TOPK_ERR_UNSUPPORTED_K: return "K larger than TOPK_K_MAX";
+    case TOPK_ERR_NO_DEVICE: return "no usable sm_103 device";
+    default: return "unknown status";
+  }
+}
+
+int topk_version(void) { return kVersion; }
+
+}  // extern "C"

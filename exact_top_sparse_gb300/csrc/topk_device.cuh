@@ -1,0 +1,828 @@
+// Device building blocks of the sample-guided exact Top-K selector (sm_103a).
+//
+// Method (web pages on "Sample-Guided Exact Top-K Selection for Long-Context
+// Sparse Attention", Tencent HPC-Ops):
+//   * PaperDaily "腾讯|长上下文稀疏注意力前K精确选择", section 问题二, Fig. 4:
+//     stage 1, a fixed-stride view of the current row proposes a provisional
+//     threshold tau0 and a wider nested tau1; stage 2, the mandatory full-row
+//     pass counts C(tau0), forms the admitted candidate set and seeds the first
+//     FP32 radix histogram; if C(tau0) < K the nested threshold is used, and if
+//     that still underfills the row is recovered exactly from the whole row;
+//     stage 3, exact radix refinement over the raw FP32 bits runs only on the
+//     unresolved boundary bin, resolved high bins are emitted and never
+//     revisited, output order is free.
+//   * codexqa.cn "几何平均快 1.55 倍…腾讯怎么测精确 Top-K", section
+//     "采样不是处处都该开": stride 128, primary target 1.5K, nested 1.75K.
+//   * arxivdaily abstract: certification and candidate formation are fused in
+//     one pass; persistent, KV-split and direct-exact execution sit behind a
+//     graph-capturable ragged-row dispatch.
+//
+// Order key: key(v) maps FP32 bits to an unsigned integer whose order is the
+// IEEE order of the scores, with -0.0 mapped onto +0.0 so that the key order
+// and the float comparison agree on every non-NaN value.
+//
+// This build differs from the pages' H20 design where GB300 pays for it: the
+// full-row pass streams the row through shared memory with 1-D bulk async
+// copies (TMA) into a 3-stage ring driven by mbarriers; candidates of the
+// nested band are collected in the same pass, so the tau1 path needs no
+// re-read; radix rounds use data-relative 11-bit digits so the first
+// histogram is not degenerate on concentrated scores.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "topk_launch.h"
+
+namespace tk {
+
+// ----------------------------------------------------------------- constants
+constexpr int THREADS = 512;                // threads per CTA for every kernel
+constexpr int NWARPS = THREADS / 32;
+constexpr int CONSUMER_WARPS = NWARPS - 1;  // warp 0 issues the bulk copies
+constexpr int CONSUMERS = CONSUMER_WARPS * 32;
+constexpr int NB_BITS = 11;
+constexpr int NB = 1 << NB_BITS;            // bins per radix round
+static_assert(NB == 4 * THREADS, "boundary search maps 4 bins to each thread");
+constexpr int STAGES = 3;                   // ring stages
+constexpr int CHUNK_BYTES = 16384;          // bytes per bulk copy / ring stage
+constexpr int CHUNK_FLOATS = CHUNK_BYTES / 4;
+constexpr int CAP = 6144;                   // on-chip candidate capacity (entries of 8 B)
+constexpr int SMALL = 32;                   // frontier size finished by one warp
+constexpr int SAMPLE_SMEM = 2 * CAP;        // sample keys kept on chip (they alias the candidates)
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // bounded waits give up after 2 s
+
+// Row paths and status bits (same values as the public header).
+constexpr int32_t PATH_SENTINEL = 0, PATH_DIRECT = 1, PATH_TAU0 = 2, PATH_TAU1 = 3,
+                  PATH_RECOVERY = 4;
+constexpr uint32_t F_LEN_CLAMPED = 0x1u, F_OVERFLOW = 0x2u, F_RECOVERY = 0x4u,
+                   F_INTERNAL = 0x8u, F_TIMEOUT = 0x10u;
+
+constexpr unsigned FULL_MASK = 0xffffffffu;
+
+// --------------------------------------------------------------- order key
+__device__ __forceinline__ uint32_t fkey(float v) {
+  const uint32_t u = __float_as_uint(v);
+  const uint32_t k = u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
+  return k + (k == 0x7fffffffu);  // -0.0 joins +0.0
+}
+
+__device__ __forceinline__ float key_to_float(uint32_t k) {
+  const uint32_t u = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
+  return __uint_as_float(u);
+}
+
+// ----------------------------------------------------------------- PTX glue
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase of `bar` with the given parity; gives up (returns false)
+// after WAIT_LIMIT_NS so that no wait can hang the GPU.
+__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0 && globaltimer() - t0 > WAIT_LIMIT_NS) return false;
+  }
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// 1-D bulk copy global -> shared, completion counted on `bar` (bytes % 16 == 0,
+// both addresses 16-byte aligned).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ float ld_keep(const float* p, uint64_t policy) {
+  float v;
+  asm volatile("ld.global.nc.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(p), "l"(policy));
+  return v;
+}
+
+// ------------------------------------------------------------ warp / block
+__device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
+
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t x) {
+  const uint32_t lane = lane_id();
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(FULL_MASK, x, o);
+    if (lane >= (uint32_t)o) x += y;
+  }
+  return x;
+}
+
+// Shared scratch of every kernel.  Lives at the start of dynamic shared memory.
+struct __align__(16) Shared {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint2 small[SMALL];            // (idx, key) of a small frontier
+  uint32_t wtmp[NWARPS + 2];
+  uint32_t wtmp2[NWARPS + 2];
+  uint32_t row;
+  uint32_t ncand;                // admitted candidates (counts past CAP)
+  uint32_t nout;                 // indices emitted for the current row
+  uint32_t c0;                   // C(tau0)
+  uint32_t small_n;
+  uint32_t take;
+  uint32_t b, above, ok;
+  uint32_t flags;
+  uint32_t kmin, kmax, res;
+  uint32_t key0, key1;
+  uint32_t last;
+};
+
+// Exclusive prefix sum over all THREADS threads (every thread must call).
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, Shared& S, uint32_t* total) {
+  const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+  const uint32_t incl = warp_incl_scan(v);
+  if (lane == 31) S.wtmp[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t w = lane < (uint32_t)NWARPS ? S.wtmp[lane] : 0u;
+    const uint32_t wi = warp_incl_scan(w);
+    if (lane < (uint32_t)NWARPS) S.wtmp[lane] = wi - w;
+    if (lane == NWARPS - 1) S.wtmp[NWARPS] = wi;
+  }
+  __syncthreads();
+  const uint32_t r = S.wtmp[warp] + incl - v;
+  *total = S.wtmp[NWARPS];
+  __syncthreads();
+  return r;
+}
+
+// Block-wide min and max of u32 values (every thread must call).
+__device__ __forceinline__ void block_minmax(uint32_t mn, uint32_t mx, Shared& S, uint32_t* omn,
+                                             uint32_t* omx) {
+  const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mn = min(mn, __shfl_xor_sync(FULL_MASK, mn, o));
+    mx = max(mx, __shfl_xor_sync(FULL_MASK, mx, o));
+  }
+  if (lane == 0) {
+    S.wtmp[warp] = mn;
+    S.wtmp2[warp] = mx;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    mn = lane < (uint32_t)NWARPS ? S.wtmp[lane] : 0xffffffffu;
+    mx = lane < (uint32_t)NWARPS ? S.wtmp2[lane] : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mn = min(mn, __shfl_xor_sync(FULL_MASK, mn, o));
+      mx = max(mx, __shfl_xor_sync(FULL_MASK, mx, o));
+    }
+    if (lane == 0) {
+      S.wtmp[NWARPS] = mn;
+      S.wtmp2[NWARPS] = mx;
+    }
+  }
+  __syncthreads();
+  *omn = S.wtmp[NWARPS];
+  *omx = S.wtmp2[NWARPS];
+  __syncthreads();
+}
+
+__device__ __forceinline__ uint32_t block_sum(uint32_t v, Shared& S) {
+  uint32_t total;
+  block_excl_scan(v, S, &total);
+  return total;
+}
+
+// ------------------------------------------------------------------ binning
+// One radix round over the key interval [lo, hi].  Keys below `base` fall in
+// bin 0, bins 1..NB-2 are 2^shift keys wide starting at base, and bin NB-1
+// also takes every key above its start up to hi.
+struct Bins {
+  uint32_t lo, hi, base, shift;
+
+  __device__ __forceinline__ uint32_t digit(uint32_t k) const {
+    if (k < base) return 0;
+    const uint32_t d = (k - base) >> shift;
+    return d < (uint32_t)(NB - 1) ? d : (uint32_t)(NB - 1);
+  }
+  __device__ __forceinline__ uint32_t bin_lo(uint32_t b) const {
+    if (b == 0) return lo;
+    const uint64_t x = (uint64_t)base + ((uint64_t)b << shift);
+    return x > hi ? hi : (uint32_t)x;
+  }
+  __device__ __forceinline__ uint32_t bin_hi(uint32_t b) const {
+    if (b == (uint32_t)(NB - 1)) return hi;
+    const uint64_t x = (uint64_t)base + ((uint64_t)(b + 1) << shift) - 1;
+    return x > hi ? hi : (uint32_t)x;
+  }
+};
+
+__device__ __forceinline__ uint32_t shift_for_span(uint32_t span, uint32_t max_digit) {
+  uint32_t s = 0;
+  while ((span >> s) > max_digit) ++s;
+  return s;
+}
+
+// Plain bins over [lo, hi]: base = lo and the narrowest shift that fits.
+__device__ __forceinline__ Bins make_bins(uint32_t lo, uint32_t hi) {
+  Bins b;
+  b.lo = lo;
+  b.hi = hi;
+  b.base = lo;
+  b.shift = shift_for_span(hi - lo, NB - 1);
+  return b;
+}
+
+// Bins whose regular range is [base, top] inside a wider frontier [lo, hi].
+__device__ __forceinline__ Bins make_bins_focus(uint32_t lo, uint32_t hi, uint32_t base,
+                                                uint32_t top) {
+  Bins b;
+  b.lo = lo;
+  b.hi = hi;
+  b.base = base < lo ? lo : (base > hi ? hi : base);
+  if (top < b.base) top = b.base;
+  if (top > hi) top = hi;
+  b.shift = shift_for_span(top - b.base, NB - 2);
+  return b;
+}
+
+// Boundary search: the largest bin b whose suffix count (bins >= b) reaches
+// Kp.  Writes S.b, S.above (count in bins > b) and S.ok (0 when the histogram
+// holds fewer than Kp keys).  Every thread must call.
+__device__ __forceinline__ void find_boundary(const uint32_t* hist, uint32_t Kp, Shared& S) {
+  const uint32_t t = threadIdx.x;
+  if (t == 0) S.ok = 0;
+  const int top = NB - 1 - 4 * (int)t;
+  const uint32_t h0 = hist[top], h1 = hist[top - 1], h2 = hist[top - 2], h3 = hist[top - 3];
+  const uint32_t s = h0 + h1 + h2 + h3;
+  uint32_t total;
+  const uint32_t pre = block_excl_scan(s, S, &total);
+  if (pre < Kp && pre + s >= Kp) {
+    uint32_t acc = pre, b = (uint32_t)top;
+    const uint32_t hh[4] = {h0, h1, h2, h3};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (acc + hh[j] >= Kp) {
+        b = (uint32_t)(top - j);
+        break;
+      }
+      acc += hh[j];
+    }
+    S.b = b;
+    S.above = acc;
+    S.ok = 1;
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ void clear_hist(uint32_t* hist) {
+  for (int i = threadIdx.x; i < NB; i += THREADS) hist[i] = 0;
+}
+
+// Descending bitonic sort of one (idx, key) pair per lane by key.
+// Invalid lanes carry key 0 and idx 0xffffffff and sort last among equals.
+__device__ __forceinline__ void warp_sort_desc(uint32_t& key, uint32_t& idx) {
+  const uint32_t lane = lane_id();
+  uint64_t v = ((uint64_t)key << 32) | (uint64_t)(~idx);
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const uint64_t o = __shfl_xor_sync(FULL_MASK, v, j);
+      const bool asc = (lane & (uint32_t)k) == 0;
+      const bool lower = (lane & (uint32_t)j) == 0;
+      // an ascending network with every choice flipped sorts descending
+      const bool take_max = (lower == asc);
+      v = take_max ? (v > o ? v : o) : (v < o ? v : o);
+    }
+  }
+  key = (uint32_t)(v >> 32);
+  idx = ~(uint32_t)v;
+}
+
+// --------------------------------------------------------------- emission
+// Warp-aggregated append of one index per flagged lane to the row's output.
+// Every lane of the warp must call.
+__device__ __forceinline__ void warp_emit(int32_t* out, int32_t K, uint32_t idx, bool flag,
+                                          Shared& S, uint32_t& lflags) {
+  const uint32_t m = __ballot_sync(FULL_MASK, flag);
+  if (m == 0) return;
+  const uint32_t lane = lane_id();
+  const uint32_t leader = __ffs(m) - 1;
+  uint32_t base = 0;
+  if (lane == leader) base = atomicAdd(&S.nout, (uint32_t)__popc(m));
+  base = __shfl_sync(FULL_MASK, base, leader);
+  if (flag) {
+    const uint32_t pos = base + __popc(m & ((1u << lane) - 1u));
+    if (pos < (uint32_t)K) out[pos] = (int32_t)idx;
+    else lflags |= F_INTERNAL;
+  }
+}
+
+// ------------------------------------------------------------- the TMA ring
+// A 3-stage ring of 16 KB shared-memory stages filled by 1-D bulk copies.
+// Warp 0, lane 0 produces; warps 1..15 consume.  Every thread keeps the same
+// chunk sequence number, so passes can follow one another without resetting
+// the barriers.
+struct Ring {
+  float* buf;
+  uint64_t* full;
+  uint64_t* empty;
+  uint32_t seq;
+  uint64_t policy;
+};
+
+__device__ __forceinline__ void ring_init(Ring& R, Shared& S, float* buf) {
+  R.buf = buf;
+  R.full = S.full;
+  R.empty = S.empty;
+  R.seq = 0;
+  R.policy = l2_policy_evict_first();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], CONSUMER_WARPS);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+}
+
+// Streams elements [start, end) of `row` through the ring and calls
+// f.quad(i0, float4, valid_mask) on the consumer warps, warp-uniformly, for
+// every group of up to four consecutive elements (element i0 + e is lane e of
+// the float4, valid when bit e of the mask is set).  The 16-byte aligned body
+// goes through bulk copies; the unaligned head and tail (< 4 elements each)
+// are read directly.  The caller synchronises the block afterwards.
+template <class F>
+__device__ __forceinline__ void ring_pass(Ring& R, const float* __restrict__ row, int64_t start,
+                                          int64_t end, F& f, uint32_t& lflags) {
+  const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31u;
+  if (end <= start) return;
+  const uintptr_t addr = reinterpret_cast<uintptr_t>(row + start);
+  int64_t a0 = start + (int64_t)(((16u - (uint32_t)(addr & 15u)) & 15u) >> 2);
+  if (a0 > end) a0 = end;
+  const int64_t a1 = a0 + ((end - a0) & ~(int64_t)3);
+  const uint32_t nchunks = (uint32_t)((a1 - a0 + CHUNK_FLOATS - 1) / CHUNK_FLOATS);
+  if (warp == 0) {
+    if (lane == 0) {
+      for (uint32_t c = 0; c < nchunks; ++c) {
+        const uint32_t q = R.seq + c, s = q % STAGES, use = q / STAGES;
+        if (!mbar_wait(&R.empty[s], (use & 1u) ^ 1u)) lflags |= F_TIMEOUT;
+        const int64_t off = a0 + (int64_t)c * CHUNK_FLOATS;
+        const int64_t n = (a1 - off) < CHUNK_FLOATS ? (a1 - off) : CHUNK_FLOATS;
+        const uint32_t bytes = (uint32_t)(n * 4);
+        fence_proxy_async();
+        mbar_arrive_expect_tx(&R.full[s], bytes);
+        bulk_load(R.buf + (size_t)s * CHUNK_FLOATS, row + off, bytes, &R.full[s], R.policy);
+      }
+    }
+  } else {
+    if (warp == 1) {
+      // head [start, a0) on lanes 0..2, tail [a1, end) on lanes 4..6
+      const int64_t nh = a0 - start, nt = end - a1;
+      int64_t i = -1;
+      if ((int64_t)lane < nh) i = start + lane;
+      else if (lane >= 4 && (int64_t)lane - 4 < nt) i = a1 + (lane - 4);
+      const float v = (i >= 0) ? row[i] : 0.0f;
+      f.quad(i >= 0 ? i : 0, make_float4(v, 0.f, 0.f, 0.f), i >= 0 ? 1u : 0u);
+    }
+    const uint32_t ct = tid - 32;
+    for (uint32_t c = 0; c < nchunks; ++c) {
+      const uint32_t q = R.seq + c, s = q % STAGES, use = q / STAGES;
+      if (!mbar_wait(&R.full[s], use & 1u)) lflags |= F_TIMEOUT;
+      const int64_t off = a0 + (int64_t)c * CHUNK_FLOATS;
+      const int64_t n = (a1 - off) < CHUNK_FLOATS ? (a1 - off) : CHUNK_FLOATS;
+      const int nf4 = (int)(n >> 2);
+      const float4* sm4 = reinterpret_cast<const float4*>(R.buf + (size_t)s * CHUNK_FLOATS);
+      const int iters = (nf4 + CONSUMERS - 1) / CONSUMERS;
+      for (int it = 0; it < iters; ++it) {
+        const int j = (int)ct + it * CONSUMERS;
+        const bool ok = j < nf4;
+        const float4 v = ok ? sm4[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+        f.quad(off + 4 * (int64_t)j, v, ok ? 0xfu : 0u);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&R.empty[s]);
+    }
+  }
+  R.seq += nchunks;
+}
+
+// ------------------------------------------------- certify + collect (stage 2)
+// Admission: key(v) >= key(tau1).  When tau1 > +0 the signed comparison of
+// the raw bits gives the same answer in one instruction (POS = true).
+template <bool POS>
+struct ScanCollect {
+  uint32_t t1;      // POS: bits of tau1; otherwise key(tau1)
+  uint32_t key0;
+  Bins bins;
+  uint2* cand;
+  uint32_t* hist;
+  uint32_t* ncand;
+  uint32_t c0;
+
+  __device__ __forceinline__ bool admit(float x) const {
+    if (POS) return (int32_t)__float_as_uint(x) >= (int32_t)t1;
+    return fkey(x) >= t1;
+  }
+
+  __device__ __forceinline__ void quad(int64_t i0, float4 v, uint32_t vm) {
+    uint32_t m = (admit(v.x) ? 1u : 0u) | (admit(v.y) ? 2u : 0u) | (admit(v.z) ? 4u : 0u) |
+                 (admit(v.w) ? 8u : 0u);
+    m &= vm;
+    if (__any_sync(FULL_MASK, m != 0)) slow(i0, v, m);
+  }
+
+  __device__ __forceinline__ void slow(int64_t i0, float4 v, uint32_t m) {
+    const uint32_t lane = lane_id();
+    const uint32_t cnt = (uint32_t)__popc(m);
+    const uint32_t incl = warp_incl_scan(cnt);
+    const uint32_t total = __shfl_sync(FULL_MASK, incl, 31);
+    uint32_t base = 0;
+    if (lane == 31 && total) base = atomicAdd(ncand, total);
+    base = __shfl_sync(FULL_MASK, base, 31);
+    uint32_t pos = base + incl - cnt;
+    const float vals[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (m & (1u << e)) {
+        const uint32_t k = fkey(vals[e]);
+        c0 += (k >= key0) ? 1u : 0u;
+        atomicAdd(&hist[bins.digit(k)], 1u);
+        if (pos < (uint32_t)CAP) cand[pos] = make_uint2((uint32_t)(i0 + e), k);
+        ++pos;
+      }
+    }
+  }
+};
+
+// ------------------------------------------------ frontier refinement engine
+enum PassMode : uint32_t { TAKE_ALL = 0, TAKE_SOME = 1, SMALL_SORT = 2, COLLECT = 3, NEXT_HIST = 4 };
+
+// Per-element work of one refinement pass.  The frontier is the keys in
+// [bins.lo, bins.hi]; keys above the boundary bin [nlo, nhi] are emitted, keys
+// inside it are handled by the mode.
+struct PassF {
+  Bins bins;
+  uint32_t nlo, nhi;
+  uint32_t mode;
+  Bins nb;
+  uint32_t Kr;
+  Shared* S;
+  uint32_t* hist;
+  uint2* cand;
+  int32_t* out;
+  int32_t K;
+  uint32_t fl;
+
+  __device__ __forceinline__ void elem(uint32_t idx, uint32_t key, bool valid) {
+    const bool inF = valid && key >= bins.lo && key <= bins.hi;
+    const bool up = inF && key > nhi;
+    const bool inb = inF && !up && key >= nlo;
+    bool em = up;
+    if (inb) {
+      if (mode == TAKE_ALL) {
+        em = true;
+      } else if (mode == TAKE_SOME) {
+        em = atomicAdd(&S->take, 1u) < Kr;
+      } else if (mode == SMALL_SORT) {
+        const uint32_t t = atomicAdd(&S->small_n, 1u);
+        if (t < (uint32_t)SMALL) S->small[t] = make_uint2(idx, key);
+      } else if (mode == COLLECT) {
+        const uint32_t t = atomicAdd(&S->ncand, 1u);
+        if (t < (uint32_t)CAP) cand[t] = make_uint2(idx, key);
+        atomicAdd(&hist[nb.digit(key)], 1u);
+      } else {
+        atomicAdd(&hist[nb.digit(key)], 1u);
+      }
+    }
+    warp_emit(out, K, idx, em, *S, fl);
+  }
+
+  __device__ __forceinline__ void quad(int64_t i0, float4 v, uint32_t vm) {
+    elem((uint32_t)i0, fkey(v.x), (vm & 1u) != 0);
+    elem((uint32_t)(i0 + 1), fkey(v.y), (vm & 2u) != 0);
+    elem((uint32_t)(i0 + 2), fkey(v.z), (vm & 4u) != 0);
+    elem((uint32_t)(i0 + 3), fkey(v.w), (vm & 8u) != 0);
+  }
+};
+
+// Histogram of the keys in [bins.lo, bins.hi] (no emission).
+struct HistF {
+  Bins bins;
+  uint32_t* hist;
+  __device__ __forceinline__ void elem(uint32_t, uint32_t key, bool valid) {
+    if (valid && key >= bins.lo && key <= bins.hi) atomicAdd(&hist[bins.digit(key)], 1u);
+  }
+  __device__ __forceinline__ void quad(int64_t i0, float4 v, uint32_t vm) {
+    elem(0, fkey(v.x), (vm & 1u) != 0);
+    elem(0, fkey(v.y), (vm & 2u) != 0);
+    elem(0, fkey(v.z), (vm & 4u) != 0);
+    elem(0, fkey(v.w), (vm & 8u) != 0);
+  }
+};
+
+// Sources the refinement loop can iterate.  for_each() calls f.elem (or
+// f.quad) warp-uniformly; the caller synchronises the block afterwards.
+struct CandSrc {  // (idx, key) entries in shared memory
+  static constexpr bool kRow = false;
+  const uint2* cand;
+  uint32_t n;
+  template <class F>
+  __device__ __forceinline__ void for_each(F& f, uint32_t&) const {
+    const uint32_t iters = (n + THREADS - 1) / THREADS;
+    for (uint32_t it = 0; it < iters; ++it) {
+      const uint32_t j = threadIdx.x + it * THREADS;
+      const bool ok = j < n;
+      const uint2 e = ok ? cand[j] : make_uint2(0u, 0u);
+      f.elem(e.x, e.y, ok);
+    }
+  }
+};
+
+struct StagedSrc {  // a whole row staged in shared memory; element i at buf[i]
+  static constexpr bool kRow = false;
+  const float* buf;
+  uint32_t n;
+  template <class F>
+  __device__ __forceinline__ void for_each(F& f, uint32_t&) const {
+    const uint32_t iters = (n + THREADS - 1) / THREADS;
+    for (uint32_t it = 0; it < iters; ++it) {
+      const uint32_t j = threadIdx.x + it * THREADS;
+      const bool ok = j < n;
+      const uint32_t k = ok ? fkey(buf[j]) : 0u;
+      f.elem(j, k, ok);
+    }
+  }
+};
+
+struct RowSrc {  // a row in global memory, streamed through the ring
+  static constexpr bool kRow = true;
+  Ring* R;
+  const float* row;
+  int64_t len;
+  template <class F>
+  __device__ __forceinline__ void for_each(F& f, uint32_t& lflags) const {
+    ring_pass(*R, row, 0, len, f, lflags);
+  }
+};
+
+// Exact selection of Kp keys from the frontier of `src` (keys in
+// [bins.lo, bins.hi]), given `hist`, the complete histogram of that frontier
+// under `bins`.  Emits into out[] through S.nout.  Every thread must call.
+template <class Src>
+__device__ void refine(const Src& src, Bins bins, uint32_t Kp, uint32_t* hist, uint2* cand,
+                       int32_t* out, int32_t K, Shared& S, uint32_t& lflags) {
+  for (int guard = 0; guard < 40; ++guard) {
+    __syncthreads();
+    find_boundary(hist, Kp, S);
+    if (!S.ok) {
+      lflags |= F_INTERNAL;
+      return;
+    }
+    const uint32_t b = S.b, above = S.above, hb = hist[b];
+    const uint32_t Kr = Kp - above;
+    const uint32_t nlo = bins.bin_lo(b), nhi = bins.bin_hi(b);
+    uint32_t mode;
+    if (hb == Kr) mode = TAKE_ALL;
+    else if (nlo == nhi) mode = TAKE_SOME;
+    else if (hb <= (uint32_t)SMALL) mode = SMALL_SORT;
+    else if (Src::kRow && hb <= (uint32_t)CAP) mode = COLLECT;
+    else mode = NEXT_HIST;
+    const Bins nb = make_bins(nlo, nhi);
+    __syncthreads();  // every thread has read hist[b]
+    if (mode == NEXT_HIST || mode == COLLECT) clear_hist(hist);
+    if (threadIdx.x == 0) {
+      S.take = 0;
+      S.small_n = 0;
+      S.ncand = 0;
+    }
+    __syncthreads();
+    PassF f{bins, nlo, nhi, mode, nb, Kr, &S, hist, cand, out, K, 0u};
+    src.for_each(f, lflags);
+    lflags |= f.fl;
+    __syncthreads();
+    if (mode == TAKE_ALL || mode == TAKE_SOME) return;
+    if (mode == SMALL_SORT) {
+      if ((threadIdx.x >> 5) == 0) {
+        const uint32_t n = min(S.small_n, (uint32_t)SMALL);
+        const uint32_t lane = lane_id();
+        uint32_t key = 0, idx = 0xffffffffu;
+        if (lane < n) {
+          key = S.small[lane].y;
+          idx = S.small[lane].x;
+        }
+        warp_sort_desc(key, idx);
+        const bool em = lane < Kr && idx != 0xffffffffu;
+        warp_emit(out, K, idx, em, S, lflags);
+      }
+      __syncthreads();
+      return;
+    }
+    if constexpr (Src::kRow) {
+      if (mode == COLLECT) {
+        const CandSrc cs{cand, min(S.ncand, (uint32_t)CAP)};
+        refine(cs, nb, Kr, hist, cand, out, K, S, lflags);
+        return;
+      }
+    }
+    bins = nb;
+    Kp = Kr;
+  }
+  lflags |= F_INTERNAL;
+}
+
+// ------------------------------------------------------------ sampler (stage 1)
+struct SampleSmem {
+  const uint32_t* keys;
+  __device__ __forceinline__ uint32_t operator()(int64_t i) const { return keys[i]; }
+};
+struct SampleGlobal {
+  const float* row;
+  int64_t stride;
+  uint64_t policy;
+  __device__ __forceinline__ uint32_t operator()(int64_t i) const {
+    return fkey(ld_keep(row + i * stride, policy));
+  }
+};
+
+// r-th largest key (1-based) among get(0..n-1), known to lie in [lo, hi]
+// with at least r keys >= lo.  Every thread must call.
+template <class G>
+__device__ uint32_t select_rank(const G& get, int64_t n, uint32_t r, uint32_t lo, uint32_t hi,
+                                uint32_t* hist, Shared& S) {
+  uint32_t rem = r;
+  for (int round = 0; round < 6; ++round) {
+    if (lo == hi) return lo;
+    const Bins bn = make_bins(lo, hi);
+    __syncthreads();
+    clear_hist(hist);
+    __syncthreads();
+    for (int64_t i = threadIdx.x; i < n; i += THREADS) {
+      const uint32_t k = get(i);
+      if (k >= lo && k <= hi) atomicAdd(&hist[bn.digit(k)], 1u);
+    }
+    __syncthreads();
+    find_boundary(hist, rem, S);
+    if (!S.ok) return lo;  // cannot happen for a consistent source
+    const uint32_t b = S.b, hb = hist[b];
+    rem -= S.above;
+    const uint32_t nlo = bn.bin_lo(b), nhi = bn.bin_hi(b);
+    if (hb <= (uint32_t)SMALL && nlo != nhi) {
+      __syncthreads();
+      if (threadIdx.x == 0) S.small_n = 0;
+      __syncthreads();
+      for (int64_t i = threadIdx.x; i < n; i += THREADS) {
+        const uint32_t k = get(i);
+        if (k >= nlo && k <= nhi) {
+          const uint32_t t = atomicAdd(&S.small_n, 1u);
+          if (t < (uint32_t)SMALL) S.small[t] = make_uint2(0u, k);
+        }
+      }
+      __syncthreads();
+      if ((threadIdx.x >> 5) == 0) {
+        const uint32_t lane = lane_id();
+        const uint32_t m = min(S.small_n, (uint32_t)SMALL);
+        uint32_t key = lane < m ? S.small[lane].y : 0u, idx = lane;
+        warp_sort_desc(key, idx);
+        if (lane == rem - 1) S.res = key;
+      }
+      __syncthreads();
+      return S.res;
+    }
+    lo = nlo;
+    hi = nhi;
+  }
+  return lo;
+}
+
+// Stage 1.  Samples at 0, s, 2s, ... < len; tau_j = r_j-th largest sample
+// with r_j = clamp(ceil(T_j * n_s / len), 1, n_s).  Leaves key0/key1 and the
+// sample key range in S.  Every thread must call.
+__device__ void sample_thresholds(const float* __restrict__ row, int64_t len, int32_t stride,
+                                  uint32_t T0, uint32_t T1, uint32_t* skeys, uint32_t* hist,
+                                  Shared& S) {
+  const int64_t ns = (len + stride - 1) / stride;
+  int64_t r0 = ((int64_t)T0 * ns + len - 1) / len;
+  int64_t r1 = ((int64_t)T1 * ns + len - 1) / len;
+  r0 = r0 < 1 ? 1 : (r0 > ns ? ns : r0);
+  r1 = r1 < 1 ? 1 : (r1 > ns ? ns : r1);
+  const uint64_t pol = l2_policy_evict_last();
+  const bool on_chip = ns <= SAMPLE_SMEM;
+  uint32_t mn = 0xffffffffu, mx = 0u;
+  constexpr int U = 8;
+  for (int64_t i0 = threadIdx.x; i0 < ns; i0 += (int64_t)THREADS * U) {
+    float v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t i = i0 + (int64_t)u * THREADS;
+      v[u] = (i < ns) ? ld_keep(row + i * stride, pol) : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t i = i0 + (int64_t)u * THREADS;
+      if (i < ns) {
+        const uint32_t k = fkey(v[u]);
+        if (on_chip) skeys[i] = k;
+        mn = min(mn, k);
+        mx = max(mx, k);
+      }
+    }
+  }
+  uint32_t kmin, kmax;
+  block_minmax(mn, mx, S, &kmin, &kmax);
+  uint32_t key1, key0;
+  if (on_chip) {
+    const SampleSmem g{skeys};
+    key1 = select_rank(g, ns, (uint32_t)r1, kmin, kmax, hist, S);
+    key0 = select_rank(g, ns, (uint32_t)r0, key1, kmax, hist, S);
+  } else {
+    const SampleGlobal g{row, stride, pol};
+    key1 = select_rank(g, ns, (uint32_t)r1, kmin, kmax, hist, S);
+    key0 = select_rank(g, ns, (uint32_t)r0, key1, kmax, hist, S);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    S.key0 = key0;
+    S.key1 = key1;
+    S.kmin = kmin;
+    S.kmax = kmax;
+  }
+  __syncthreads();
+}
+
+// Seeded bins of the full-row pass: the candidates' keys start at key(tau1);
+// the regular bins span up to the largest sample, the top bin takes the rest.
+__device__ __forceinline__ Bins scan_bins(uint32_t key1, uint32_t kmax) {
+  return make_bins_focus(key1, 0xffffffffu, key1, kmax);
+}
+
+// Bins of the first recovery pass: the frontier is every key below key(tau1);
+// the regular bins start at the smallest sample.
+__device__ __forceinline__ Bins recovery_bins(uint32_t key1, uint32_t kmin) {
+  const uint32_t hi = key1 - 1u;
+  return make_bins_focus(0u, hi, kmin, hi);
+}
+
+__device__ __forceinline__ void write_sentinel_row(int32_t* out, int32_t K, int64_t len) {
+  for (int32_t i = threadIdx.x; i < K; i += THREADS) out[i] = (i < len) ? i : -1;
+}
+
+}  // namespace tk

@@ -1,0 +1,536 @@
+// Kernels of the sample-guided exact Top-K selector and their launchers.
+//
+// Three execution paths (arxivdaily abstract of "Sample-Guided Exact Top-K
+// Selection for Long-Context Sparse Attention"; PaperDaily walkthrough,
+// section 问题二, last paragraphs):
+//   * direct     -- one CTA per row; the whole row is staged on chip with bulk
+//                   copies and selected exactly there (short rows, where the
+//                   codexqa.cn width sweep found an exact boundary beats
+//                   sampling);
+//   * persistent -- long-lived CTAs pull whole rows from a queue and run
+//                   sample -> certify+collect -> refine / recover per row;
+//   * KV-split   -- few very long rows: a prepare kernel samples each row, then
+//                   several CTAs scan disjoint segments of one score row and
+//                   merge counts, candidates and histograms in global memory;
+//                   the last CTA of a row to finish (an atomic ticket, nobody
+//                   waits) runs the exact refinement.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdio>
+
+#include "topk_device.cuh"
+#include "topk_launch.h"
+
+namespace tk {
+
+__device__ uint32_t g_status;  // OR of row flags since the last read
+
+// ------------------------------------------------------- shared-memory plan
+constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+constexpr size_t SH_HDR = align_up(sizeof(Shared), 128);
+constexpr size_t SH_RING = SH_HDR;
+constexpr size_t SH_CAND = SH_RING + (size_t)STAGES * CHUNK_BYTES;
+constexpr size_t SH_HIST = SH_CAND + (size_t)CAP * sizeof(uint2);
+constexpr size_t SH_ROW_TOTAL = SH_HIST + (size_t)NB * sizeof(uint32_t);
+
+// KV-split per-row state in the workspace.
+struct KvHdr {
+  uint32_t mode;  // 0 sentinel, 1 exact without sampling, 2 sampled
+  uint32_t len;
+  uint32_t key0, key1, kmin, kmax;
+  uint32_t c0, ncand, ticket, ovf, flags;
+  float tau0, tau1;
+};
+constexpr size_t KV_HIST_OFF = 256;
+constexpr size_t KV_CAND_OFF = KV_HIST_OFF + (size_t)NB * sizeof(uint32_t);
+constexpr size_t KV_ROW_BYTES = align_up(KV_CAND_OFF + (size_t)CAP * sizeof(uint2), 256);
+static_assert(sizeof(KvHdr) <= KV_HIST_OFF, "KV row header too large");
+
+struct RowCarve {
+  Shared* S;
+  float* ring;
+  uint2* cand;
+  uint32_t* hist;
+};
+
+__device__ __forceinline__ RowCarve carve(uint8_t* smem) {
+  RowCarve c;
+  c.S = reinterpret_cast<Shared*>(smem);
+  c.ring = reinterpret_cast<float*>(smem + SH_RING);
+  c.cand = reinterpret_cast<uint2*>(smem + SH_CAND);
+  c.hist = reinterpret_cast<uint32_t*>(smem + SH_HIST);
+  return c;
+}
+
+__device__ __forceinline__ int64_t clamp_len(int32_t raw, int64_t n_alloc, uint32_t& fl) {
+  int64_t v = raw;
+  if (v < 0) {
+    v = 0;
+    fl |= F_LEN_CLAMPED;
+  }
+  if (v > n_alloc) {
+    v = n_alloc;
+    fl |= F_LEN_CLAMPED;
+  }
+  return v;
+}
+
+// Closes a row: pads a short output (only after an internal failure), folds
+// the per-thread flags and writes the diagnostics.  Every thread must call.
+__device__ void finish_row(Shared& S, int32_t* out, int32_t K, uint32_t lflags, RowDiag* diag,
+                           int64_t r, int32_t path, float tau0, float tau1, uint32_t c0,
+                           uint32_t c1) {
+  __syncthreads();
+  const uint32_t nout = S.nout;
+  if (nout != (uint32_t)K) {
+    lflags |= F_INTERNAL;
+    for (uint32_t i = min(nout, (uint32_t)K) + threadIdx.x; i < (uint32_t)K; i += THREADS)
+      out[i] = -1;
+  }
+  if (lflags) atomicOr(&S.flags, lflags);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t fl = S.flags;
+    if (fl) atomicOr(&g_status, fl);
+    if (diag) {
+      RowDiag d;
+      d.tau0 = tau0;
+      d.tau1 = tau1;
+      d.count0 = c0;
+      d.count1 = c1;
+      d.path = path;
+      d.flags = fl;
+      diag[r] = d;
+    }
+    S.flags = 0;
+  }
+  __syncthreads();
+}
+
+// Exact selection without sampling, streaming the row from global memory:
+// one histogram pass over the whole key range, then refinement passes.
+__device__ void exact_row_stream(const float* row, int64_t len, int32_t* out, int32_t K, Ring& R,
+                                 const RowCarve& c, uint32_t& lflags) {
+  Shared& S = *c.S;
+  const Bins bins = make_bins(0u, 0xffffffffu);
+  __syncthreads();
+  clear_hist(c.hist);
+  __syncthreads();
+  HistF hf{bins, c.hist};
+  ring_pass(R, row, 0, len, hf, lflags);
+  __syncthreads();
+  refine(RowSrc{&R, row, len}, bins, (uint32_t)K, c.hist, c.cand, out, K, S, lflags);
+}
+
+// The full-row certify+collect pass over [s0, s1) with thresholds in S.
+__device__ uint32_t scan_collect(const float* row, int64_t s0, int64_t s1, Ring& R,
+                                 const RowCarve& c, uint32_t key0, uint32_t key1, const Bins& sb,
+                                 uint32_t& lflags) {
+  Shared& S = *c.S;
+  const float tau1 = key_to_float(key1);
+  uint32_t c0 = 0;
+  if (tau1 > 0.0f) {
+    ScanCollect<true> f{__float_as_uint(tau1), key0, sb, c.cand, c.hist, &S.ncand, 0u};
+    ring_pass(R, row, s0, s1, f, lflags);
+    c0 = f.c0;
+  } else {
+    ScanCollect<false> f{key1, key0, sb, c.cand, c.hist, &S.ncand, 0u};
+    ring_pass(R, row, s0, s1, f, lflags);
+    c0 = f.c0;
+  }
+  __syncthreads();
+  return block_sum(c0, S);
+}
+
+// Everything after the full-row pass of a sampled row whose candidates,
+// histogram and counts are on chip: refine, or re-read on overflow, or
+// recover.  Returns the row path.
+__device__ int32_t select_after_scan(const float* row, int64_t len, int32_t* out, int32_t K,
+                                     Ring& R, const RowCarve& c, uint32_t C0, uint32_t C1,
+                                     bool overflow, uint32_t key1, uint32_t kmin, const Bins& sb,
+                                     uint32_t& lflags) {
+  Shared& S = *c.S;
+  const int32_t path = (C0 >= (uint32_t)K) ? PATH_TAU0 : (C1 >= (uint32_t)K ? PATH_TAU1 : PATH_RECOVERY);
+  if (C1 >= (uint32_t)K && !overflow) {
+    refine(CandSrc{c.cand, C1}, sb, (uint32_t)K, c.hist, c.cand, out, K, S, lflags);
+  } else if (C1 >= (uint32_t)K) {
+    // More admitted scores than the on-chip buffer holds.  The histogram is
+    // complete, so the refinement re-reads the row for the boundary bin only.
+    lflags |= F_OVERFLOW;
+    refine(RowSrc{&R, row, len}, sb, (uint32_t)K, c.hist, c.cand, out, K, S, lflags);
+  } else {
+    // C(tau1) < K: every admitted score belongs to the answer; the remaining
+    // K - C(tau1) come from the scores below tau1, selected exactly from the
+    // whole row.
+    lflags |= F_RECOVERY;
+    if (key1 == 0u) {
+      lflags |= F_INTERNAL;
+      return path;
+    }
+    const uint32_t iters = (C1 + THREADS - 1) / THREADS;
+    for (uint32_t it = 0; it < iters; ++it) {
+      const uint32_t j = threadIdx.x + it * THREADS;
+      const bool ok = j < C1;
+      warp_emit(out, K, ok ? c.cand[j].x : 0u, ok, S, lflags);
+    }
+    const Bins rb = recovery_bins(key1, kmin);
+    __syncthreads();
+    clear_hist(c.hist);
+    __syncthreads();
+    HistF hf{rb, c.hist};
+    ring_pass(R, row, 0, len, hf, lflags);
+    __syncthreads();
+    refine(RowSrc{&R, row, len}, rb, (uint32_t)K - C1, c.hist, c.cand, out, K, S, lflags);
+  }
+  return path;
+}
+
+// ------------------------------------------------------------ persistent path
+__global__ void __launch_bounds__(THREADS, 2)
+    k_persistent(const float* __restrict__ scores, const int32_t* __restrict__ row_lens,
+                 int32_t* __restrict__ out_idx, RowDiag* __restrict__ diag, uint32_t* hdr,
+                 Params P) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const RowCarve c = carve(smem);
+  Shared& S = *c.S;
+  if (threadIdx.x == 0) S.flags = 0;
+  Ring R;
+  ring_init(R, S, c.ring);
+  const int32_t K = P.K;
+  for (;;) {
+    if (threadIdx.x == 0) S.row = atomicAdd(&hdr[0], 1u);
+    __syncthreads();
+    const int64_t r = S.row;
+    __syncthreads();
+    if (r >= P.M) break;
+    uint32_t lflags = 0;
+    const int64_t len = clamp_len(row_lens[r], P.N_alloc, lflags);
+    const float* row = scores + r * P.N_alloc;
+    int32_t* out = out_idx + r * (int64_t)K;
+    if (threadIdx.x == 0) S.nout = 0;
+    __syncthreads();
+    const float qnan = __int_as_float(0x7fc00000);
+    if (len <= K) {
+      write_sentinel_row(out, K, len);
+      if (threadIdx.x == 0) S.nout = (uint32_t)K;
+      finish_row(S, out, K, lflags, diag, r, PATH_SENTINEL, qnan, qnan, 0, 0);
+      continue;
+    }
+    if (len < P.sample_min_len) {
+      exact_row_stream(row, len, out, K, R, c, lflags);
+      finish_row(S, out, K, lflags, diag, r, PATH_DIRECT, qnan, qnan, 0, 0);
+      continue;
+    }
+    sample_thresholds(row, len, P.stride, P.target0, P.target1,
+                      reinterpret_cast<uint32_t*>(c.cand), c.hist, S);
+    const uint32_t key0 = S.key0, key1 = S.key1, kmin = S.kmin, kmax = S.kmax;
+    const Bins sb = scan_bins(key1, kmax);
+    __syncthreads();
+    clear_hist(c.hist);
+    if (threadIdx.x == 0) S.ncand = 0;
+    __syncthreads();
+    const uint32_t C0 = scan_collect(row, 0, len, R, c, key0, key1, sb, lflags);
+    const uint32_t C1 = S.ncand;
+    __syncthreads();
+    const int32_t path = select_after_scan(row, len, out, K, R, c, C0, C1, C1 > (uint32_t)CAP,
+                                           key1, kmin, sb, lflags);
+    finish_row(S, out, K, lflags, diag, r, path, key_to_float(key0), key_to_float(key1), C0, C1);
+  }
+  // The last CTA to leave resets the queue, so the next launch (or graph
+  // replay) starts from zero without a separate memset.
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(&hdr[1], 1u) == gridDim.x - 1) {
+      atomicExch(&hdr[0], 0u);
+      atomicExch(&hdr[1], 0u);
+      __threadfence();
+    }
+  }
+}
+
+// ---------------------------------------------------------------- direct path
+__global__ void __launch_bounds__(THREADS, 1)
+    k_direct(const float* __restrict__ scores, const int32_t* __restrict__ row_lens,
+             int32_t* __restrict__ out_idx, RowDiag* __restrict__ diag, Params P) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  Shared& S = *reinterpret_cast<Shared*>(smem);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem + SH_HDR);
+  float* stage = reinterpret_cast<float*>(smem + SH_HDR + (size_t)NB * sizeof(uint32_t));
+  const int64_t r = blockIdx.x;
+  const int32_t K = P.K;
+  uint32_t lflags = 0;
+  const int64_t len = clamp_len(row_lens[r], P.N_alloc, lflags);
+  const float* row = scores + r * P.N_alloc;
+  int32_t* out = out_idx + r * (int64_t)K;
+  const float qnan = __int_as_float(0x7fc00000);
+  if (threadIdx.x == 0) {
+    S.flags = 0;
+    S.nout = 0;
+  }
+  __syncthreads();
+  if (len <= K) {
+    write_sentinel_row(out, K, len);
+    if (threadIdx.x == 0) S.nout = (uint32_t)K;
+    finish_row(S, out, K, lflags, diag, r, PATH_SENTINEL, qnan, qnan, 0, 0);
+    return;
+  }
+  // Stage the row: the 16-byte aligned body by bulk copies, head and tail
+  // singly.  Element i lives at buf[i] with buf = stage + sh, where sh makes
+  // the body's first element land on a 16-byte boundary.
+  const uintptr_t addr = reinterpret_cast<uintptr_t>(row);
+  int64_t a0 = (int64_t)(((16u - (uint32_t)(addr & 15u)) & 15u) >> 2);
+  if (a0 > len) a0 = len;
+  const int64_t a1 = a0 + ((len - a0) & ~(int64_t)3);
+  const int64_t sh = (4 - (a0 & 3)) & 3;
+  float* buf = stage + sh;
+  if (threadIdx.x == 0) {
+    mbar_init(&S.full[0], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint64_t pol = l2_policy_evict_first();
+    const uint32_t bytes = (uint32_t)((a1 - a0) * 4);
+    mbar_arrive_expect_tx(&S.full[0], bytes);
+    constexpr uint32_t PIECE = 32768;
+    for (uint32_t o = 0; o < bytes; o += PIECE) {
+      const uint32_t nb = (bytes - o) < PIECE ? (bytes - o) : PIECE;
+      bulk_load(reinterpret_cast<uint8_t*>(buf + a0) + o,
+                reinterpret_cast<const uint8_t*>(row + a0) + o, nb, &S.full[0], pol);
+    }
+  }
+  for (int64_t i = threadIdx.x; i < a0; i += THREADS) buf[i] = row[i];
+  for (int64_t i = a1 + threadIdx.x; i < len; i += THREADS) buf[i] = row[i];
+  if (!mbar_wait(&S.full[0], 0)) lflags |= F_TIMEOUT;
+  __syncthreads();
+  // Exact boundary over the staged keys: data-relative bins over [min, max].
+  uint32_t mn = 0xffffffffu, mx = 0u;
+  for (int64_t i = threadIdx.x; i < len; i += THREADS) {
+    const uint32_t k = fkey(buf[i]);
+    mn = min(mn, k);
+    mx = max(mx, k);
+  }
+  uint32_t kmin, kmax;
+  block_minmax(mn, mx, S, &kmin, &kmax);
+  const Bins bins = make_bins(kmin, kmax);
+  clear_hist(hist);
+  __syncthreads();
+  const StagedSrc src{buf, (uint32_t)len};
+  HistF hf{bins, hist};
+  src.for_each(hf, lflags);
+  __syncthreads();
+  refine(src, bins, (uint32_t)K, hist, nullptr, out, K, S, lflags);
+  finish_row(S, out, K, lflags, diag, r, PATH_DIRECT, qnan, qnan, 0, 0);
+}
+
+// --------------------------------------------------------------- KV-split path
+__device__ __forceinline__ KvHdr* kv_hdr(uint8_t* ws_rows, int64_t r) {
+  return reinterpret_cast<KvHdr*>(ws_rows + (size_t)r * KV_ROW_BYTES);
+}
+
+// One CTA per row: lengths, thresholds, and a fresh merge state.
+__global__ void __launch_bounds__(THREADS, 1)
+    k_kv_prepare(const float* __restrict__ scores, const int32_t* __restrict__ row_lens,
+                 uint8_t* __restrict__ ws_rows, Params P) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  Shared& S = *reinterpret_cast<Shared*>(smem);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem + SH_HDR);
+  uint32_t* skeys = hist + NB;
+  const int64_t r = blockIdx.x;
+  uint32_t lflags = 0;
+  const int64_t len = clamp_len(row_lens[r], P.N_alloc, lflags);
+  const float* row = scores + r * P.N_alloc;
+  uint8_t* base = ws_rows + (size_t)r * KV_ROW_BYTES;
+  KvHdr* h = reinterpret_cast<KvHdr*>(base);
+  uint32_t* ghist = reinterpret_cast<uint32_t*>(base + KV_HIST_OFF);
+  for (int i = threadIdx.x; i < NB; i += THREADS) ghist[i] = 0;
+  uint32_t mode = 2;
+  if (len <= P.K) mode = 0;
+  else if (len < P.sample_min_len) mode = 1;
+  uint32_t key0 = 0, key1 = 0, kmin = 0, kmax = 0;
+  if (mode == 2) {
+    sample_thresholds(row, len, P.stride, P.target0, P.target1, skeys, hist, S);
+    key0 = S.key0;
+    key1 = S.key1;
+    kmin = S.kmin;
+    kmax = S.kmax;
+  }
+  if (threadIdx.x == 0) {
+    h->mode = mode;
+    h->len = (uint32_t)len;
+    h->key0 = key0;
+    h->key1 = key1;
+    h->kmin = kmin;
+    h->kmax = kmax;
+    h->c0 = 0;
+    h->ncand = 0;
+    h->ticket = 0;
+    h->ovf = 0;
+    h->flags = lflags;
+    h->tau0 = key_to_float(key0);
+    h->tau1 = key_to_float(key1);
+  }
+}
+
+__global__ void __launch_bounds__(THREADS, 2)
+    k_kv_segment(const float* __restrict__ scores, int32_t* __restrict__ out_idx,
+                 RowDiag* __restrict__ diag, uint8_t* __restrict__ ws_rows, Params P) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const RowCarve c = carve(smem);
+  Shared& S = *c.S;
+  const int64_t item = blockIdx.x;
+  const int64_t r = item / P.segments;
+  const int32_t seg = (int32_t)(item % P.segments);
+  uint8_t* base = ws_rows + (size_t)r * KV_ROW_BYTES;
+  KvHdr* h = reinterpret_cast<KvHdr*>(base);
+  uint32_t* ghist = reinterpret_cast<uint32_t*>(base + KV_HIST_OFF);
+  uint2* gcand = reinterpret_cast<uint2*>(base + KV_CAND_OFF);
+  const uint32_t mode = h->mode;
+  const int64_t len = h->len;
+  const uint32_t key0 = h->key0, key1 = h->key1, kmin = h->kmin, kmax = h->kmax;
+  const float* row = scores + r * P.N_alloc;
+  const int32_t K = P.K;
+  if (threadIdx.x == 0) {
+    S.flags = 0;
+    S.nout = 0;
+  }
+  Ring R;
+  ring_init(R, S, c.ring);
+  uint32_t lflags = 0;
+  const Bins sb = scan_bins(key1, kmax);
+  if (mode == 2) {
+    const int64_t s0 = len * seg / P.segments, s1 = len * (seg + 1) / P.segments;
+    clear_hist(c.hist);
+    if (threadIdx.x == 0) S.ncand = 0;
+    __syncthreads();
+    const uint32_t C0 = scan_collect(row, s0, s1, R, c, key0, key1, sb, lflags);
+    const uint32_t nloc = S.ncand;
+    if (threadIdx.x == 0) {
+      atomicAdd(&h->c0, C0);
+      S.res = atomicAdd(&h->ncand, nloc);
+      if (nloc > (uint32_t)CAP) atomicOr(&h->ovf, 1u);
+    }
+    __syncthreads();
+    const uint32_t gbase = S.res;
+    const uint32_t ncopy = min(nloc, (uint32_t)CAP);
+    for (uint32_t j = threadIdx.x; j < ncopy; j += THREADS) {
+      if (gbase + j < (uint32_t)CAP) gcand[gbase + j] = c.cand[j];
+    }
+    for (int i = threadIdx.x; i < NB; i += THREADS) {
+      const uint32_t v = c.hist[i];
+      if (v) atomicAdd(&ghist[i], v);
+    }
+  }
+  // Ticket: the CTA that completes the row's last segment selects it.
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const uint32_t t = atomicAdd(&h->ticket, 1u);
+    S.last = (t == (uint32_t)P.segments - 1) ? 1u : 0u;
+  }
+  __syncthreads();
+  if (!S.last) return;
+  __threadfence();
+  int32_t* out = out_idx + r * (int64_t)K;
+  const float qnan = __int_as_float(0x7fc00000);
+  lflags |= __ldcg(&h->flags);
+  if (mode == 0) {
+    write_sentinel_row(out, K, len);
+    if (threadIdx.x == 0) S.nout = (uint32_t)K;
+    finish_row(S, out, K, lflags, diag, r, PATH_SENTINEL, qnan, qnan, 0, 0);
+    return;
+  }
+  if (mode == 1) {
+    exact_row_stream(row, len, out, K, R, c, lflags);
+    finish_row(S, out, K, lflags, diag, r, PATH_DIRECT, qnan, qnan, 0, 0);
+    return;
+  }
+  const uint32_t C0 = __ldcg(&h->c0);
+  const uint32_t C1 = __ldcg(&h->ncand);
+  const bool overflow = __ldcg(&h->ovf) != 0u || C1 > (uint32_t)CAP;
+  for (int i = threadIdx.x; i < NB; i += THREADS) c.hist[i] = __ldcg(&ghist[i]);
+  const uint32_t nload = min(C1, (uint32_t)CAP);
+  for (uint32_t j = threadIdx.x; j < nload; j += THREADS) {
+    const uint2* p = gcand + j;
+    c.cand[j] = make_uint2(__ldcg(&p->x), __ldcg(&p->y));
+  }
+  __syncthreads();
+  const int32_t path =
+      select_after_scan(row, len, out, K, R, c, C0, C1, overflow, key1, kmin, sb, lflags);
+  finish_row(S, out, K, lflags, diag, r, path, key_to_float(key0), key_to_float(key1), C0, C1);
+}
+
+// ------------------------------------------------------------------ launchers
+size_t persistent_smem_bytes() { return SH_ROW_TOTAL; }
+size_t kv_segment_smem_bytes() { return SH_ROW_TOTAL; }
+size_t kv_prepare_smem_bytes() {
+  return SH_HDR + (size_t)NB * sizeof(uint32_t) + (size_t)SAMPLE_SMEM * sizeof(uint32_t);
+}
+size_t direct_smem_bytes(int64_t n_alloc) {
+  return SH_HDR + (size_t)NB * sizeof(uint32_t) + align_up((size_t)(n_alloc + 4) * 4, 16);
+}
+size_t kv_row_bytes() { return KV_ROW_BYTES; }
+
+static cudaError_t set_smem(const void* fn, size_t bytes) {
+  return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+cudaError_t prepare_device() {
+  cudaError_t e;
+  if ((e = set_smem((const void*)k_persistent, persistent_smem_bytes())) != cudaSuccess) return e;
+  if ((e = set_smem((const void*)k_kv_segment, kv_segment_smem_bytes())) != cudaSuccess) return e;
+  if ((e = set_smem((const void*)k_kv_prepare, kv_prepare_smem_bytes())) != cudaSuccess) return e;
+  int dev = 0, optin = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
+      cudaSuccess)
+    return e;
+  return set_smem((const void*)k_direct, (size_t)optin);
+}
+
+cudaError_t persistent_occupancy(int* blocks_per_sm) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k_persistent, THREADS,
+                                                       persistent_smem_bytes());
+}
+
+cudaError_t launch_direct(const float* scores, const int32_t* row_lens, int32_t* out,
+                          RowDiag* diag, const Params& P, cudaStream_t st) {
+  k_direct<<<(unsigned)P.M, THREADS, direct_smem_bytes(P.N_alloc), st>>>(scores, row_lens, out,
+                                                                       diag, P);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_persistent(const float* scores, const int32_t* row_lens, int32_t* out,
+                              RowDiag* diag, uint32_t* hdr, int grid, const Params& P,
+                              cudaStream_t st) {
+  k_persistent<<<grid, THREADS, persistent_smem_bytes(), st>>>(scores, row_lens, out, diag, hdr,
+                                                               P);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kvsplit(const float* scores, const int32_t* row_lens, int32_t* out,
+                           RowDiag* diag, uint8_t* ws_rows, const Params& P, cudaStream_t st) {
+  k_kv_prepare<<<(unsigned)P.M, THREADS, kv_prepare_smem_bytes(), st>>>(scores, row_lens,
+                                                                        ws_rows, P);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t items = P.M * (int64_t)P.segments;
+  k_kv_segment<<<(unsigned)items, THREADS, kv_segment_smem_bytes(), st>>>(scores, out, diag,
+                                                                         ws_rows, P);
+  return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_status(cudaStream_t st, uint32_t* flags) {
+  uint32_t h = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(&h, g_status, sizeof(uint32_t), 0,
+                                            cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyToSymbolAsync(g_status, &zero, sizeof(uint32_t), 0, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return e;
+  e = cudaStreamSynchronize(st);
+  *flags = h;
+  return e;
+}
+
+}  // namespace tk

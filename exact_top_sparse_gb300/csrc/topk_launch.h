@@ -1,0 +1,51 @@
+// Internal interface between the C-ABI layer and the kernels (not installed).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace tk {
+
+// Per-call parameters passed by value to every kernel.
+struct Params {
+  int64_t M;
+  int64_t N_alloc;
+  int32_t K;
+  int32_t stride;
+  uint32_t target0;  // ceil(rho0 * K)
+  uint32_t target1;  // ceil(rho1 * K)
+  int64_t sample_min_len;
+  int32_t segments;  // KV-split segments per row
+};
+
+// Same layout as topk_row_diag in the public header.
+struct RowDiag {
+  float tau0, tau1;
+  int64_t count0, count1;
+  int32_t path;
+  uint32_t flags;
+};
+
+size_t persistent_smem_bytes();
+size_t kv_segment_smem_bytes();
+size_t kv_prepare_smem_bytes();
+size_t direct_smem_bytes(int64_t n_alloc);
+size_t kv_row_bytes();
+
+// Sets the kernels' shared-memory limits on the current device.
+cudaError_t prepare_device();
+cudaError_t persistent_occupancy(int* blocks_per_sm);
+
+cudaError_t launch_direct(const float* scores, const int32_t* row_lens, int32_t* out,
+                          RowDiag* diag, const Params& P, cudaStream_t st);
+cudaError_t launch_persistent(const float* scores, const int32_t* row_lens, int32_t* out,
+                              RowDiag* diag, uint32_t* hdr, int grid, const Params& P,
+                              cudaStream_t st);
+cudaError_t launch_kvsplit(const float* scores, const int32_t* row_lens, int32_t* out,
+                           RowDiag* diag, uint8_t* ws_rows, const Params& P, cudaStream_t st);
+
+cudaError_t read_and_clear_status(cudaStream_t st, uint32_t* flags);
+
+}  // namespace tk

@@ -1,0 +1,195 @@
+/*
+ * topk.h -- sample-guided exact Top-K over ragged FP32 score rows (GB300, sm_103a).
+ *
+ * The operation: for every row r of a row-major FP32 matrix scores[M][N_alloc]
+ * with valid prefix length len_r = clamp(row_lens[r], 0, N_alloc), return the
+ * indices of the K largest scores of that prefix.  The result follows the set
+ * contract of "Sample-Guided Exact Top-K Selection for Long-Context Sparse
+ * Attention" as summarised in the codexqa.cn article "几何平均快 1.55 倍，但短行
+ * 采样会输：腾讯怎么测精确 Top-K", section "什么叫精确，时间怎么量":
+ *   - indices are distinct and lie inside [0, len_r);
+ *   - len_r > K: exactly K indices, min(selected scores) >= max(scores left
+ *     out); equal scores at the boundary may go either way; order is free;
+ *     no floating-point tolerance;
+ *   - len_r <= K: every valid index 0..len_r-1, followed by K - len_r
+ *     sentinels of value -1.
+ * The method (PaperDaily "腾讯|长上下文稀疏注意力前K精确选择", section 问题二,
+ * Fig. 4; arxivdaily abstract of the same paper): a fixed-stride sample of the
+ * current row proposes a coarse threshold tau0 and a nested, wider tau1; one
+ * mandatory full-row pass certifies C(tau0) >= K, collects the admitted
+ * candidates and seeds an FP32 radix histogram; exact radix refinement runs
+ * only over the unresolved boundary bin; the nested threshold and an exact
+ * whole-row recovery serve rows the proposal underfills.  Short rows use an
+ * exact boundary directly, long rows with few rows per call are split across
+ * CTAs (KV-split), and many rows run on persistent CTAs.
+ *
+ * Scores are compared by their IEEE order with -0.0 equal to +0.0.  NaN is not
+ * a supported score value (the library stays in bounds but the result is not
+ * specified).
+ *
+ * Conventions for every entry point below:
+ *   - "device" pointers are CUDA device (or managed) memory owned by the
+ *     caller; the library never frees or keeps them past the call's work;
+ *   - scores must be 4-byte aligned; rows start at scores + r * N_alloc and
+ *     need not be 16-byte aligned (unaligned heads/tails are read singly);
+ *   - a call never reads a score at or beyond len_r in its row;
+ *   - work is enqueued on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream) and the call returns without waiting for it, so device
+ *     memory errors surface at the caller's next synchronisation;
+ *   - the calls do no host synchronisation and read no device memory from the
+ *     host, so they can be captured in a CUDA graph once the library's
+ *     workspace for that stream exists (a call that would have to allocate
+ *     during capture returns TOPK_ERR_CAPTURE_ALLOC);
+ *   - on an error code nothing has been enqueued.
+ */
+#ifndef EXACT_TOPK_GB300_TOPK_H
+#define EXACT_TOPK_GB300_TOPK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t is `struct CUstream_st *` */
+
+typedef enum topk_status {
+  TOPK_OK = 0,
+  TOPK_ERR_ARG = -1,            /* null pointer, negative size, K < 1, size overflow */
+  TOPK_ERR_ALIGN = -2,          /* scores or out_idx not 4-byte aligned, workspace not 256-byte aligned */
+  TOPK_ERR_WORKSPACE = -3,      /* explicit workspace smaller than topk_workspace_bytes() */
+  TOPK_ERR_CUDA = -4,           /* a CUDA runtime call failed (allocation, launch, copy) */
+  TOPK_ERR_CAPTURE_ALLOC = -5,  /* the call would allocate while `stream` is capturing */
+  TOPK_ERR_UNSUPPORTED_K = -6,  /* K > TOPK_K_MAX */
+  TOPK_ERR_NO_DEVICE = -7       /* no usable sm_103 device is current */
+} topk_status;
+
+/* Largest supported K.  The sampled path is tuned for K = 2048. */
+#define TOPK_K_MAX 4096
+
+/* Per-row path identifiers reported by topk_ragged_diag(). */
+#define TOPK_PATH_SENTINEL 0 /* len <= K: 0..len-1 then -1 */
+#define TOPK_PATH_DIRECT 1   /* exact boundary without sampling (short rows) */
+#define TOPK_PATH_TAU0 2     /* C(tau0) >= K: refinement over the certified candidates */
+#define TOPK_PATH_TAU1 3     /* C(tau0) < K <= C(tau1): the nested threshold serves the row */
+#define TOPK_PATH_RECOVERY 4 /* C(tau1) < K: exact whole-row recovery */
+
+/* Bits of topk_row_diag.flags and of the device status word. */
+#define TOPK_FLAG_LEN_CLAMPED 0x1u /* row_lens[r] was outside [0, N_alloc] and was clamped */
+#define TOPK_FLAG_OVERFLOW 0x2u    /* admitted candidates exceeded the on-chip buffer; served by re-reading the row */
+#define TOPK_FLAG_RECOVERY 0x4u    /* exact whole-row recovery ran */
+#define TOPK_FLAG_INTERNAL 0x8u    /* an internal invariant failed (a library bug; the row is not valid) */
+#define TOPK_FLAG_TIMEOUT 0x10u    /* a bounded wait on an asynchronous copy gave up (the row is not valid) */
+
+/* Execution paths of the host planner (topk_plan_info.kind, topk_params.force_kind). */
+#define TOPK_KIND_AUTO 0
+#define TOPK_KIND_DIRECT 1     /* one CTA per row, the row staged on chip */
+#define TOPK_KIND_PERSISTENT 2 /* persistent CTAs pull whole rows from a queue */
+#define TOPK_KIND_KVSPLIT 3    /* several CTAs per row scan disjoint segments; the last one to finish selects */
+
+/* Per-row diagnostics written by topk_ragged_diag() (device array of M). */
+typedef struct topk_row_diag {
+  float tau0;      /* primary sampled threshold (NaN when the row was not sampled) */
+  float tau1;      /* nested secondary threshold (NaN when the row was not sampled) */
+  int64_t count0;  /* C(tau0): scores of the valid prefix >= tau0 (0 when not sampled) */
+  int64_t count1;  /* C(tau1) (0 when not sampled) */
+  int32_t path;    /* TOPK_PATH_* */
+  uint32_t flags;  /* TOPK_FLAG_* for this row */
+} topk_row_diag;
+
+/* Process-wide tuning knobs.  Sampling knobs follow the codexqa.cn section
+ * "采样不是处处都该开": stride s = 128, primary target 1.5K candidates,
+ * secondary 1.75K.  A sample rank is r = ceil(T * n_s / len) clamped to
+ * [1, n_s], with T = ceil(rho * K), n_s = ceil(len / s) and samples at
+ * positions 0, s, 2s, ... below len. */
+typedef struct topk_params {
+  int32_t stride;          /* sample stride s >= 1 (default 128) */
+  float rho0;              /* primary target as a multiple of K (default 1.5) */
+  float rho1;              /* secondary target, >= rho0 (default 1.75) */
+  int64_t sample_min_len;  /* rows shorter than this skip sampling (exact boundary) */
+  int64_t direct_max;      /* N_alloc at or below which the on-chip direct kernel serves every row */
+  int32_t force_kind;      /* TOPK_KIND_*; AUTO lets the planner choose */
+  int32_t kv_segments;     /* KV-split segments per row; 0 = planner's choice */
+} topk_params;
+
+typedef struct topk_plan_info {
+  int32_t kind;            /* TOPK_KIND_* chosen for (M, N_alloc, K) on the current device */
+  int32_t grid;            /* CTAs of the main kernel */
+  int32_t segments;        /* KV-split segments per row (1 otherwise) */
+  int32_t sm_count;        /* SMs on the current device */
+  size_t workspace_bytes;  /* device workspace the call needs */
+  size_t smem_bytes;       /* dynamic shared memory per CTA of the main kernel */
+} topk_plan_info;
+
+/* Exact Top-K of every row (the spec call).
+ *   scores   device, [M][N_alloc] FP32, row-major, row stride N_alloc
+ *   row_lens device, [M] int32; values outside [0, N_alloc] are clamped and
+ *            flagged in the device status word (TOPK_FLAG_LEN_CLAMPED)
+ *   M >= 0, 0 <= N_alloc <= INT32_MAX, 1 <= K <= TOPK_K_MAX
+ *   out_idx  device, [M][K] int32, written completely
+ * Uses a workspace the library allocates on first use per (device, stream)
+ * and keeps until topk_release_workspaces().  M == 0 is a no-op.
+ * Returns TOPK_OK or a topk_status error. */
+int topk_ragged(const float* scores, const int32_t* row_lens, int64_t M, int64_t N_alloc,
+                int32_t K, int32_t* out_idx, struct CUstream_st* stream);
+
+/* Same as topk_ragged, and also writes diag[M] (device) with each row's
+ * thresholds, counts, path and flags. */
+int topk_ragged_diag(const float* scores, const int32_t* row_lens, int64_t M, int64_t N_alloc,
+                     int32_t K, int32_t* out_idx, topk_row_diag* diag,
+                     struct CUstream_st* stream);
+
+/* Device workspace bytes a call with these sizes needs under the current
+ * parameters (0 is a valid answer only for M == 0). */
+size_t topk_workspace_bytes(int64_t M, int64_t N_alloc, int32_t K);
+
+/* Explicit-workspace form.  `workspace` is device memory of at least
+ * topk_workspace_bytes(M, N_alloc, K) bytes, 256-byte aligned, zero-filled
+ * before its first use; every call leaves it ready for the next.  Calls that
+ * share one workspace must be ordered (same stream, or synchronised). */
+int topk_ragged_ws(const float* scores, const int32_t* row_lens, int64_t M, int64_t N_alloc,
+                   int32_t K, int32_t* out_idx, void* workspace, size_t workspace_bytes,
+                   struct CUstream_st* stream);
+
+/* Host-buffer form: copies the rows in chunks to the device, selects and
+ * copies the indices back, overlapping copies with selection on two streams.
+ *   h_scores  host [M][N_alloc] FP32 (page-locked memory gives full copy speed)
+ *   h_lens    host [M] int32
+ *   h_out     host [M][K] int32
+ *   rows_per_chunk  rows per device chunk; 0 picks about 1 GiB of scores per chunk
+ * Synchronous: returns after h_out is written.  Device buffers are cached
+ * per device until topk_release_workspaces(). */
+int topk_ragged_host(const float* h_scores, const int32_t* h_lens, int64_t M, int64_t N_alloc,
+                     int32_t K, int32_t* h_out, int64_t rows_per_chunk);
+
+/* Read-only planning: what a call with these sizes would launch. */
+int topk_plan(int64_t M, int64_t N_alloc, int32_t K, topk_plan_info* info);
+
+/* Set / get the process-wide parameters (host memory structs).  Invalid
+ * values (stride < 1, rho0 < 1, rho1 < rho0, negative lengths, unknown kind)
+ * return TOPK_ERR_ARG and change nothing.  Not thread-safe with calls in
+ * flight on other host threads. */
+int topk_set_params(const topk_params* p);
+int topk_get_params(topk_params* p);
+void topk_default_params(topk_params* p);
+
+/* Read and clear the current device's status word: the OR of TOPK_FLAG_* over
+ * every row selected since the last read.  Synchronises `stream` first. */
+int topk_read_status(struct CUstream_st* stream, uint32_t* flags);
+
+/* Free every cached workspace and host-path buffer of this process
+ * (synchronises the devices that own them). */
+void topk_release_workspaces(void);
+
+/* Human-readable name of a topk_status code (static string). */
+const char* topk_status_string(int code);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int topk_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXACT_TOPK_GB300_TOPK_H */

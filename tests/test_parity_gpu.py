@@ -1,0 +1,383 @@
+"""Parity of the CUDA selector with the CPU oracle (GPU only).
+
+Every result must pass the oracle's set-contract checker on every row, and
+must equal the oracle's set exactly on every row whose boundary is untied
+(index work: bit-exact, no tolerance).  Sampled rows also have their
+thresholds tau0/tau1, counts C(tau0)/C(tau1) and path compared with the
+oracle's definition of stage 1 and 2, exactly.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_top_sparse_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+K = 2048
+DEV = torch.device("cuda", 0)
+
+
+@pytest.fixture(scope="module")
+def ets():
+    import __graft_entry__ as g
+    g.build()
+    import exact_top_sparse_gb300 as m
+    return m
+
+
+@pytest.fixture
+def params(ets):
+    old = ets.get_params()
+    yield ets
+    ets.set_params(**old)
+
+
+def verify(x, lens, K, got, rows=None):
+    """Checker on every row plus exact equality on untied rows."""
+    if rows is not None:
+        x, lens, got = x[rows], lens[rows], got[rows]
+    xh = x.cpu().numpy()
+    lh = lens.cpu().numpy()
+    gh = got.cpu().numpy()
+    v = oracle.compare(xh, lh, K, gh)
+    bad = np.nonzero(v["check"])[0]
+    assert bad.size == 0, "rows %s fail the contract: %s" % (
+        bad[:8].tolist(), [oracle.CHECK_CODES[int(c)] for c in v["check"][bad[:8]]])
+    mism = np.nonzero(v["set_mismatch"])[0]
+    assert mism.size == 0, "untied rows %s differ from the oracle set" % mism[:8].tolist()
+    return v
+
+
+def verify_diag(ets, x, lens, K, diag, rows=None, sample_min_len=0):
+    """Thresholds, counts and path of sampled rows equal the oracle's."""
+    p = ets.get_params()
+    T0 = int(np.ceil(np.float64(np.float32(p["rho0"])) * K))
+    T1 = int(np.ceil(np.float64(np.float32(p["rho1"])) * K))
+    if rows is not None:
+        x, lens, diag = x[rows], lens[rows], diag[rows]
+    ref = oracle.thresholds(x.cpu().numpy(), lens.cpu().numpy(), K, p["stride"], T0, T1,
+                            sample_min_len)
+    sampled = ref["path"] >= oracle.PATH_TAU0
+    assert np.array_equal(diag["path"][sampled], ref["path"][sampled])
+    assert np.array_equal(diag["tau0"][sampled], ref["tau"][sampled, 0])
+    assert np.array_equal(diag["tau1"][sampled], ref["tau"][sampled, 1])
+    assert np.array_equal(diag["count0"][sampled], ref["count"][sampled, 0])
+    assert np.array_equal(diag["count1"][sampled], ref["count"][sampled, 1])
+    assert np.array_equal(diag["path"][~sampled], ref["path"][~sampled])
+    assert not np.any(diag["flags"] & (ets.FLAG_INTERNAL | ets.FLAG_TIMEOUT))
+    return ref
+
+
+def run(ets, x, lens, K=K, diag=False):
+    d_lens = lens.to(DEV)
+    if diag:
+        out, dg = ets.topk_ragged_diag(x, d_lens, K)
+    else:
+        out, dg = ets.topk_ragged(x, d_lens, K), None
+    torch.cuda.synchronize()
+    return out, dg
+
+
+# ------------------------------------------------------------------ config 1
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
+@pytest.mark.parametrize("kind", ["auto", "persistent", "kvsplit"])
+def test_tiny_config(params, seed, kind):
+    ets = params
+    N = 16384
+    lens = synth.tiny_lens(seed, M=8, N_alloc=N, K=K)
+    x = synth.indexer_rows(lens, N, seed=seed, device=DEV)
+    kinds = {"auto": ets.KIND_AUTO, "persistent": ets.KIND_PERSISTENT, "kvsplit": ets.KIND_KVSPLIT}
+    ets.set_params(force_kind=kinds[kind], sample_min_len=0 if kind != "auto" else 16384,
+                   kv_segments=4 if kind == "kvsplit" else 0)
+    got, dg = run(ets, x, lens, diag=True)
+    verify(x, lens, K, got)
+    if kind != "auto":
+        verify_diag(ets, x, lens, K, dg)
+    else:
+        assert set(dg["path"].tolist()) <= {ets.PATH_SENTINEL, ets.PATH_DIRECT}
+
+
+# ------------------------------------------------------------- configs 2 / 3
+@pytest.mark.parametrize("group", [0, 15])
+@pytest.mark.parametrize("kind", ["auto", "persistent"])
+def test_128k_operator_matrix_group(params, group, kind):
+    ets = params
+    N, M = 131072, 512
+    if kind == "persistent":
+        ets.set_params(force_kind=ets.KIND_PERSISTENT)
+    lens = synth.causal_lens(N, M, group)
+    x = synth.indexer_rows(lens, N, seed=100 + group, device=DEV)
+    got, dg = run(ets, x, lens, diag=True)
+    verify(x, lens, K, got)
+    verify_diag(ets, x, lens, K, dg, sample_min_len=ets.get_params()["sample_min_len"])
+
+
+@pytest.mark.parametrize("N,M", [(262144, 1024), (524288, 512), (1048576, 512)])
+def test_long_rows_default_dispatch(ets, N, M):
+    lens = synth.causal_lens(N, M, group=8192 // M - 1)
+    x = synth.indexer_rows(lens, N, seed=N + M, device=DEV)
+    got, dg = run(ets, x, lens, diag=True)
+    verify(x, lens, K, got)
+    verify_diag(ets, x, lens, K, dg, sample_min_len=ets.get_params()["sample_min_len"])
+    del x
+
+
+def test_full_size_1m_by_8192_sampled_rows(ets):
+    """The benchmark's configuration (1M columns, 8192 causal rows, default
+    dispatch); the oracle checks 48 sampled rows one by one."""
+    N, M = 1048576, 8192
+    plan = ets.plan(M, N, K)
+    lens = synth.causal_lens(N, M, 0)
+    x = synth.indexer_rows(lens, N, seed=7, device=DEV)
+    got, dg = run(ets, x, lens, diag=True)
+    g = torch.Generator().manual_seed(3)
+    rows = torch.cat([torch.tensor([0, M - 1]), torch.randperm(M, generator=g)[:46]])
+    rows = rows.sort().values
+    verify(x, lens, K, got, rows=rows.to(DEV))
+    verify_diag(ets, x, lens, K, dg, rows=rows.numpy(),
+                sample_min_len=ets.get_params()["sample_min_len"])
+    # every row: K distinct indices inside its prefix (property that holds at any size)
+    gs = got.sort(dim=1).values
+    assert bool((gs[:, 0] >= 0).all())
+    assert bool((gs[:, 1:] != gs[:, :-1]).all())
+    assert bool((gs[:, -1] < lens.to(DEV)).all())
+    assert plan["kind"] == "persistent"
+    assert not np.any(dg["flags"] & (ets.FLAG_INTERNAL | ets.FLAG_TIMEOUT))
+    del x
+
+
+# ------------------------------------------------------------------ config 4
+@pytest.mark.parametrize("N", [16384, 24576, 32768, 40960, 49152, 57344, 65536])
+@pytest.mark.parametrize("M", [64, 512])
+def test_width_sweep(ets, N, M):
+    lens = synth.causal_lens(N, M, group=0, window=min(8192, 64 * M))
+    x = synth.indexer_rows(lens, N, seed=N // 1024 + M, device=DEV)
+    got, _ = run(ets, x, lens)
+    verify(x, lens, K, got)
+
+
+@pytest.mark.parametrize("stride", [16, 64, 128, 256])
+@pytest.mark.parametrize("kind", ["persistent", "kvsplit"])
+def test_stride_sweep_sampled(params, stride, kind):
+    ets = params
+    N, M = 65536, 256
+    ets.set_params(stride=stride, sample_min_len=0,
+                   force_kind=ets.KIND_PERSISTENT if kind == "persistent" else ets.KIND_KVSPLIT)
+    lens = synth.causal_lens(N, M, group=0, window=8192)
+    x = synth.indexer_rows(lens, N, seed=stride, device=DEV)
+    got, dg = run(ets, x, lens, diag=True)
+    verify(x, lens, K, got)
+    verify_diag(ets, x, lens, K, dg)
+
+
+@pytest.mark.parametrize("kind", ["direct", "persistent", "kvsplit"])
+def test_bf16_grid_ties(params, kind):
+    ets = params
+    N, M = 65536 if kind != "direct" else 32768, 128
+    kinds = {"direct": ets.KIND_DIRECT, "persistent": ets.KIND_PERSISTENT,
+             "kvsplit": ets.KIND_KVSPLIT}
+    ets.set_params(force_kind=kinds[kind], sample_min_len=0)
+    lens = synth.causal_lens(N, M, group=0, window=4096)
+    x = synth.to_bf16_grid(synth.indexer_rows(lens, N, seed=5, device=DEV))
+    got, dg = run(ets, x, lens, diag=True)
+    v = verify(x, lens, K, got)
+    assert v["tied"].mean() > 0.5
+    if kind != "direct":
+        verify_diag(ets, x, lens, K, dg)
+
+
+@pytest.mark.parametrize("kind", ["direct", "persistent", "kvsplit"])
+def test_uniform_rows(params, kind):
+    ets = params
+    N, M = 49152, 96
+    kinds = {"direct": ets.KIND_DIRECT, "persistent": ets.KIND_PERSISTENT,
+             "kvsplit": ets.KIND_KVSPLIT}
+    ets.set_params(force_kind=kinds[kind], sample_min_len=0)
+    lens = synth.causal_lens(N, M, group=0, window=96 * 64)
+    x = synth.uniform_rows(lens, N, seed=9, device=DEV)
+    got, dg = run(ets, x, lens, diag=True)
+    verify(x, lens, K, got)
+    if kind != "direct":
+        verify_diag(ets, x, lens, K, dg)
+
+
+@pytest.mark.parametrize("kind", ["persistent", "kvsplit"])
+def test_forced_paths_tau1_recovery_overflow(params, kind):
+    """Rows built so the proposal underfills (tau1 path, exact recovery) or
+    overfills past the on-chip buffer; every row must still be exact."""
+    ets = params
+    ets.set_params(sample_min_len=0, kv_segments=7 if kind == "kvsplit" else 0,
+                   force_kind=ets.KIND_PERSISTENT if kind == "persistent" else ets.KIND_KVSPLIT)
+    L = 65536
+    lens = torch.full((1,), L, dtype=torch.int32)
+    rows = [
+        synth.strided_high_rows(lens, L, seed=1, stride=128, n_top=26, n_mid=2100),   # tau1
+        synth.strided_high_rows(lens, L, seed=2, stride=128, n_top=40, n_mid=2100),   # recovery
+        synth.strided_high_rows(lens, L, seed=3, stride=128, n_top=0, n_mid=20000,
+                                on_grid=False),                                       # overflow
+        synth.strided_high_rows(lens, L, seed=4, stride=128, n_top=10, n_mid=3000),   # tau0
+    ]
+    x = torch.cat(rows).to(DEV)
+    lens4 = torch.full((4,), L, dtype=torch.int32)
+    got, dg = run(ets, x, lens4, diag=True)
+    verify(x, lens4, K, got)
+    ref = verify_diag(ets, x, lens4, K, dg)
+    assert ref["path"].tolist() == [ets.PATH_TAU1, ets.PATH_RECOVERY, ets.PATH_TAU0,
+                                    ets.PATH_TAU0]
+    assert dg["flags"][1] & ets.FLAG_RECOVERY
+    assert dg["flags"][2] & ets.FLAG_OVERFLOW
+
+
+@pytest.mark.parametrize("kind", ["direct", "persistent", "kvsplit"])
+def test_constant_rows(params, kind):
+    ets = params
+    N, M = 40000, 6
+    kinds = {"direct": ets.KIND_DIRECT, "persistent": ets.KIND_PERSISTENT,
+             "kvsplit": ets.KIND_KVSPLIT}
+    ets.set_params(force_kind=kinds[kind], sample_min_len=0, kv_segments=3)
+    lens = torch.tensor([40000, 2049, 2048, 5000, 39999, 12345], dtype=torch.int32)
+    x = synth.constant_rows(lens, N, 3.25, device=DEV)
+    got, _ = run(ets, x, lens)
+    verify(x, lens, K, got)
+
+
+# ---------------------------------------------------------------- edge cases
+def test_empty_batch_and_zero_width(ets):
+    x = torch.empty((0, 100), dtype=torch.float32, device=DEV)
+    out = ets.topk_ragged(x, torch.empty(0, dtype=torch.int32, device=DEV), K)
+    assert out.shape == (0, K)
+    x = torch.empty((3, 0), dtype=torch.float32, device=DEV)
+    out = ets.topk_ragged(x, torch.tensor([0, 5, -2], dtype=torch.int32, device=DEV), 16)
+    torch.cuda.synchronize()
+    assert bool((out == -1).all())
+
+
+@pytest.mark.parametrize("kind", ["direct", "persistent", "kvsplit"])
+def test_clamped_lengths_and_status(params, kind):
+    ets = params
+    kinds = {"direct": ets.KIND_DIRECT, "persistent": ets.KIND_PERSISTENT,
+             "kvsplit": ets.KIND_KVSPLIT}
+    ets.set_params(force_kind=kinds[kind], sample_min_len=0)
+    N = 40000
+    raw = torch.tensor([-7, 10 ** 9, 100, N], dtype=torch.int32)
+    lens = raw.clamp(0, N)
+    x = synth.indexer_rows(lens, N, seed=4, device=DEV)
+    ets.read_status()
+    got, dg = run(ets, x, raw, diag=True)
+    verify(x, lens, K, got)
+    assert ets.read_status() & ets.FLAG_LEN_CLAMPED
+    assert dg["flags"][0] & ets.FLAG_LEN_CLAMPED and dg["flags"][1] & ets.FLAG_LEN_CLAMPED
+    assert not dg["flags"][2] & ets.FLAG_LEN_CLAMPED
+
+
+@pytest.mark.parametrize("k", [1, 7, 2048, 4096])
+@pytest.mark.parametrize("kind", ["direct", "persistent", "kvsplit"])
+def test_other_k(params, k, kind):
+    ets = params
+    kinds = {"direct": ets.KIND_DIRECT, "persistent": ets.KIND_PERSISTENT,
+             "kvsplit": ets.KIND_KVSPLIT}
+    ets.set_params(force_kind=kinds[kind], sample_min_len=0)
+    N, M = 45000, 5
+    lens = torch.tensor([45000, k, k + 1, 30001, 4097], dtype=torch.int32)
+    x = synth.indexer_rows(lens, N, seed=k, device=DEV)
+    got, _ = run(ets, x, lens, K=k)
+    verify(x, lens, k, got)
+
+
+@pytest.mark.parametrize("kind", ["direct", "persistent", "kvsplit"])
+def test_unaligned_rows(params, kind):
+    """Rows that start off 16-byte boundaries (odd N_alloc, offset base)."""
+    ets = params
+    kinds = {"direct": ets.KIND_DIRECT, "persistent": ets.KIND_PERSISTENT,
+             "kvsplit": ets.KIND_KVSPLIT}
+    ets.set_params(force_kind=kinds[kind], sample_min_len=0)
+    N, M = 40001, 9
+    lens = torch.tensor([40001, 40000, 39999, 39998, 2049, 3000, 12345, 40001, 20001],
+                        dtype=torch.int32)
+    base = torch.empty(M * N + 3, dtype=torch.float32, device=DEV)
+    x = base[1:1 + M * N].view(M, N)
+    x.copy_(synth.indexer_rows(lens, N, seed=77, device=DEV))
+    assert x.data_ptr() % 16 != 0
+    got, _ = run(ets, x, lens)
+    verify(x, lens, K, got)
+
+
+def test_explicit_workspace(ets):
+    N, M = 131072, 64
+    lens = synth.causal_lens(N, M, 0, window=8192)
+    x = synth.indexer_rows(lens, N, seed=12, device=DEV)
+    need = ets.workspace_bytes(M, N, K)
+    assert need > 0
+    small = torch.zeros(max(256, need - 256), dtype=torch.uint8, device=DEV)
+    with pytest.raises(ets.TopKError) as e:
+        ets.topk_ragged_ws(x, lens.to(DEV), K, small)
+    assert e.value.code == -3
+    ws = torch.zeros(need, dtype=torch.uint8, device=DEV)
+    for _ in range(2):
+        got = ets.topk_ragged_ws(x, lens.to(DEV), K, ws)
+        torch.cuda.synchronize()
+        verify(x, lens, K, got)
+
+
+@pytest.mark.parametrize("N,M", [(131072, 512), (131072, 2048), (1048576, 256)])
+def test_cuda_graph_replay(ets, N, M):
+    """Capture once, replay with new scores and lengths written in place."""
+    lens = synth.causal_lens(N, M, 0, window=max(M, 8192 if N > 8192 else M))
+    x = synth.indexer_rows(lens, N, seed=1, device=DEV)
+    d_lens = lens.to(DEV)
+    out = torch.empty((M, K), dtype=torch.int32, device=DEV)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        ets.topk_ragged(x, d_lens, K, out=out)  # creates the workspace before capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        ets.topk_ragged(x, d_lens, K, out=out)
+    for rep in range(3):
+        lens2 = (lens - 37 * rep).clamp(min=0)
+        x.copy_(synth.indexer_rows(lens2, N, seed=50 + rep, device=DEV))
+        d_lens.copy_(lens2.to(DEV))
+        out.fill_(-5)
+        g.replay()
+        torch.cuda.synchronize()
+        verify(x, lens2, K, out)
+
+
+def test_capture_without_workspace_is_refused(ets):
+    N, M = 131072, 64
+    x = torch.zeros((M, N), dtype=torch.float32, device=DEV)
+    lens = torch.full((M,), N, dtype=torch.int32, device=DEV)
+    out = torch.empty((M, K), dtype=torch.int32, device=DEV)
+    ets.plan(M, N, K)  # device set-up happens outside the capture
+    s = torch.cuda.Stream()  # a stream the library has never seen
+    lib = ets.load_library()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        g.capture_begin()
+        try:
+            rc = lib.topk_ragged(x.data_ptr(), lens.data_ptr(), M, N, K, out.data_ptr(),
+                                 ctypes.c_void_p(s.cuda_stream))
+        finally:
+            g.capture_end()
+    assert rc == -5
+
+
+def test_host_buffer_api(ets):
+    N, M = 131072, 300
+    lens = synth.causal_lens(N, M, 0, window=600)
+    x = synth.indexer_rows(lens, N, seed=21, device=DEV).cpu().numpy()
+    got = ets.topk_ragged_host(x, lens.numpy(), K, rows_per_chunk=64)
+    v = oracle.compare(x, lens.numpy(), K, got)
+    assert not v["check"].any() and not v["set_mismatch"].any()
+
+
+def test_plan_kinds(ets):
+    assert ets.plan(8, 16384, K)["kind"] == "direct"
+    assert ets.plan(8192, 1048576, K)["kind"] == "persistent"
+    p = ets.plan(512, 1048576, K)
+    assert p["kind"] == "kvsplit" and p["segments"] > 1
