@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--force-kind", default="auto",
+                    choices=["auto", "direct", "persistent", "kvsplit"])
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per launch from an ncu capture of this kernel")
     return ap.parse_args()
@@ -238,6 +240,9 @@ def run_gb300(args):
     N, M, K = args.N, args.M, args.K
     peak, peak_kind = measured_peaks()
     stream = torch.cuda.Stream(device=dev)
+    if args.force_kind != "auto":
+        ets.set_params(force_kind={"direct": ets.KIND_DIRECT, "persistent": ets.KIND_PERSISTENT,
+                                   "kvsplit": ets.KIND_KVSPLIT}[args.force_kind])
 
     x, lens = make_inputs(N, M, 0, seed=7 + rank, device=dev)
     d_lens = lens.to(dev)
@@ -259,6 +264,12 @@ def run_gb300(args):
     kern_ms = statistics.mean(per)
     achieved = valid_bytes / (kern_ms / 1000.0) / 1e9
     status = ets.read_status(dev, stream)
+    # per-row paths of one (untimed) call with diagnostics
+    with torch.cuda.stream(stream):
+        _, dg = ets.topk_ragged_diag(x, d_lens, K)
+    paths = {name: int((dg["path"] == code).sum()) for name, code in
+             (("sentinel", 0), ("direct", 1), ("tau0", 2), ("tau1", 3), ("recovery", 4))}
+    paths["overflow"] = int(((dg["flags"] & ets.FLAG_OVERFLOW) != 0).sum())
 
     result = {
         "metric": METRIC, "value": rows_per_s, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -281,6 +292,7 @@ def run_gb300(args):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "status_flags": status,
+        "row_paths": paths,
     }
     # a short exactness spot check of the timed output (8 rows, oracle)
     if rank == 0:

@@ -121,7 +121,7 @@ def _inputs(scores, row_lens, K, out):
         raise TypeError("scores must be a CUDA tensor")
     if scores.dtype != torch.float32 or scores.dim() != 2:
         raise TypeError("scores must be a 2-D float32 tensor [M, N_alloc]")
-    if scores.stride(1) != 1 or (scores.shape[0] > 1 and scores.stride(0) != scores.shape[1]):
+    if not scores.is_contiguous():
         raise ValueError("scores must be contiguous (row stride N_alloc)")
     if not (isinstance(row_lens, torch.Tensor) and row_lens.device == scores.device
             and row_lens.dtype == torch.int32 and row_lens.dim() == 1
