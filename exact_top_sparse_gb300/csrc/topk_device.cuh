@@ -118,15 +118,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase of `bar` with the given parity; gives up (returns false)
-// after WAIT_LIMIT_NS so that no wait can hang the GPU.
-__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Set by the first wait that gives up; every later wait then fails at once,
+// so a kernel that lost a copy finishes quickly (its rows flagged) instead of
+// timing out wait after wait.  Cleared when the status word is read and by
+// the last CTA of each persistent launch.
+__device__ uint32_t g_abort;
+
+// Slow path of mbar_wait: polls until the phase completes, giving up after
+// WAIT_LIMIT_NS so that no wait can hang the GPU.
+__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0 && globaltimer() - t0 > WAIT_LIMIT_NS) return false;
+    if ((it & 63u) == 0) {
+      if (*reinterpret_cast<volatile uint32_t*>(&g_abort) != 0u) return false;
+      if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+        atomicExch(&g_abort, 1u);
+        return false;
+      }
+    }
   }
+}
+
+// Waits for the phase of `bar` with the given parity (false after a timeout).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity);
 }
 
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
@@ -152,9 +169,11 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// A single score, cached in L2 only (one 32-byte sector, no L1 line fill),
+// with the given L2 eviction policy.
 __device__ __forceinline__ float ld_keep(const float* p, uint64_t policy) {
   float v;
-  asm volatile("ld.global.nc.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(p), "l"(policy));
+  asm volatile("ld.global.cg.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(p), "l"(policy));
   return v;
 }
 
@@ -487,18 +506,13 @@ struct ScanCollect {
     uint32_t m = (admit(v.x) ? 1u : 0u) | (admit(v.y) ? 2u : 0u) | (admit(v.z) ? 4u : 0u) |
                  (admit(v.w) ? 8u : 0u);
     m &= vm;
-    if (__any_sync(FULL_MASK, m != 0)) slow(i0, v, m);
+    if (m) slow(i0, v, m);
   }
 
+  // Admitted scores are rare (about 1.75K of a row), so each lane appends its
+  // own with one shared-memory atomic; no warp-wide step on this path.
   __device__ __forceinline__ void slow(int64_t i0, float4 v, uint32_t m) {
-    const uint32_t lane = lane_id();
-    const uint32_t cnt = (uint32_t)__popc(m);
-    const uint32_t incl = warp_incl_scan(cnt);
-    const uint32_t total = __shfl_sync(FULL_MASK, incl, 31);
-    uint32_t base = 0;
-    if (lane == 31 && total) base = atomicAdd(ncand, total);
-    base = __shfl_sync(FULL_MASK, base, 31);
-    uint32_t pos = base + incl - cnt;
+    uint32_t pos = atomicAdd(ncand, (uint32_t)__popc(m));
     const float vals[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -753,12 +767,66 @@ __device__ uint32_t select_rank(const G& get, int64_t n, uint32_t r, uint32_t lo
   return lo;
 }
 
+// The r0-th and r1-th largest (r0 <= r1) of keys[0..n) held in shared memory,
+// whose range is [kmin, kmax].  One histogram round finds the bin holding
+// the r1-th largest; when the keys from that bin up number at most THREADS
+// they are gathered into `list` and ranked by counting, which yields both
+// answers at once.  Otherwise two general rank selections run.  Every thread
+// must call.
+__device__ void select_two_ranks(const uint32_t* keys, uint32_t n, uint32_t r0, uint32_t r1,
+                                 uint32_t kmin, uint32_t kmax, uint32_t* hist, uint32_t* list,
+                                 Shared& S, uint32_t* key0, uint32_t* key1) {
+  if (kmin == kmax) {
+    *key0 = *key1 = kmin;
+    return;
+  }
+  const Bins bn = make_bins(kmin, kmax);
+  __syncthreads();
+  clear_hist(hist);
+  if (threadIdx.x == 0) S.small_n = 0;
+  __syncthreads();
+  for (uint32_t i = threadIdx.x; i < n; i += THREADS) atomicAdd(&hist[bn.digit(keys[i])], 1u);
+  __syncthreads();
+  find_boundary(hist, r1, S);
+  const uint32_t lo1 = bn.bin_lo(S.b);
+  const uint32_t L = S.above + hist[S.b];
+  if (S.ok && L <= (uint32_t)THREADS) {
+    for (uint32_t i = threadIdx.x; i < n; i += THREADS) {
+      const uint32_t k = keys[i];
+      if (k >= lo1) {
+        const uint32_t t = atomicAdd(&S.small_n, 1u);
+        if (t < (uint32_t)THREADS) list[t] = k;
+      }
+    }
+    __syncthreads();
+    const uint32_t m = min(S.small_n, (uint32_t)THREADS);
+    if (threadIdx.x < m) {
+      const uint32_t k = list[threadIdx.x];
+      uint32_t rank = 0;
+      for (uint32_t j = 0; j < m; ++j) {
+        const uint32_t kj = list[j];
+        rank += (kj > k || (kj == k && j < threadIdx.x)) ? 1u : 0u;
+      }
+      if (rank == r0 - 1) S.key0 = k;
+      if (rank == r1 - 1) S.key1 = k;
+    }
+    __syncthreads();
+    *key0 = S.key0;
+    *key1 = S.key1;
+    __syncthreads();
+    return;
+  }
+  const SampleSmem g{keys};
+  *key1 = select_rank(g, n, r1, kmin, kmax, hist, S);
+  *key0 = select_rank(g, n, r0, *key1, kmax, hist, S);
+}
+
 // Stage 1.  Samples at 0, s, 2s, ... < len; tau_j = r_j-th largest sample
 // with r_j = clamp(ceil(T_j * n_s / len), 1, n_s).  Leaves key0/key1 and the
 // sample key range in S.  Every thread must call.
 __device__ void sample_thresholds(const float* __restrict__ row, int64_t len, int32_t stride,
                                   uint32_t T0, uint32_t T1, uint32_t* skeys, uint32_t* hist,
-                                  Shared& S) {
+                                  uint32_t* list, Shared& S) {
   const int64_t ns = (len + stride - 1) / stride;
   int64_t r0 = ((int64_t)T0 * ns + len - 1) / len;
   int64_t r1 = ((int64_t)T1 * ns + len - 1) / len;
@@ -767,7 +835,7 @@ __device__ void sample_thresholds(const float* __restrict__ row, int64_t len, in
   const uint64_t pol = l2_policy_evict_last();
   const bool on_chip = ns <= SAMPLE_SMEM;
   uint32_t mn = 0xffffffffu, mx = 0u;
-  constexpr int U = 8;
+  constexpr int U = 16;  // one round trip for up to 8192 samples
   for (int64_t i0 = threadIdx.x; i0 < ns; i0 += (int64_t)THREADS * U) {
     float v[U];
 #pragma unroll
@@ -790,9 +858,8 @@ __device__ void sample_thresholds(const float* __restrict__ row, int64_t len, in
   block_minmax(mn, mx, S, &kmin, &kmax);
   uint32_t key1, key0;
   if (on_chip) {
-    const SampleSmem g{skeys};
-    key1 = select_rank(g, ns, (uint32_t)r1, kmin, kmax, hist, S);
-    key0 = select_rank(g, ns, (uint32_t)r0, key1, kmax, hist, S);
+    select_two_ranks(skeys, (uint32_t)ns, (uint32_t)r0, (uint32_t)r1, kmin, kmax, hist, list, S,
+                     &key0, &key1);
   } else {
     const SampleGlobal g{row, stride, pol};
     key1 = select_rank(g, ns, (uint32_t)r1, kmin, kmax, hist, S);

@@ -32,7 +32,8 @@ constexpr size_t SH_HDR = align_up(sizeof(Shared), 128);
 constexpr size_t SH_RING = SH_HDR;
 constexpr size_t SH_CAND = SH_RING + (size_t)STAGES * CHUNK_BYTES;
 constexpr size_t SH_HIST = SH_CAND + (size_t)CAP * sizeof(uint2);
-constexpr size_t SH_ROW_TOTAL = SH_HIST + (size_t)NB * sizeof(uint32_t);
+constexpr size_t SH_LIST = SH_HIST + (size_t)NB * sizeof(uint32_t);
+constexpr size_t SH_ROW_TOTAL = SH_LIST + (size_t)THREADS * sizeof(uint32_t);
 
 // KV-split per-row state in the workspace.
 struct KvHdr {
@@ -52,6 +53,7 @@ struct RowCarve {
   float* ring;
   uint2* cand;
   uint32_t* hist;
+  uint32_t* list;
 };
 
 __device__ __forceinline__ RowCarve carve(uint8_t* smem) {
@@ -60,6 +62,7 @@ __device__ __forceinline__ RowCarve carve(uint8_t* smem) {
   c.ring = reinterpret_cast<float*>(smem + SH_RING);
   c.cand = reinterpret_cast<uint2*>(smem + SH_CAND);
   c.hist = reinterpret_cast<uint32_t*>(smem + SH_HIST);
+  c.list = reinterpret_cast<uint32_t*>(smem + SH_LIST);
   return c;
 }
 
@@ -223,7 +226,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       continue;
     }
     sample_thresholds(row, len, P.stride, P.target0, P.target1,
-                      reinterpret_cast<uint32_t*>(c.cand), c.hist, S);
+                      reinterpret_cast<uint32_t*>(c.cand), c.hist, c.list, S);
     const uint32_t key0 = S.key0, key1 = S.key1, kmin = S.kmin, kmax = S.kmax;
     const Bins sb = scan_bins(key1, kmax);
     __syncthreads();
@@ -244,6 +247,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     if (atomicAdd(&hdr[1], 1u) == gridDim.x - 1) {
       atomicExch(&hdr[0], 0u);
       atomicExch(&hdr[1], 0u);
+      atomicExch(&g_abort, 0u);
       __threadfence();
     }
   }
@@ -336,7 +340,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   extern __shared__ __align__(128) uint8_t smem[];
   Shared& S = *reinterpret_cast<Shared*>(smem);
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem + SH_HDR);
-  uint32_t* skeys = hist + NB;
+  uint32_t* list = hist + NB;
+  uint32_t* skeys = list + THREADS;
   const int64_t r = blockIdx.x;
   uint32_t lflags = 0;
   const int64_t len = clamp_len(row_lens[r], P.N_alloc, lflags);
@@ -350,7 +355,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   else if (len < P.sample_min_len) mode = 1;
   uint32_t key0 = 0, key1 = 0, kmin = 0, kmax = 0;
   if (mode == 2) {
-    sample_thresholds(row, len, P.stride, P.target0, P.target1, skeys, hist, S);
+    sample_thresholds(row, len, P.stride, P.target0, P.target1, skeys, hist, list, S);
     key0 = S.key0;
     key1 = S.key1;
     kmin = S.kmin;
@@ -465,7 +470,7 @@ __global__ void __launch_bounds__(THREADS, 2)
 size_t persistent_smem_bytes() { return SH_ROW_TOTAL; }
 size_t kv_segment_smem_bytes() { return SH_ROW_TOTAL; }
 size_t kv_prepare_smem_bytes() {
-  return SH_HDR + (size_t)NB * sizeof(uint32_t) + (size_t)SAMPLE_SMEM * sizeof(uint32_t);
+  return SH_HDR + (size_t)(NB + THREADS + SAMPLE_SMEM) * sizeof(uint32_t);
 }
 size_t direct_smem_bytes(int64_t n_alloc) {
   return SH_HDR + (size_t)NB * sizeof(uint32_t) + align_up((size_t)(n_alloc + 4) * 4, 16);
@@ -527,6 +532,8 @@ cudaError_t read_and_clear_status(cudaStream_t st, uint32_t* flags) {
                                             cudaMemcpyDeviceToHost, st);
   if (e != cudaSuccess) return e;
   e = cudaMemcpyToSymbolAsync(g_status, &zero, sizeof(uint32_t), 0, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyToSymbolAsync(g_abort, &zero, sizeof(uint32_t), 0, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return e;
   e = cudaStreamSynchronize(st);
   *flags = h;
