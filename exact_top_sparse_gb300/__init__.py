@@ -64,7 +64,8 @@ class PlanInfo(ctypes.Structure):
 EXPORTS = ("topk_ragged", "topk_ragged_diag", "topk_ragged_ws", "topk_workspace_bytes",
            "topk_ragged_host", "topk_plan", "topk_set_params", "topk_get_params",
            "topk_default_params", "topk_read_status", "topk_release_workspaces",
-           "topk_status_string", "topk_version")
+           "topk_status_string", "topk_version", "topk_ragged_noalloc")
+NOALLOC_MAX_ROWS = 64
 
 _lib = None
 
@@ -84,6 +85,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.topk_ragged.argtypes = [vp, vp, i64, i64, i32, vp, vp]
     lib.topk_ragged_diag.argtypes = [vp, vp, i64, i64, i32, vp, vp, vp]
     lib.topk_ragged_ws.argtypes = [vp, vp, i64, i64, i32, vp, vp, sz, vp]
+    lib.topk_ragged_noalloc.argtypes = [vp, vp, i64, i64, i32, vp, vp]
     lib.topk_workspace_bytes.argtypes = [i64, i64, i32]
     lib.topk_workspace_bytes.restype = sz
     lib.topk_ragged_host.argtypes = [vp, vp, i64, i64, i32, vp, i64]
@@ -99,6 +101,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.topk_status_string.restype = ctypes.c_char_p
     lib.topk_version.argtypes = []
     for name in ("topk_ragged", "topk_ragged_diag", "topk_ragged_ws", "topk_ragged_host",
+                 "topk_ragged_noalloc",
                  "topk_plan", "topk_set_params", "topk_get_params", "topk_read_status",
                  "topk_version"):
         getattr(lib, name).restype = ctypes.c_int
@@ -174,6 +177,24 @@ def topk_ragged_ws(scores, row_lens, K, workspace: torch.Tensor, out=None, strea
                                 workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                 _stream_handle(scores.device, stream))
     _check(rc, "topk_ragged_ws")
+    return out
+
+
+def topk_ragged_noalloc(scores, row_lens, K: int = 2048, out=None, stream=None):
+    """Fixed-scratch form: allocates no device memory in the library.
+
+    For callers that may not allocate (an allocator that owns the whole GPU,
+    a plugin host that forbids allocation while it runs).  At most
+    NOALLOC_MAX_ROWS rows per call; calls that overlap on the GPU race on the
+    shared scratch.  Pass `out` to avoid the one allocation this wrapper would
+    otherwise make for the result tensor.
+    """
+    lib = load_library()
+    M, N, out = _inputs(scores, row_lens, K, out)
+    with torch.cuda.device(scores.device):
+        rc = lib.topk_ragged_noalloc(scores.data_ptr(), row_lens.data_ptr(), M, N, K,
+                                     out.data_ptr(), _stream_handle(scores.device, stream))
+    _check(rc, "topk_ragged_noalloc")
     return out
 
 

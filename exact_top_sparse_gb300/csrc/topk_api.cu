@@ -279,6 +279,64 @@ int topk_ragged_ws(const float* scores, const int32_t* row_lens, int64_t M, int6
              stream);
 }
 
+}  // extern "C"
+
+namespace {
+
+// Scratch of topk_ragged_noalloc(): the KV-split merge state of up to
+// TOPK_NOALLOC_MAX_ROWS rows.  In host code this name is only a stand-in for
+// the device object; its device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[(size_t)TOPK_NOALLOC_MAX_ROWS *
+                                                           tk::kKvRowBytes];
+
+constexpr int kNoallocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kNoallocMaxDevices] = {};  // per device, found on its first call
+
+}  // namespace
+
+extern "C" {
+
+int topk_ragged_noalloc(const float* scores, const int32_t* row_lens, int64_t M, int64_t N_alloc,
+                        int32_t K, int32_t* out_idx, struct CUstream_st* stream) {
+  int rc = check_sizes(M, N_alloc, K);
+  if (rc) return rc;
+  rc = validate_ptrs(scores, row_lens, M, N_alloc, out_idx);
+  if (rc) return rc;
+  if (M == 0) return TOPK_OK;
+  if (M > TOPK_NOALLOC_MAX_ROWS) return TOPK_ERR_WORKSPACE;
+  DevInfo d;
+  int dev = 0;
+  rc = device_info(&d, &dev);
+  if (rc) return rc;
+  if (dev < 0 || dev >= kNoallocMaxDevices) return TOPK_ERR_NO_DEVICE;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+        cudaGetLastError();
+        return TOPK_ERR_CUDA;
+      }
+      g_noalloc_addr[dev] = p;
+    }
+    scratch = g_noalloc_addr[dev];
+  }
+  topk_params p = params_snapshot();
+  p.force_kind = TOPK_KIND_KVSPLIT;
+  Plan pl;
+  rc = make_plan(M, N_alloc, K, p, d, &pl);
+  if (rc) return rc;
+  if (pl.kind != TOPK_KIND_KVSPLIT ||
+      (size_t)M * tk::kv_row_bytes() > sizeof(g_noalloc_scratch))
+    return TOPK_ERR_WORKSPACE;
+  const cudaError_t e =
+      tk::launch_kvsplit(scores, row_lens, out_idx, nullptr, static_cast<uint8_t*>(scratch),
+                         kernel_params(M, N_alloc, K, p, pl), stream);
+  return e == cudaSuccess ? TOPK_OK : TOPK_ERR_CUDA;
+}
+
 size_t topk_workspace_bytes(int64_t M, int64_t N_alloc, int32_t K) {
   if (check_sizes(M, N_alloc, K) || M == 0) return 0;
   DevInfo d;

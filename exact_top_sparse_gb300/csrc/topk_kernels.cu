@@ -47,6 +47,7 @@ constexpr size_t KV_HIST_OFF = 256;
 constexpr size_t KV_CAND_OFF = KV_HIST_OFF + (size_t)NB * sizeof(uint32_t);
 constexpr size_t KV_ROW_BYTES = align_up(KV_CAND_OFF + (size_t)CAP * sizeof(uint2), 256);
 static_assert(sizeof(KvHdr) <= KV_HIST_OFF, "KV row header too large");
+static_assert(KV_ROW_BYTES == kKvRowBytes, "kKvRowBytes must match the KV-split row layout");
 
 struct RowCarve {
   Shared* S;

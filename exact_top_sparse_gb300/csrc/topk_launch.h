@@ -33,6 +33,8 @@ size_t kv_segment_smem_bytes();
 size_t kv_prepare_smem_bytes();
 size_t direct_smem_bytes(int64_t n_alloc);
 size_t kv_row_bytes();
+// Bytes of KV-split merge state per row (equals kv_row_bytes()).
+constexpr size_t kKvRowBytes = 57600;
 
 // Sets the kernels' shared-memory limits on the current device.
 cudaError_t prepare_device();

@@ -152,6 +152,27 @@ int topk_ragged_ws(const float* scores, const int32_t* row_lens, int64_t M, int6
                    int32_t K, int32_t* out_idx, void* workspace, size_t workspace_bytes,
                    struct CUstream_st* stream);
 
+/* Rows topk_ragged_noalloc() accepts in one call. */
+#define TOPK_NOALLOC_MAX_ROWS 64
+
+/* Fixed-scratch form, for callers that may not allocate device memory.  The
+ * paper has no counterpart; this exists because some callers cannot call
+ * cudaMalloc: serving processes whose allocator owns every byte of the GPU,
+ * plugin hosts that forbid allocation while they execute, and code that must
+ * not risk the device-wide synchronisation or out-of-memory failure an
+ * allocation can bring.  It runs the KV-split path with its per-row merge
+ * state in one statically sized device array (TOPK_NOALLOC_MAX_ROWS rows,
+ * about 3.5 MiB) that every GPU loading this library holds until the process
+ * exits.  Arguments and results are those of topk_ragged(); M above
+ * TOPK_NOALLOC_MAX_ROWS returns TOPK_ERR_WORKSPACE.  The first call on a
+ * device looks up the array's device address (make that first call before
+ * any stream capture).  Every call shares the one array and the kernels
+ * re-initialise it, so calls that overlap on the GPU (different streams, or
+ * other host threads) race and must be serialised by the caller.  It never
+ * calls cudaMalloc or cudaFree. */
+int topk_ragged_noalloc(const float* scores, const int32_t* row_lens, int64_t M, int64_t N_alloc,
+                        int32_t K, int32_t* out_idx, struct CUstream_st* stream);
+
 /* Host-buffer form: copies the rows in chunks to the device, selects and
  * copies the indices back, overlapping copies with selection on two streams.
  *   h_scores  host [M][N_alloc] FP32 (page-locked memory gives full copy speed)
