@@ -130,6 +130,28 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def profiled_traffic(kind, valid_bytes):
+    """DRAM bytes per launch from the committed ncu capture of this kernel.
+
+    profiles/k_persistent_traffic.json holds the DRAM-bytes-per-valid-byte
+    ratio of one capture and a hash of the kernel sources it was taken on;
+    the figure is reported only while those sources are unchanged (else None).
+    """
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "k_persistent_traffic.json")
+    if kind != "persistent" or not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    h = hashlib.sha256()
+    for name in ("topk_device.cuh", "topk_kernels.cu", "topk_launch.h"):
+        with open(os.path.join(ROOT, "exact_top_sparse_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest()[:16] != d.get("kernel_sources_sha256_16"):
+        return None
+    return float(d["dram_bytes_per_valid_byte"]) * valid_bytes
+
+
 def make_inputs(N, M, group, seed, device):
     from exact_top_sparse_gb300 import synth
     lens = synth.causal_lens(N, M, group)
@@ -285,7 +307,8 @@ def run_gb300(args):
                    "gbps_valid_scores": achieved},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": args.traffic,
+                     "traffic": (args.traffic if args.traffic is not None
+                                 else profiled_traffic(plan["kind"], valid_bytes)),
                      "bytes_per_launch": valid_bytes,
                      "kernel": "k_kv_segment" if plan["kind"] == "kvsplit" else
                                ("k_direct" if plan["kind"] == "direct" else "k_persistent")},
