@@ -45,7 +45,8 @@ constexpr int NB_BITS = 11;
 constexpr int NB = 1 << NB_BITS;            // bins per radix round
 static_assert(NB == 4 * THREADS, "boundary search maps 4 bins to each thread");
 constexpr int STAGES = 3;                   // ring stages
-constexpr int CHUNK_BYTES = 16384;          // bytes per bulk copy / ring stage
+constexpr int CHUNK_BYTES = 8 * CONSUMERS * 4;  // bytes per bulk copy / ring stage (15 KB):
+                                                // two float4 per consumer thread
 constexpr int CHUNK_FLOATS = CHUNK_BYTES / 4;
 constexpr int CAP = 6144;                   // on-chip candidate capacity (entries of 8 B)
 constexpr int SMALL = 32;                   // frontier size finished by one warp
@@ -526,6 +527,82 @@ struct ScanCollect {
     }
   }
 };
+
+// The largest admission operand of four scores (raw bits as signed integers
+// when tau1 > +0; keys mapped to signed order otherwise).
+template <bool POS>
+__device__ __forceinline__ int32_t max_operand(const float4& v) {
+  if (POS) {
+    const int32_t a = (int32_t)__float_as_uint(v.x), b = (int32_t)__float_as_uint(v.y);
+    const int32_t c = (int32_t)__float_as_uint(v.z), d = (int32_t)__float_as_uint(v.w);
+    return max(max(a, b), max(c, d));
+  }
+  return (int32_t)(max(max(fkey(v.x), fkey(v.y)), max(fkey(v.z), fkey(v.w))) ^ 0x80000000u);
+}
+
+// The certify+collect pass over [start, end) of `row`.  Same ring protocol as
+// ring_pass, with the consumer side shaped for the common case: a full chunk
+// is exactly two float4 per consumer thread, all eight scores are tested with
+// one integer max, the stage is handed back as soon as the loads have fed
+// that test, and only lanes holding an admitted score (rare) do more work.
+template <bool POS>
+__device__ __forceinline__ void scan_pass(Ring& R, const float* __restrict__ row, int64_t start,
+                                          int64_t end, ScanCollect<POS>& f, uint32_t& lflags) {
+  static_assert(CHUNK_FLOATS == 8 * CONSUMERS, "a full chunk is two float4 per consumer");
+  const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31u;
+  if (end <= start) return;
+  const uintptr_t addr = reinterpret_cast<uintptr_t>(row + start);
+  int64_t a0 = start + (int64_t)(((16u - (uint32_t)(addr & 15u)) & 15u) >> 2);
+  if (a0 > end) a0 = end;
+  const int64_t a1 = a0 + ((end - a0) & ~(int64_t)3);
+  const uint32_t nchunks = (uint32_t)((a1 - a0 + CHUNK_FLOATS - 1) / CHUNK_FLOATS);
+  if (warp == 0) {
+    if (lane == 0) {
+      for (uint32_t c = 0; c < nchunks; ++c) {
+        const uint32_t q = R.seq + c, s = q % STAGES, use = q / STAGES;
+        if (!mbar_wait(&R.empty[s], (use & 1u) ^ 1u)) lflags |= F_TIMEOUT;
+        const int64_t off = a0 + (int64_t)c * CHUNK_FLOATS;
+        const int64_t n = (a1 - off) < CHUNK_FLOATS ? (a1 - off) : CHUNK_FLOATS;
+        const uint32_t bytes = (uint32_t)(n * 4);
+        fence_proxy_async();
+        mbar_arrive_expect_tx(&R.full[s], bytes);
+        bulk_load(R.buf + (size_t)s * CHUNK_FLOATS, row + off, bytes, &R.full[s], R.policy);
+      }
+    }
+  } else {
+    if (warp == 1) {
+      // head [start, a0) on lanes 0..2, tail [a1, end) on lanes 4..6
+      const int64_t nh = a0 - start, nt = end - a1;
+      int64_t i = -1;
+      if ((int64_t)lane < nh) i = start + lane;
+      else if (lane >= 4 && (int64_t)lane - 4 < nt) i = a1 + (lane - 4);
+      const float v = (i >= 0) ? row[i] : 0.0f;
+      f.quad(i >= 0 ? i : 0, make_float4(v, 0.f, 0.f, 0.f), i >= 0 ? 1u : 0u);
+    }
+    const uint32_t ct = tid - 32;
+    const int32_t thr = POS ? (int32_t)f.t1 : (int32_t)(f.t1 ^ 0x80000000u);
+    for (uint32_t c = 0; c < nchunks; ++c) {
+      const uint32_t q = R.seq + c, s = q % STAGES, use = q / STAGES;
+      if (!mbar_wait(&R.full[s], use & 1u)) lflags |= F_TIMEOUT;
+      const int64_t off = a0 + (int64_t)c * CHUNK_FLOATS;
+      const int64_t n = (a1 - off) < CHUNK_FLOATS ? (a1 - off) : CHUNK_FLOATS;
+      const int nf4 = (int)(n >> 2);
+      const float4* sm4 = reinterpret_cast<const float4*>(R.buf + (size_t)s * CHUNK_FLOATS);
+      const int j0 = (int)ct, j1 = (int)ct + CONSUMERS;
+      const bool ok0 = j0 < nf4, ok1 = j1 < nf4;
+      const float4 v0 = ok0 ? sm4[j0] : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 v1 = ok1 ? sm4[j1] : make_float4(0.f, 0.f, 0.f, 0.f);
+      const int32_t m0 = ok0 ? max_operand<POS>(v0) : INT32_MIN;
+      const int32_t m1 = ok1 ? max_operand<POS>(v1) : INT32_MIN;
+      // both loads have fed m0/m1: hand the stage back before any appends
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&R.empty[s]);
+      if (ok0 && m0 >= thr) f.quad(off + 4 * (int64_t)j0, v0, 0xfu);
+      if (ok1 && m1 >= thr) f.quad(off + 4 * (int64_t)j1, v1, 0xfu);
+    }
+  }
+  R.seq += nchunks;
+}
 
 // ------------------------------------------------ frontier refinement engine
 enum PassMode : uint32_t { TAKE_ALL = 0, TAKE_SOME = 1, SMALL_SORT = 2, COLLECT = 3, NEXT_HIST = 4 };

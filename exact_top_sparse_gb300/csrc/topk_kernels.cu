@@ -136,11 +136,11 @@ __device__ uint32_t scan_collect(const float* row, int64_t s0, int64_t s1, Ring&
   uint32_t c0 = 0;
   if (tau1 > 0.0f) {
     ScanCollect<true> f{__float_as_uint(tau1), key0, sb, c.cand, c.hist, &S.ncand, 0u};
-    ring_pass(R, row, s0, s1, f, lflags);
+    scan_pass(R, row, s0, s1, f, lflags);
     c0 = f.c0;
   } else {
     ScanCollect<false> f{key1, key0, sb, c.cand, c.hist, &S.ncand, 0u};
-    ring_pass(R, row, s0, s1, f, lflags);
+    scan_pass(R, row, s0, s1, f, lflags);
     c0 = f.c0;
   }
   __syncthreads();
