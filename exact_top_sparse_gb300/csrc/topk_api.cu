@@ -144,6 +144,7 @@ int make_plan(int64_t M, int64_t N, int32_t K, const topk_params& p, const DevIn
   } else if (kind == TOPK_KIND_PERSISTENT) {
     pl->grid = (int)(M < resident ? M : resident);
     pl->smem = tk::persistent_smem_bytes();
+    pl->ws += (size_t)pl->grid * tk::persistent_spill_bytes();
   } else {
     pl->grid = (int)(M * pl->segments);
     pl->smem = tk::kv_segment_smem_bytes();
@@ -184,8 +185,8 @@ int launch(const Plan& pl, const tk::Params& P, const float* scores, const int32
   if (pl.kind == TOPK_KIND_DIRECT) {
     e = tk::launch_direct(scores, row_lens, out_idx, d, P, st);
   } else if (pl.kind == TOPK_KIND_PERSISTENT) {
-    e = tk::launch_persistent(scores, row_lens, out_idx, d, static_cast<uint32_t*>(ws), pl.grid,
-                              P, st);
+    e = tk::launch_persistent(scores, row_lens, out_idx, d, static_cast<uint32_t*>(ws),
+                              static_cast<uint8_t*>(ws) + kHdrBytes, pl.grid, P, st);
   } else {
     e = tk::launch_kvsplit(scores, row_lens, out_idx, d,
                            static_cast<uint8_t*>(ws) + kHdrBytes, P, st);

@@ -49,6 +49,8 @@ constexpr int CHUNK_BYTES = 8 * CONSUMERS * 4;  // bytes per bulk copy / ring st
                                                 // two float4 per consumer thread
 constexpr int CHUNK_FLOATS = CHUNK_BYTES / 4;
 constexpr int CAP = 6144;                   // on-chip candidate capacity (entries of 8 B)
+constexpr int SPILL = 10240;                // further candidates kept in global memory
+constexpr int CAP_ALL = CAP + SPILL;        // candidates one full-row pass can keep
 constexpr int SMALL = 32;                   // frontier size finished by one warp
 constexpr int SAMPLE_SMEM = 2 * CAP;        // sample keys kept on chip (they alias the candidates)
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // bounded waits give up after 2 s
@@ -485,48 +487,75 @@ __device__ __forceinline__ void ring_pass(Ring& R, const float* __restrict__ row
   R.seq += nchunks;
 }
 
+// Candidate j of a row: entries [0, CAP) live in shared memory, the rest in a
+// global spill area written earlier in the same kernel (read through L2).
+__device__ __forceinline__ uint2 cand_at(const uint2* cand, const uint2* spill, uint32_t j) {
+  if (j < (uint32_t)CAP) return cand[j];
+  const uint2* p = spill + (j - (uint32_t)CAP);
+  return make_uint2(__ldcg(&p->x), __ldcg(&p->y));
+}
+
 // ------------------------------------------------- certify + collect (stage 2)
 // Admission: key(v) >= key(tau1).  When tau1 > +0 the signed comparison of
 // the raw bits gives the same answer in one instruction (POS = true).
+// During the pass an admitted score is only appended, as (index, key), to the
+// shared candidate array; C(tau0) and the seeded histogram are taken from the
+// array once the pass is over (tally_candidates), which keeps the histogram
+// atomics out of the streaming loop.
 template <bool POS>
 struct ScanCollect {
-  uint32_t t1;      // POS: bits of tau1; otherwise key(tau1)
-  uint32_t key0;
-  Bins bins;
-  uint2* cand;
-  uint32_t* hist;
+  uint32_t t1;  // POS: bits of tau1; otherwise key(tau1)
+  uint2* cand;  // CAP entries in shared memory
+  uint2* spill; // entries CAP.. in global memory (nullptr: none)
+  uint32_t cap; // CAP_ALL with a spill area, else CAP
   uint32_t* ncand;
-  uint32_t c0;
 
   __device__ __forceinline__ bool admit(float x) const {
     if (POS) return (int32_t)__float_as_uint(x) >= (int32_t)t1;
     return fkey(x) >= t1;
   }
-
-  __device__ __forceinline__ void quad(int64_t i0, float4 v, uint32_t vm) {
-    uint32_t m = (admit(v.x) ? 1u : 0u) | (admit(v.y) ? 2u : 0u) | (admit(v.z) ? 4u : 0u) |
-                 (admit(v.w) ? 8u : 0u);
-    m &= vm;
-    if (m) slow(i0, v, m);
+  __device__ __forceinline__ uint32_t admit_mask(const float4& v) const {
+    return (admit(v.x) ? 1u : 0u) | (admit(v.y) ? 2u : 0u) | (admit(v.z) ? 4u : 0u) |
+           (admit(v.w) ? 8u : 0u);
   }
-
-  // Admitted scores are rare (about 1.75K of a row), so each lane appends its
-  // own with one shared-memory atomic; no warp-wide step on this path.
-  __device__ __forceinline__ void slow(int64_t i0, float4 v, uint32_t m) {
-    uint32_t pos = atomicAdd(ncand, (uint32_t)__popc(m));
+  __device__ __forceinline__ void put(uint32_t& pos, int64_t i0, const float4& v,
+                                      uint32_t m) const {
     const float vals[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       if (m & (1u << e)) {
-        const uint32_t k = fkey(vals[e]);
-        c0 += (k >= key0) ? 1u : 0u;
-        atomicAdd(&hist[bins.digit(k)], 1u);
-        if (pos < (uint32_t)CAP) cand[pos] = make_uint2((uint32_t)(i0 + e), k);
+        const uint2 ent = make_uint2((uint32_t)(i0 + e), fkey(vals[e]));
+        if (pos < (uint32_t)CAP) cand[pos] = ent;
+        else if (pos < cap) spill[pos - (uint32_t)CAP] = ent;
         ++pos;
       }
     }
   }
+  // Appends the admitted scores among the elements of v selected by vm
+  // (element i0 + e is lane e): one shared-memory atomic reserves this lane's
+  // slots.
+  __device__ __forceinline__ void lane_put(int64_t i0, const float4& v, uint32_t vm) const {
+    const uint32_t m = admit_mask(v) & vm;
+    if (m) {
+      uint32_t pos = atomicAdd(ncand, (uint32_t)__popc(m));
+      put(pos, i0, v, m);
+    }
+  }
 };
+
+// C(tau0) and the seeded histogram of the full-row pass, from candidates
+// [0, n).  Returns this thread's share of C(tau0).
+__device__ __forceinline__ uint32_t tally_candidates(const uint2* cand, const uint2* spill,
+                                                     uint32_t n, uint32_t key0, const Bins& sb,
+                                                     uint32_t* hist) {
+  uint32_t c0 = 0;
+  for (uint32_t j = threadIdx.x; j < n; j += THREADS) {
+    const uint32_t k = cand_at(cand, spill, j).y;
+    c0 += (k >= key0) ? 1u : 0u;
+    atomicAdd(&hist[sb.digit(k)], 1u);
+  }
+  return c0;
+}
 
 // The largest admission operand of four scores (raw bits as signed integers
 // when tau1 > +0; keys mapped to signed order otherwise).
@@ -544,7 +573,7 @@ __device__ __forceinline__ int32_t max_operand(const float4& v) {
 // ring_pass, with the consumer side shaped for the common case: a full chunk
 // is exactly two float4 per consumer thread, all eight scores are tested with
 // one integer max, the stage is handed back as soon as the loads have fed
-// that test, and only lanes holding an admitted score (rare) do more work.
+// that test, and only lanes holding an admitted score (rare) append.
 template <bool POS>
 __device__ __forceinline__ void scan_pass(Ring& R, const float* __restrict__ row, int64_t start,
                                           int64_t end, ScanCollect<POS>& f, uint32_t& lflags) {
@@ -577,7 +606,7 @@ __device__ __forceinline__ void scan_pass(Ring& R, const float* __restrict__ row
       if ((int64_t)lane < nh) i = start + lane;
       else if (lane >= 4 && (int64_t)lane - 4 < nt) i = a1 + (lane - 4);
       const float v = (i >= 0) ? row[i] : 0.0f;
-      f.quad(i >= 0 ? i : 0, make_float4(v, 0.f, 0.f, 0.f), i >= 0 ? 1u : 0u);
+      if (i >= 0) f.lane_put(i, make_float4(v, 0.f, 0.f, 0.f), 1u);
     }
     const uint32_t ct = tid - 32;
     const int32_t thr = POS ? (int32_t)f.t1 : (int32_t)(f.t1 ^ 0x80000000u);
@@ -597,8 +626,8 @@ __device__ __forceinline__ void scan_pass(Ring& R, const float* __restrict__ row
       // both loads have fed m0/m1: hand the stage back before any appends
       __syncwarp();
       if (lane == 0) mbar_arrive(&R.empty[s]);
-      if (ok0 && m0 >= thr) f.quad(off + 4 * (int64_t)j0, v0, 0xfu);
-      if (ok1 && m1 >= thr) f.quad(off + 4 * (int64_t)j1, v1, 0xfu);
+      if (ok0 && m0 >= thr) f.lane_put(off + 4 * (int64_t)j0, v0, 0xfu);
+      if (ok1 && m1 >= thr) f.lane_put(off + 4 * (int64_t)j1, v1, 0xfu);
     }
   }
   R.seq += nchunks;
@@ -670,11 +699,33 @@ struct HistF {
   }
 };
 
+// Seeded histogram of the full-row pass rebuilt from the row (keys >= bins.lo)
+// together with C(tau0).
+struct SeedF {
+  Bins bins;
+  uint32_t key0;
+  uint32_t* hist;
+  uint32_t c0;
+  __device__ __forceinline__ void elem(uint32_t, uint32_t key, bool valid) {
+    if (valid && key >= bins.lo) {
+      atomicAdd(&hist[bins.digit(key)], 1u);
+      c0 += (key >= key0) ? 1u : 0u;
+    }
+  }
+  __device__ __forceinline__ void quad(int64_t, float4 v, uint32_t vm) {
+    elem(0, fkey(v.x), (vm & 1u) != 0);
+    elem(0, fkey(v.y), (vm & 2u) != 0);
+    elem(0, fkey(v.z), (vm & 4u) != 0);
+    elem(0, fkey(v.w), (vm & 8u) != 0);
+  }
+};
+
 // Sources the refinement loop can iterate.  for_each() calls f.elem (or
 // f.quad) warp-uniformly; the caller synchronises the block afterwards.
-struct CandSrc {  // (idx, key) entries in shared memory
+struct CandSrc {  // (idx, key) entries: shared memory, then the spill area
   static constexpr bool kRow = false;
   const uint2* cand;
+  const uint2* spill;
   uint32_t n;
   template <class F>
   __device__ __forceinline__ void for_each(F& f, uint32_t&) const {
@@ -682,7 +733,7 @@ struct CandSrc {  // (idx, key) entries in shared memory
     for (uint32_t it = 0; it < iters; ++it) {
       const uint32_t j = threadIdx.x + it * THREADS;
       const bool ok = j < n;
-      const uint2 e = ok ? cand[j] : make_uint2(0u, 0u);
+      const uint2 e = ok ? cand_at(cand, spill, j) : make_uint2(0u, 0u);
       f.elem(e.x, e.y, ok);
     }
   }
@@ -769,7 +820,7 @@ __device__ void refine(const Src& src, Bins bins, uint32_t Kp, uint32_t* hist, u
     }
     if constexpr (Src::kRow) {
       if (mode == COLLECT) {
-        const CandSrc cs{cand, min(S.ncand, (uint32_t)CAP)};
+        const CandSrc cs{cand, nullptr, min(S.ncand, (uint32_t)CAP)};
         refine(cs, nb, Kr, hist, cand, out, K, S, lflags);
         return;
       }

@@ -45,7 +45,7 @@ struct KvHdr {
 };
 constexpr size_t KV_HIST_OFF = 256;
 constexpr size_t KV_CAND_OFF = KV_HIST_OFF + (size_t)NB * sizeof(uint32_t);
-constexpr size_t KV_ROW_BYTES = align_up(KV_CAND_OFF + (size_t)CAP * sizeof(uint2), 256);
+constexpr size_t KV_ROW_BYTES = align_up(KV_CAND_OFF + (size_t)CAP_ALL * sizeof(uint2), 256);
 static_assert(sizeof(KvHdr) <= KV_HIST_OFF, "KV row header too large");
 static_assert(KV_ROW_BYTES == kKvRowBytes, "kKvRowBytes must match the KV-split row layout");
 
@@ -127,41 +127,54 @@ __device__ void exact_row_stream(const float* row, int64_t len, int32_t* out, in
   refine(RowSrc{&R, row, len}, bins, (uint32_t)K, c.hist, c.cand, out, K, S, lflags);
 }
 
-// The full-row certify+collect pass over [s0, s1) with thresholds in S.
+// The full-row certify+collect pass over [s0, s1): candidates in c.cand and
+// past CAP in `spill` (nullptr: none), their count in S.ncand (past the
+// capacity when they did not fit), the seeded histogram of the kept ones in
+// c.hist.  Returns C(tau0) over the kept candidates, which is the exact
+// count unless they overflowed.
 __device__ uint32_t scan_collect(const float* row, int64_t s0, int64_t s1, Ring& R,
-                                 const RowCarve& c, uint32_t key0, uint32_t key1, const Bins& sb,
-                                 uint32_t& lflags) {
+                                 const RowCarve& c, uint2* spill, uint32_t key0, uint32_t key1,
+                                 const Bins& sb, uint32_t& lflags) {
   Shared& S = *c.S;
   const float tau1 = key_to_float(key1);
-  uint32_t c0 = 0;
+  const uint32_t cap = spill ? (uint32_t)CAP_ALL : (uint32_t)CAP;
   if (tau1 > 0.0f) {
-    ScanCollect<true> f{__float_as_uint(tau1), key0, sb, c.cand, c.hist, &S.ncand, 0u};
+    ScanCollect<true> f{__float_as_uint(tau1), c.cand, spill, cap, &S.ncand};
     scan_pass(R, row, s0, s1, f, lflags);
-    c0 = f.c0;
   } else {
-    ScanCollect<false> f{key1, key0, sb, c.cand, c.hist, &S.ncand, 0u};
+    ScanCollect<false> f{key1, c.cand, spill, cap, &S.ncand};
     scan_pass(R, row, s0, s1, f, lflags);
-    c0 = f.c0;
   }
   __syncthreads();
+  const uint32_t c0 = tally_candidates(c.cand, spill, min(S.ncand, cap), key0, sb, c.hist);
   return block_sum(c0, S);
 }
 
-// Everything after the full-row pass of a sampled row whose candidates,
-// histogram and counts are on chip: refine, or re-read on overflow, or
-// recover.  Returns the row path.
+// Everything after the full-row pass of a sampled row whose candidates
+// (c.cand, then `spill`), histogram and counts are ready: refine, or re-read
+// on overflow, or recover.  Returns the row path.
 __device__ int32_t select_after_scan(const float* row, int64_t len, int32_t* out, int32_t K,
-                                     Ring& R, const RowCarve& c, uint32_t C0, uint32_t C1,
-                                     bool overflow, uint32_t key1, uint32_t kmin, const Bins& sb,
-                                     uint32_t& lflags) {
+                                     Ring& R, const RowCarve& c, const uint2* spill, uint32_t& C0,
+                                     uint32_t C1, bool overflow, uint32_t key0, uint32_t key1,
+                                     uint32_t kmin, const Bins& sb, uint32_t& lflags) {
   Shared& S = *c.S;
-  const int32_t path = (C0 >= (uint32_t)K) ? PATH_TAU0 : (C1 >= (uint32_t)K ? PATH_TAU1 : PATH_RECOVERY);
+  int32_t path = (C0 >= (uint32_t)K) ? PATH_TAU0 : (C1 >= (uint32_t)K ? PATH_TAU1 : PATH_RECOVERY);
   if (C1 >= (uint32_t)K && !overflow) {
-    refine(CandSrc{c.cand, C1}, sb, (uint32_t)K, c.hist, c.cand, out, K, S, lflags);
+    refine(CandSrc{c.cand, spill, C1}, sb, (uint32_t)K, c.hist, c.cand, out, K, S, lflags);
   } else if (C1 >= (uint32_t)K) {
-    // More admitted scores than the on-chip buffer holds.  The histogram is
-    // complete, so the refinement re-reads the row for the boundary bin only.
+    // More admitted scores than the candidate buffers hold.  The ones past
+    // them were not kept, so one pass over the row rebuilds the seeded
+    // histogram and C(tau0); the refinement then re-reads the row for the
+    // boundary bin only.
     lflags |= F_OVERFLOW;
+    __syncthreads();
+    clear_hist(c.hist);
+    __syncthreads();
+    SeedF sf{sb, key0, c.hist, 0u};
+    ring_pass(R, row, 0, len, sf, lflags);
+    __syncthreads();
+    C0 = block_sum(sf.c0, S);
+    path = (C0 >= (uint32_t)K) ? PATH_TAU0 : PATH_TAU1;
     refine(RowSrc{&R, row, len}, sb, (uint32_t)K, c.hist, c.cand, out, K, S, lflags);
   } else {
     // C(tau1) < K: every admitted score belongs to the answer; the remaining
@@ -194,9 +207,10 @@ __device__ int32_t select_after_scan(const float* row, int64_t len, int32_t* out
 __global__ void __launch_bounds__(THREADS, 2)
     k_persistent(const float* __restrict__ scores, const int32_t* __restrict__ row_lens,
                  int32_t* __restrict__ out_idx, RowDiag* __restrict__ diag, uint32_t* hdr,
-                 Params P) {
+                 uint2* __restrict__ spill_all, Params P) {
   extern __shared__ __align__(128) uint8_t smem[];
   const RowCarve c = carve(smem);
+  uint2* spill = spill_all + (size_t)blockIdx.x * SPILL;
   Shared& S = *c.S;
   if (threadIdx.x == 0) S.flags = 0;
   Ring R;
@@ -234,11 +248,11 @@ __global__ void __launch_bounds__(THREADS, 2)
     clear_hist(c.hist);
     if (threadIdx.x == 0) S.ncand = 0;
     __syncthreads();
-    const uint32_t C0 = scan_collect(row, 0, len, R, c, key0, key1, sb, lflags);
+    uint32_t C0 = scan_collect(row, 0, len, R, c, spill, key0, key1, sb, lflags);
     const uint32_t C1 = S.ncand;
     __syncthreads();
-    const int32_t path = select_after_scan(row, len, out, K, R, c, C0, C1, C1 > (uint32_t)CAP,
-                                           key1, kmin, sb, lflags);
+    const int32_t path = select_after_scan(row, len, out, K, R, c, spill, C0, C1,
+                                           C1 > (uint32_t)CAP_ALL, key0, key1, kmin, sb, lflags);
     finish_row(S, out, K, lflags, diag, r, path, key_to_float(key0), key_to_float(key1), C0, C1);
   }
   // The last CTA to leave resets the queue, so the next launch (or graph
@@ -410,7 +424,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     clear_hist(c.hist);
     if (threadIdx.x == 0) S.ncand = 0;
     __syncthreads();
-    const uint32_t C0 = scan_collect(row, s0, s1, R, c, key0, key1, sb, lflags);
+    const uint32_t C0 = scan_collect(row, s0, s1, R, c, nullptr, key0, key1, sb, lflags);
     const uint32_t nloc = S.ncand;
     if (threadIdx.x == 0) {
       atomicAdd(&h->c0, C0);
@@ -421,7 +435,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     const uint32_t gbase = S.res;
     const uint32_t ncopy = min(nloc, (uint32_t)CAP);
     for (uint32_t j = threadIdx.x; j < ncopy; j += THREADS) {
-      if (gbase + j < (uint32_t)CAP) gcand[gbase + j] = c.cand[j];
+      if (gbase + j < (uint32_t)CAP_ALL) gcand[gbase + j] = c.cand[j];
     }
     for (int i = threadIdx.x; i < NB; i += THREADS) {
       const uint32_t v = c.hist[i];
@@ -452,9 +466,9 @@ __global__ void __launch_bounds__(THREADS, 2)
     finish_row(S, out, K, lflags, diag, r, PATH_DIRECT, qnan, qnan, 0, 0);
     return;
   }
-  const uint32_t C0 = __ldcg(&h->c0);
+  uint32_t C0 = __ldcg(&h->c0);
   const uint32_t C1 = __ldcg(&h->ncand);
-  const bool overflow = __ldcg(&h->ovf) != 0u || C1 > (uint32_t)CAP;
+  const bool overflow = __ldcg(&h->ovf) != 0u || C1 > (uint32_t)CAP_ALL;
   for (int i = threadIdx.x; i < NB; i += THREADS) c.hist[i] = __ldcg(&ghist[i]);
   const uint32_t nload = min(C1, (uint32_t)CAP);
   for (uint32_t j = threadIdx.x; j < nload; j += THREADS) {
@@ -463,7 +477,8 @@ __global__ void __launch_bounds__(THREADS, 2)
   }
   __syncthreads();
   const int32_t path =
-      select_after_scan(row, len, out, K, R, c, C0, C1, overflow, key1, kmin, sb, lflags);
+      select_after_scan(row, len, out, K, R, c, gcand + CAP, C0, C1, overflow, key0, key1, kmin,
+                        sb, lflags);
   finish_row(S, out, K, lflags, diag, r, path, key_to_float(key0), key_to_float(key1), C0, C1);
 }
 
@@ -477,6 +492,7 @@ size_t direct_smem_bytes(int64_t n_alloc) {
   return SH_HDR + (size_t)NB * sizeof(uint32_t) + align_up((size_t)(n_alloc + 4) * 4, 16);
 }
 size_t kv_row_bytes() { return KV_ROW_BYTES; }
+size_t persistent_spill_bytes() { return (size_t)SPILL * sizeof(uint2); }
 
 static cudaError_t set_smem(const void* fn, size_t bytes) {
   return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
@@ -508,10 +524,10 @@ cudaError_t launch_direct(const float* scores, const int32_t* row_lens, int32_t*
 }
 
 cudaError_t launch_persistent(const float* scores, const int32_t* row_lens, int32_t* out,
-                              RowDiag* diag, uint32_t* hdr, int grid, const Params& P,
+                              RowDiag* diag, uint32_t* hdr, void* spill, int grid, const Params& P,
                               cudaStream_t st) {
-  k_persistent<<<grid, THREADS, persistent_smem_bytes(), st>>>(scores, row_lens, out, diag, hdr,
-                                                               P);
+  k_persistent<<<grid, THREADS, persistent_smem_bytes(), st>>>(
+      scores, row_lens, out, diag, hdr, static_cast<uint2*>(spill), P);
   return cudaGetLastError();
 }
 

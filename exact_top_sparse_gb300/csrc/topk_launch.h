@@ -34,7 +34,9 @@ size_t kv_prepare_smem_bytes();
 size_t direct_smem_bytes(int64_t n_alloc);
 size_t kv_row_bytes();
 // Bytes of KV-split merge state per row (equals kv_row_bytes()).
-constexpr size_t kKvRowBytes = 57600;
+constexpr size_t kKvRowBytes = 139520;
+// Bytes of global candidate spill area per persistent CTA.
+size_t persistent_spill_bytes();
 
 // Sets the kernels' shared-memory limits on the current device.
 cudaError_t prepare_device();
@@ -43,7 +45,7 @@ cudaError_t persistent_occupancy(int* blocks_per_sm);
 cudaError_t launch_direct(const float* scores, const int32_t* row_lens, int32_t* out,
                           RowDiag* diag, const Params& P, cudaStream_t st);
 cudaError_t launch_persistent(const float* scores, const int32_t* row_lens, int32_t* out,
-                              RowDiag* diag, uint32_t* hdr, int grid, const Params& P,
+                              RowDiag* diag, uint32_t* hdr, void* spill, int grid, const Params& P,
                               cudaStream_t st);
 cudaError_t launch_kvsplit(const float* scores, const int32_t* row_lens, int32_t* out,
                            RowDiag* diag, uint8_t* ws_rows, const Params& P, cudaStream_t st);
