@@ -52,7 +52,9 @@ assert DIAG_DTYPE.itemsize == ctypes.sizeof(RowDiag)
 class Params(ctypes.Structure):
     _fields_ = [("stride", ctypes.c_int32), ("rho0", ctypes.c_float), ("rho1", ctypes.c_float),
                 ("sample_min_len", ctypes.c_int64), ("direct_max", ctypes.c_int64),
-                ("force_kind", ctypes.c_int32), ("kv_segments", ctypes.c_int32)]
+                ("force_kind", ctypes.c_int32), ("kv_segments", ctypes.c_int32),
+                ("long_len", ctypes.c_int64), ("long_stride", ctypes.c_int32),
+                ("long_rho0", ctypes.c_float), ("long_rho1", ctypes.c_float)]
 
 
 class PlanInfo(ctypes.Structure):

@@ -53,13 +53,17 @@ struct HostPipe {
 std::map<int, HostPipe> g_pipe;
 
 void defaults(topk_params* p) {
-  p->stride = 128;
-  p->rho0 = 1.5f;
-  p->rho1 = 1.75f;
+  p->stride = 256;
+  p->rho0 = 2.0f;
+  p->rho1 = 2.25f;
   p->sample_min_len = 16384;
   p->direct_max = 49152;
   p->force_kind = TOPK_KIND_AUTO;
   p->kv_segments = 0;
+  p->long_len = 786432;
+  p->long_stride = 512;
+  p->long_rho0 = 2.75f;
+  p->long_rho1 = 3.0f;
 }
 
 topk_params params_snapshot() {
@@ -173,6 +177,11 @@ tk::Params kernel_params(int64_t M, int64_t N, int32_t K, const topk_params& p, 
   P.target0 = (uint32_t)std::ceil((double)p.rho0 * (double)K);
   P.target1 = (uint32_t)std::ceil((double)p.rho1 * (double)K);
   if (P.target1 < P.target0) P.target1 = P.target0;
+  P.long_len = p.long_len;
+  P.long_stride = p.long_stride;
+  P.long_target0 = (uint32_t)std::ceil((double)p.long_rho0 * (double)K);
+  P.long_target1 = (uint32_t)std::ceil((double)p.long_rho1 * (double)K);
+  if (P.long_target1 < P.long_target0) P.long_target1 = P.long_target0;
   P.sample_min_len = p.sample_min_len;
   P.segments = pl.segments;
   return P;
@@ -373,6 +382,8 @@ void topk_default_params(topk_params* p) {
 int topk_set_params(const topk_params* p) {
   if (!p) return TOPK_ERR_ARG;
   if (p->stride < 1 || !(p->rho0 >= 1.0f) || !(p->rho1 >= p->rho0) || !(p->rho1 <= 64.0f) ||
+      p->long_stride < 1 || !(p->long_rho0 >= 1.0f) || !(p->long_rho1 >= p->long_rho0) ||
+      !(p->long_rho1 <= 64.0f) || p->long_len < 0 ||
       p->sample_min_len < 0 || p->direct_max < 0 || p->kv_segments < 0 ||
       p->kv_segments > 4096 || p->force_kind < TOPK_KIND_AUTO || p->force_kind > TOPK_KIND_KVSPLIT)
     return TOPK_ERR_ARG;

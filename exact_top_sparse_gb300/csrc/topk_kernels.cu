@@ -26,6 +26,16 @@ namespace tk {
 
 __device__ uint32_t g_status;  // OR of row flags since the last read
 
+// Sampling stride and targets of a row of `len` elements.
+struct SampleSpec {
+  int32_t stride;
+  uint32_t target0, target1;
+};
+__device__ __forceinline__ SampleSpec sample_spec(const Params& P, int64_t len) {
+  if (P.long_len > 0 && len >= P.long_len) return {P.long_stride, P.long_target0, P.long_target1};
+  return {P.stride, P.target0, P.target1};
+}
+
 // ------------------------------------------------------- shared-memory plan
 constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 constexpr size_t SH_HDR = align_up(sizeof(Shared), 128);
@@ -240,7 +250,8 @@ __global__ void __launch_bounds__(THREADS, 2)
       finish_row(S, out, K, lflags, diag, r, PATH_DIRECT, qnan, qnan, 0, 0);
       continue;
     }
-    sample_thresholds(row, len, P.stride, P.target0, P.target1,
+    const SampleSpec sp = sample_spec(P, len);
+    sample_thresholds(row, len, sp.stride, sp.target0, sp.target1,
                       reinterpret_cast<uint32_t*>(c.cand), c.hist, c.list, S);
     const uint32_t key0 = S.key0, key1 = S.key1, kmin = S.kmin, kmax = S.kmax;
     const Bins sb = scan_bins(key1, kmax);
@@ -370,7 +381,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   else if (len < P.sample_min_len) mode = 1;
   uint32_t key0 = 0, key1 = 0, kmin = 0, kmax = 0;
   if (mode == 2) {
-    sample_thresholds(row, len, P.stride, P.target0, P.target1, skeys, hist, list, S);
+    const SampleSpec sp = sample_spec(P, len);
+    sample_thresholds(row, len, sp.stride, sp.target0, sp.target1, skeys, hist, list, S);
     key0 = S.key0;
     key1 = S.key1;
     kmin = S.kmin;

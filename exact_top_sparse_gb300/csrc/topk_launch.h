@@ -18,6 +18,10 @@ struct Params {
   uint32_t target1;  // ceil(rho1 * K)
   int64_t sample_min_len;
   int32_t segments;  // KV-split segments per row
+  int64_t long_len;  // rows this long or longer sample with the long_* values (0: none)
+  int32_t long_stride;
+  uint32_t long_target0;
+  uint32_t long_target1;
 };
 
 // Same layout as topk_row_diag in the public header.

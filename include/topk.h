@@ -98,19 +98,28 @@ typedef struct topk_row_diag {
   uint32_t flags;  /* TOPK_FLAG_* for this row */
 } topk_row_diag;
 
-/* Process-wide tuning knobs.  Sampling knobs follow the codexqa.cn section
- * "采样不是处处都该开": stride s = 128, primary target 1.5K candidates,
- * secondary 1.75K.  A sample rank is r = ceil(T * n_s / len) clamped to
- * [1, n_s], with T = ceil(rho * K), n_s = ceil(len / s) and samples at
- * positions 0, s, 2s, ... below len. */
+/* Process-wide tuning knobs.  A sampled row is viewed at a fixed stride s
+ * (positions 0, s, 2s, ... below len, n_s = ceil(len / s) samples); its
+ * thresholds are the samples of rank r = ceil(T * n_s / len), clamped to
+ * [1, n_s], with targets T = ceil(rho * K) (codexqa.cn section
+ * "采样不是处处都该开", which uses s = 128, T = 1.5K and 1.75K on H20).
+ * Every sampled element costs one DRAM access on GB300, so the defaults
+ * take a wider stride with proportionally larger targets (the same sample
+ * ranks), and rows of at least long_len elements a wider one still:
+ *   len <  long_len: s = stride,      T = rho0 * K,      rho1 * K
+ *   len >= long_len: s = long_stride, T = long_rho0 * K, long_rho1 * K */
 typedef struct topk_params {
-  int32_t stride;          /* sample stride s >= 1 (default 128) */
-  float rho0;              /* primary target as a multiple of K (default 1.5) */
-  float rho1;              /* secondary target, >= rho0 (default 1.75) */
+  int32_t stride;          /* sample stride s >= 1 (default 256) */
+  float rho0;              /* primary target as a multiple of K (default 2.0) */
+  float rho1;              /* secondary target, >= rho0 (default 2.25) */
   int64_t sample_min_len;  /* rows shorter than this skip sampling (exact boundary) */
   int64_t direct_max;      /* N_alloc at or below which the on-chip direct kernel serves every row */
   int32_t force_kind;      /* TOPK_KIND_*; AUTO lets the planner choose */
   int32_t kv_segments;     /* KV-split segments per row; 0 = planner's choice */
+  int64_t long_len;        /* rows this long or longer use the long_* knobs; 0 = never (default 786432) */
+  int32_t long_stride;     /* default 512 */
+  float long_rho0;         /* default 2.75 */
+  float long_rho1;         /* >= long_rho0, default 3.0 */
 } topk_params;
 
 typedef struct topk_plan_info {

@@ -56,7 +56,9 @@ def test_host_only_calls(lib):
     assert lib.topk_status_string(0) == b"ok"
     assert lib.topk_status_string(-5).startswith(b"workspace allocation")
     d = ets.default_params()
-    assert d["stride"] == 128 and abs(d["rho0"] - 1.5) < 1e-7 and abs(d["rho1"] - 1.75) < 1e-7
+    assert d["stride"] == 256 and d["rho0"] == 2.0 and d["rho1"] == 2.25
+    assert d["long_len"] == 786432 and d["long_stride"] == 512
+    assert d["long_rho0"] == 2.75 and d["long_rho1"] == 3.0
     old = ets.set_params(stride=64)
     try:
         assert ets.get_params()["stride"] == 64
@@ -64,7 +66,8 @@ def test_host_only_calls(lib):
         ets.set_params(**old)
     assert ets.get_params()["stride"] == old["stride"]
     for bad in ({"stride": 0}, {"rho0": 0.5}, {"rho1": 1.0}, {"force_kind": 9},
-                {"sample_min_len": -1}):
+                {"sample_min_len": -1}, {"long_stride": 0}, {"long_len": -1},
+                {"long_rho0": 0.5}, {"long_rho1": 2.5}):
         with pytest.raises(ets.TopKError):
             ets.set_params(**bad)
     assert ets.get_params() == old

@@ -53,15 +53,39 @@ def verify(x, lens, K, got, rows=None):
     return v
 
 
+def sampling_tiers(p, lens, K):
+    """(row mask, stride, T0, T1) of the two sampling tiers under params p:
+    rows of at least long_len elements (when long_len > 0) use the long_*
+    stride and targets, the others the base ones; T = ceil(rho * K) with rho
+    read as FP32, as the library computes it."""
+    lh = np.asarray(lens)
+    def target(rho):
+        return int(np.ceil(np.float64(np.float32(rho)) * K))
+    long_rows = (lh >= p["long_len"]) if p["long_len"] > 0 else np.zeros(lh.shape, bool)
+    return [(~long_rows, p["stride"], target(p["rho0"]), target(p["rho1"])),
+            (long_rows, p["long_stride"], target(p["long_rho0"]), target(p["long_rho1"]))]
+
+
+def oracle_thresholds(p, xh, lh, K, sample_min_len):
+    """The oracle's stage-1/2 quantities, each row under its own tier."""
+    M = lh.shape[0]
+    ref = {"tau": np.zeros((M, 2), np.float32), "count": np.zeros((M, 2), np.int64),
+           "rank": np.zeros((M, 2), np.int64), "path": np.zeros(M, np.int32)}
+    for mask, stride, T0, T1 in sampling_tiers(p, lh, K):
+        if not mask.any():
+            continue
+        part = oracle.thresholds(xh[mask], lh[mask], K, stride, T0, T1, sample_min_len)
+        for k in ref:
+            ref[k][mask] = part[k]
+    return ref
+
+
 def verify_diag(ets, x, lens, K, diag, rows=None, sample_min_len=0):
     """Thresholds, counts and path of sampled rows equal the oracle's."""
     p = ets.get_params()
-    T0 = int(np.ceil(np.float64(np.float32(p["rho0"])) * K))
-    T1 = int(np.ceil(np.float64(np.float32(p["rho1"])) * K))
     if rows is not None:
         x, lens, diag = x[rows], lens[rows], diag[rows]
-    ref = oracle.thresholds(x.cpu().numpy(), lens.cpu().numpy(), K, p["stride"], T0, T1,
-                            sample_min_len)
+    ref = oracle_thresholds(p, x.cpu().numpy(), lens.cpu().numpy(), K, sample_min_len)
     sampled = ref["path"] >= oracle.PATH_TAU0
     assert np.array_equal(diag["path"][sampled], ref["path"][sampled])
     assert np.array_equal(diag["tau0"][sampled], ref["tau"][sampled, 0])
@@ -161,6 +185,26 @@ def test_width_sweep(ets, N, M):
     verify(x, lens, K, got)
 
 
+@pytest.mark.parametrize("kind", ["persistent", "kvsplit"])
+def test_two_sampling_tiers_in_one_batch(params, kind):
+    """Rows on both sides of long_len in one call: each is sampled with its
+    own tier's stride and targets."""
+    ets = params
+    N, M = 65536, 96
+    ets.set_params(sample_min_len=0, long_len=40000, long_stride=96, long_rho0=1.7,
+                   long_rho1=2.6, stride=40, rho0=1.25, rho1=1.5,
+                   force_kind=ets.KIND_PERSISTENT if kind == "persistent" else ets.KIND_KVSPLIT)
+    lens = torch.randint(20000, N + 1, (M,), generator=torch.Generator().manual_seed(12),
+                         dtype=torch.int32)
+    lens[:2] = torch.tensor([40000, 39999], dtype=torch.int32)
+    x = synth.indexer_rows(lens, N, seed=12, device=DEV)
+    got, dg = run(ets, x, lens, diag=True)
+    verify(x, lens, K, got)
+    verify_diag(ets, x, lens, K, dg)
+    tiers = sampling_tiers(ets.get_params(), lens.numpy(), K)
+    assert tiers[0][0].sum() > 10 and tiers[1][0].sum() > 10
+
+
 @pytest.mark.parametrize("stride", [16, 64, 128, 256])
 @pytest.mark.parametrize("kind", ["persistent", "kvsplit"])
 def test_stride_sweep_sampled(params, stride, kind):
@@ -211,8 +255,10 @@ def test_forced_paths_tau1_recovery_overflow(params, kind):
     """Rows built so the proposal underfills (tau1 path, exact recovery) or
     overfills past the on-chip buffer; every row must still be exact."""
     ets = params
+    # the rows are built for stride 128 and targets 1.5K / 1.75K
     ets.set_params(sample_min_len=0, kv_segments=7 if kind == "kvsplit" else 0,
-                   force_kind=ets.KIND_PERSISTENT if kind == "persistent" else ets.KIND_KVSPLIT)
+                   force_kind=ets.KIND_PERSISTENT if kind == "persistent" else ets.KIND_KVSPLIT,
+                   stride=128, rho0=1.5, rho1=1.75, long_len=0)
     L = 65536
     lens = torch.full((1,), L, dtype=torch.int32)
     rows = [
@@ -221,16 +267,20 @@ def test_forced_paths_tau1_recovery_overflow(params, kind):
         synth.strided_high_rows(lens, L, seed=3, stride=128, n_top=0, n_mid=20000,
                                 on_grid=False),                                       # overflow
         synth.strided_high_rows(lens, L, seed=4, stride=128, n_top=10, n_mid=3000),   # tau0
+        synth.strided_high_rows(lens, L, seed=5, stride=128, n_top=0, n_mid=9000,
+                                on_grid=False),                                       # spill
     ]
     x = torch.cat(rows).to(DEV)
-    lens4 = torch.full((4,), L, dtype=torch.int32)
-    got, dg = run(ets, x, lens4, diag=True)
-    verify(x, lens4, K, got)
-    ref = verify_diag(ets, x, lens4, K, dg)
+    lens5 = torch.full((5,), L, dtype=torch.int32)
+    got, dg = run(ets, x, lens5, diag=True)
+    verify(x, lens5, K, got)
+    ref = verify_diag(ets, x, lens5, K, dg)
     assert ref["path"].tolist() == [ets.PATH_TAU1, ets.PATH_RECOVERY, ets.PATH_TAU0,
-                                    ets.PATH_TAU0]
+                                    ets.PATH_TAU0, ets.PATH_TAU0]
     assert dg["flags"][1] & ets.FLAG_RECOVERY
     assert dg["flags"][2] & ets.FLAG_OVERFLOW
+    # more candidates than the on-chip buffer holds, fewer than the spill area adds
+    assert 6144 < dg["count1"][4] <= 16384 and not dg["flags"][4] & ets.FLAG_OVERFLOW
 
 
 @pytest.mark.parametrize("kind", ["direct", "persistent", "kvsplit"])
