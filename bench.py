@@ -134,7 +134,8 @@ def profiled_traffic(kind, valid_bytes):
     """DRAM bytes per launch from the committed ncu capture of this kernel.
 
     profiles/k_persistent_traffic.json holds the DRAM-bytes-per-valid-byte
-    ratio of one capture and a hash of the kernel sources it was taken on;
+    ratio of one capture and a hash of the kernel and planner sources (the
+    planner holds the sampling defaults) it was taken on;
     the figure is reported only while those sources are unchanged (else None).
     """
     import hashlib
@@ -144,7 +145,7 @@ def profiled_traffic(kind, valid_bytes):
     with open(p) as f:
         d = json.load(f)
     h = hashlib.sha256()
-    for name in ("topk_device.cuh", "topk_kernels.cu", "topk_launch.h"):
+    for name in ("topk_device.cuh", "topk_kernels.cu", "topk_launch.h", "topk_api.cu"):
         with open(os.path.join(ROOT, "exact_top_sparse_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     if h.hexdigest()[:16] != d.get("kernel_sources_sha256_16"):
