@@ -22,8 +22,15 @@ namespace {
 constexpr int kVersion = 10000;  // 1.0.0
 constexpr size_t kHdrBytes = 256;
 constexpr int64_t kMinSegment = 32768;  // floats per KV-split segment, at least
-constexpr int kKvWavesPersistent = 6;   // M >= this many resident waves -> persistent
-constexpr int kKvTargetWaves = 12;      // KV-split aims at this many CTA waves
+// Planner crossovers, measured on GB300 over 128K-1M columns and M = 64-2048:
+// with at least two rows per resident CTA the persistent queue balances
+// well; below that, rows of 384K+ elements leave a long tail on the
+// persistent path and are split, and shorter rows are split only when they
+// would leave half the CTAs idle.  KV-split cuts rows into segments of
+// about 256K floats, and into more when that gives fewer CTAs than resident.
+constexpr int kPersistentRowsPerCta = 2;
+constexpr int64_t kKvLongRow = 393216;
+constexpr int64_t kKvSegmentTarget = 262144;
 
 std::mutex g_mu;
 topk_params g_params;
@@ -121,14 +128,17 @@ int make_plan(int64_t M, int64_t N, int32_t K, const topk_params& p, const DevIn
   if (kind == TOPK_KIND_DIRECT && !direct_fits) return TOPK_ERR_ARG;
   if (kind == TOPK_KIND_AUTO) {
     if (N <= p.direct_max && direct_fits) kind = TOPK_KIND_DIRECT;
-    else if (M >= (int64_t)kKvWavesPersistent * resident) kind = TOPK_KIND_PERSISTENT;
-    else kind = TOPK_KIND_KVSPLIT;
+    else if (M >= (int64_t)kPersistentRowsPerCta * resident) kind = TOPK_KIND_PERSISTENT;
+    else if (N >= kKvLongRow || 2 * M < (int64_t)resident) kind = TOPK_KIND_KVSPLIT;
+    else kind = TOPK_KIND_PERSISTENT;
   }
   int segments = 1;
   if (kind == TOPK_KIND_KVSPLIT) {
     int64_t P = p.kv_segments;
     if (P <= 0) {
-      P = ((int64_t)kKvTargetWaves * resident + M - 1) / (M > 0 ? M : 1);
+      const int64_t by_len = (N + kKvSegmentTarget - 1) / kKvSegmentTarget;
+      const int64_t by_fill = ((int64_t)resident + M - 1) / (M > 0 ? M : 1);
+      P = by_len > by_fill ? by_len : by_fill;
       int64_t pmax = N / kMinSegment;
       if (pmax < 1) pmax = 1;
       if (P > pmax) P = pmax;

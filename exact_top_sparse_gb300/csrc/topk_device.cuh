@@ -557,6 +557,46 @@ __device__ __forceinline__ uint32_t tally_candidates(const uint2* cand, const ui
   return c0;
 }
 
+// Producer side of one chunk: wait for stage q % STAGES to be free, then
+// start the bulk copy of chunk c of the 16-byte aligned body [a0, a1).
+__device__ __forceinline__ void ring_issue(Ring& R, const float* __restrict__ row, int64_t a0,
+                                           int64_t a1, uint32_t c, uint32_t& lflags) {
+  const uint32_t q = R.seq + c, s = q % STAGES, use = q / STAGES;
+  if (!mbar_wait(&R.empty[s], (use & 1u) ^ 1u)) lflags |= F_TIMEOUT;
+  const int64_t off = a0 + (int64_t)c * CHUNK_FLOATS;
+  const int64_t n = (a1 - off) < CHUNK_FLOATS ? (a1 - off) : CHUNK_FLOATS;
+  const uint32_t bytes = (uint32_t)(n * 4);
+  fence_proxy_async();
+  mbar_arrive_expect_tx(&R.full[s], bytes);
+  bulk_load(R.buf + (size_t)s * CHUNK_FLOATS, row + off, bytes, &R.full[s], R.policy);
+}
+
+// The 16-byte aligned body [a0, a1) of [start, end) and its chunk count.
+__device__ __forceinline__ uint32_t ring_span(const float* row, int64_t start, int64_t end,
+                                              int64_t* a0, int64_t* a1) {
+  const uintptr_t addr = reinterpret_cast<uintptr_t>(row + start);
+  int64_t b0 = start + (int64_t)(((16u - (uint32_t)(addr & 15u)) & 15u) >> 2);
+  if (b0 > end) b0 = end;
+  *a0 = b0;
+  *a1 = b0 + ((end - b0) & ~(int64_t)3);
+  return (uint32_t)((*a1 - b0 + CHUNK_FLOATS - 1) / CHUNK_FLOATS);
+}
+
+// Starts the first chunks (up to STAGES) of a later scan_pass over
+// [start, end) while the ring is idle, so that they load during the row's
+// sampling.  Every thread calls; returns the number started, which that
+// scan_pass must be given.
+__device__ __forceinline__ uint32_t ring_prime(Ring& R, const float* __restrict__ row,
+                                               int64_t start, int64_t end, uint32_t& lflags) {
+  if (end <= start) return 0;
+  int64_t a0, a1;
+  const uint32_t nchunks = ring_span(row, start, end, &a0, &a1);
+  const uint32_t n = nchunks < (uint32_t)STAGES ? nchunks : (uint32_t)STAGES;
+  if (threadIdx.x == 0)
+    for (uint32_t c = 0; c < n; ++c) ring_issue(R, row, a0, a1, c, lflags);
+  return n;
+}
+
 // The largest admission operand of four scores (raw bits as signed integers
 // when tau1 > +0; keys mapped to signed order otherwise).
 template <bool POS>
@@ -569,35 +609,24 @@ __device__ __forceinline__ int32_t max_operand(const float4& v) {
   return (int32_t)(max(max(fkey(v.x), fkey(v.y)), max(fkey(v.z), fkey(v.w))) ^ 0x80000000u);
 }
 
-// The certify+collect pass over [start, end) of `row`.  Same ring protocol as
+// The certify+collect pass over [start, end) of `row`, whose first `primed`
+// chunks ring_prime already started.  Same ring protocol as
 // ring_pass, with the consumer side shaped for the common case: a full chunk
 // is exactly two float4 per consumer thread, all eight scores are tested with
 // one integer max, the stage is handed back as soon as the loads have fed
 // that test, and only lanes holding an admitted score (rare) append.
 template <bool POS>
 __device__ __forceinline__ void scan_pass(Ring& R, const float* __restrict__ row, int64_t start,
-                                          int64_t end, ScanCollect<POS>& f, uint32_t& lflags) {
+                                          int64_t end, ScanCollect<POS>& f, uint32_t& lflags,
+                                          uint32_t primed) {
   static_assert(CHUNK_FLOATS == 8 * CONSUMERS, "a full chunk is two float4 per consumer");
   const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31u;
   if (end <= start) return;
-  const uintptr_t addr = reinterpret_cast<uintptr_t>(row + start);
-  int64_t a0 = start + (int64_t)(((16u - (uint32_t)(addr & 15u)) & 15u) >> 2);
-  if (a0 > end) a0 = end;
-  const int64_t a1 = a0 + ((end - a0) & ~(int64_t)3);
-  const uint32_t nchunks = (uint32_t)((a1 - a0 + CHUNK_FLOATS - 1) / CHUNK_FLOATS);
+  int64_t a0, a1;
+  const uint32_t nchunks = ring_span(row, start, end, &a0, &a1);
   if (warp == 0) {
-    if (lane == 0) {
-      for (uint32_t c = 0; c < nchunks; ++c) {
-        const uint32_t q = R.seq + c, s = q % STAGES, use = q / STAGES;
-        if (!mbar_wait(&R.empty[s], (use & 1u) ^ 1u)) lflags |= F_TIMEOUT;
-        const int64_t off = a0 + (int64_t)c * CHUNK_FLOATS;
-        const int64_t n = (a1 - off) < CHUNK_FLOATS ? (a1 - off) : CHUNK_FLOATS;
-        const uint32_t bytes = (uint32_t)(n * 4);
-        fence_proxy_async();
-        mbar_arrive_expect_tx(&R.full[s], bytes);
-        bulk_load(R.buf + (size_t)s * CHUNK_FLOATS, row + off, bytes, &R.full[s], R.policy);
-      }
-    }
+    if (lane == 0)
+      for (uint32_t c = primed; c < nchunks; ++c) ring_issue(R, row, a0, a1, c, lflags);
   } else {
     if (warp == 1) {
       // head [start, a0) on lanes 0..2, tail [a1, end) on lanes 4..6
@@ -698,6 +727,42 @@ struct HistF {
     elem(0, fkey(v.w), (vm & 8u) != 0);
   }
 };
+
+// Admits the keys in [lo, hi) and appends (index, key) to the candidate
+// array (shared memory, then the spill area), one shared atomic per lane.
+struct BandCollect {
+  uint32_t lo, hi;
+  uint2* cand;
+  uint2* spill;
+  uint32_t cap;
+  uint32_t* ncand;
+  __device__ __forceinline__ void quad(int64_t i0, float4 v, uint32_t vm) {
+    const uint32_t k[4] = {fkey(v.x), fkey(v.y), fkey(v.z), fkey(v.w)};
+    uint32_t m = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (((vm >> e) & 1u) && k[e] >= lo && k[e] < hi) m |= 1u << e;
+    if (m) {
+      uint32_t pos = atomicAdd(ncand, (uint32_t)__popc(m));
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if ((m >> e) & 1u) {
+          const uint2 ent = make_uint2((uint32_t)(i0 + e), k[e]);
+          if (pos < (uint32_t)CAP) cand[pos] = ent;
+          else if (pos < cap) spill[pos - (uint32_t)CAP] = ent;
+          ++pos;
+        }
+      }
+    }
+  }
+};
+
+// Histogram of candidates [0, n) under `bins`.
+__device__ __forceinline__ void hist_candidates(const uint2* cand, const uint2* spill, uint32_t n,
+                                                const Bins& bins, uint32_t* hist) {
+  for (uint32_t j = threadIdx.x; j < n; j += THREADS)
+    atomicAdd(&hist[bins.digit(cand_at(cand, spill, j).y)], 1u);
+}
 
 // Seeded histogram of the full-row pass rebuilt from the row (keys >= bins.lo)
 // together with C(tau0).

@@ -144,16 +144,16 @@ __device__ void exact_row_stream(const float* row, int64_t len, int32_t* out, in
 // count unless they overflowed.
 __device__ uint32_t scan_collect(const float* row, int64_t s0, int64_t s1, Ring& R,
                                  const RowCarve& c, uint2* spill, uint32_t key0, uint32_t key1,
-                                 const Bins& sb, uint32_t& lflags) {
+                                 const Bins& sb, uint32_t& lflags, uint32_t primed) {
   Shared& S = *c.S;
   const float tau1 = key_to_float(key1);
   const uint32_t cap = spill ? (uint32_t)CAP_ALL : (uint32_t)CAP;
   if (tau1 > 0.0f) {
     ScanCollect<true> f{__float_as_uint(tau1), c.cand, spill, cap, &S.ncand};
-    scan_pass(R, row, s0, s1, f, lflags);
+    scan_pass(R, row, s0, s1, f, lflags, primed);
   } else {
     ScanCollect<false> f{key1, c.cand, spill, cap, &S.ncand};
-    scan_pass(R, row, s0, s1, f, lflags);
+    scan_pass(R, row, s0, s1, f, lflags, primed);
   }
   __syncthreads();
   const uint32_t c0 = tally_candidates(c.cand, spill, min(S.ncand, cap), key0, sb, c.hist);
@@ -164,9 +164,10 @@ __device__ uint32_t scan_collect(const float* row, int64_t s0, int64_t s1, Ring&
 // (c.cand, then `spill`), histogram and counts are ready: refine, or re-read
 // on overflow, or recover.  Returns the row path.
 __device__ int32_t select_after_scan(const float* row, int64_t len, int32_t* out, int32_t K,
-                                     Ring& R, const RowCarve& c, const uint2* spill, uint32_t& C0,
-                                     uint32_t C1, bool overflow, uint32_t key0, uint32_t key1,
-                                     uint32_t kmin, const Bins& sb, uint32_t& lflags) {
+                                     Ring& R, const RowCarve& c, uint2* spill, const SampleSpec& sp,
+                                     uint32_t& C0, uint32_t C1, bool overflow, uint32_t key0,
+                                     uint32_t key1, uint32_t kmin, const Bins& sb,
+                                     uint32_t& lflags) {
   Shared& S = *c.S;
   int32_t path = (C0 >= (uint32_t)K) ? PATH_TAU0 : (C1 >= (uint32_t)K ? PATH_TAU1 : PATH_RECOVERY);
   if (C1 >= (uint32_t)K && !overflow) {
@@ -200,6 +201,32 @@ __device__ int32_t select_after_scan(const float* row, int64_t len, int32_t* out
       const uint32_t j = threadIdx.x + it * THREADS;
       const bool ok = j < C1;
       warp_emit(out, K, ok ? c.cand[j].x : 0u, ok, S, lflags);
+    }
+    __syncthreads();
+    // One pass when it suffices: a lower threshold tau2 from the same view
+    // (rank of the target 2 * T1) admits the band [tau2, tau1); if the band
+    // holds the K - C(tau1) still missing and fits the candidate buffers, it
+    // is refined on chip.  Otherwise the two-pass selection below runs.
+    const uint32_t need = (uint32_t)K - C1;
+    const uint32_t cap = spill ? (uint32_t)CAP_ALL : (uint32_t)CAP;
+    sample_thresholds(row, len, sp.stride, 2u * sp.target1, 2u * sp.target1,
+                      reinterpret_cast<uint32_t*>(c.cand), c.hist, c.list, S);
+    const uint32_t key2 = S.key1;
+    if (key2 < key1) {
+      if (threadIdx.x == 0) S.ncand = 0;
+      __syncthreads();
+      BandCollect bf{key2, key1, c.cand, spill, cap, &S.ncand};
+      ring_pass(R, row, 0, len, bf, lflags);
+      __syncthreads();
+      const uint32_t n2 = S.ncand;
+      if (n2 >= need && n2 <= cap) {
+        const Bins bb = make_bins(key2, key1 - 1u);
+        clear_hist(c.hist);
+        __syncthreads();
+        hist_candidates(c.cand, spill, n2, bb, c.hist);
+        refine(CandSrc{c.cand, spill, n2}, bb, need, c.hist, c.cand, out, K, S, lflags);
+        return path;
+      }
     }
     const Bins rb = recovery_bins(key1, kmin);
     __syncthreads();
@@ -250,6 +277,8 @@ __global__ void __launch_bounds__(THREADS, 2)
       finish_row(S, out, K, lflags, diag, r, PATH_DIRECT, qnan, qnan, 0, 0);
       continue;
     }
+    // the ring is idle: start the row's first chunks before sampling it
+    const uint32_t primed = ring_prime(R, row, 0, len, lflags);
     const SampleSpec sp = sample_spec(P, len);
     sample_thresholds(row, len, sp.stride, sp.target0, sp.target1,
                       reinterpret_cast<uint32_t*>(c.cand), c.hist, c.list, S);
@@ -259,10 +288,10 @@ __global__ void __launch_bounds__(THREADS, 2)
     clear_hist(c.hist);
     if (threadIdx.x == 0) S.ncand = 0;
     __syncthreads();
-    uint32_t C0 = scan_collect(row, 0, len, R, c, spill, key0, key1, sb, lflags);
+    uint32_t C0 = scan_collect(row, 0, len, R, c, spill, key0, key1, sb, lflags, primed);
     const uint32_t C1 = S.ncand;
     __syncthreads();
-    const int32_t path = select_after_scan(row, len, out, K, R, c, spill, C0, C1,
+    const int32_t path = select_after_scan(row, len, out, K, R, c, spill, sp, C0, C1,
                                            C1 > (uint32_t)CAP_ALL, key0, key1, kmin, sb, lflags);
     finish_row(S, out, K, lflags, diag, r, path, key_to_float(key0), key_to_float(key1), C0, C1);
   }
@@ -436,7 +465,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     clear_hist(c.hist);
     if (threadIdx.x == 0) S.ncand = 0;
     __syncthreads();
-    const uint32_t C0 = scan_collect(row, s0, s1, R, c, nullptr, key0, key1, sb, lflags);
+    const uint32_t C0 = scan_collect(row, s0, s1, R, c, nullptr, key0, key1, sb, lflags, 0u);
     const uint32_t nloc = S.ncand;
     if (threadIdx.x == 0) {
       atomicAdd(&h->c0, C0);
@@ -489,8 +518,8 @@ __global__ void __launch_bounds__(THREADS, 2)
   }
   __syncthreads();
   const int32_t path =
-      select_after_scan(row, len, out, K, R, c, gcand + CAP, C0, C1, overflow, key0, key1, kmin,
-                        sb, lflags);
+      select_after_scan(row, len, out, K, R, c, gcand + CAP, sample_spec(P, len), C0, C1, overflow,
+                        key0, key1, kmin, sb, lflags);
   finish_row(S, out, K, lflags, diag, r, path, key_to_float(key0), key_to_float(key1), C0, C1);
 }
 

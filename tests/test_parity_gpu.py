@@ -252,8 +252,9 @@ def test_uniform_rows(params, kind):
 
 @pytest.mark.parametrize("kind", ["persistent", "kvsplit"])
 def test_forced_paths_tau1_recovery_overflow(params, kind):
-    """Rows built so the proposal underfills (tau1 path, exact recovery) or
-    overfills past the on-chip buffer; every row must still be exact."""
+    """Rows built so the proposal underfills (tau1 path, exact recovery in one
+    band pass or in two passes) or overfills past the on-chip buffer (spill
+    area, overflow); every row must still be exact."""
     ets = params
     # the rows are built for stride 128 and targets 1.5K / 1.75K
     ets.set_params(sample_min_len=0, kv_segments=7 if kind == "kvsplit" else 0,
@@ -269,15 +270,16 @@ def test_forced_paths_tau1_recovery_overflow(params, kind):
         synth.strided_high_rows(lens, L, seed=4, stride=128, n_top=10, n_mid=3000),   # tau0
         synth.strided_high_rows(lens, L, seed=5, stride=128, n_top=0, n_mid=9000,
                                 on_grid=False),                                       # spill
-    ]
+        synth.strided_high_rows(lens, L, seed=6, stride=128, n_top=80, n_mid=2100),   # recovery,
+    ]                                                                                  # two passes
     x = torch.cat(rows).to(DEV)
-    lens5 = torch.full((5,), L, dtype=torch.int32)
-    got, dg = run(ets, x, lens5, diag=True)
-    verify(x, lens5, K, got)
-    ref = verify_diag(ets, x, lens5, K, dg)
+    lens6 = torch.full((6,), L, dtype=torch.int32)
+    got, dg = run(ets, x, lens6, diag=True)
+    verify(x, lens6, K, got)
+    ref = verify_diag(ets, x, lens6, K, dg)
     assert ref["path"].tolist() == [ets.PATH_TAU1, ets.PATH_RECOVERY, ets.PATH_TAU0,
-                                    ets.PATH_TAU0, ets.PATH_TAU0]
-    assert dg["flags"][1] & ets.FLAG_RECOVERY
+                                    ets.PATH_TAU0, ets.PATH_TAU0, ets.PATH_RECOVERY]
+    assert dg["flags"][1] & ets.FLAG_RECOVERY and dg["flags"][5] & ets.FLAG_RECOVERY
     assert dg["flags"][2] & ets.FLAG_OVERFLOW
     # more candidates than the on-chip buffer holds, fewer than the spill area adds
     assert 6144 < dg["count1"][4] <= 16384 and not dg["flags"][4] & ets.FLAG_OVERFLOW
@@ -432,3 +434,7 @@ def test_plan_kinds(ets):
     assert ets.plan(8192, 1048576, K)["kind"] == "persistent"
     p = ets.plan(512, 1048576, K)
     assert p["kind"] == "kvsplit" and p["segments"] > 1
+    sms = p["sm_count"]
+    assert ets.plan(512, 131072, K)["kind"] == "persistent"   # short rows: split only when tiny
+    assert ets.plan(sms // 4, 131072, K)["kind"] == "kvsplit"
+    assert ets.plan(4 * sms, 1048576, K)["kind"] == "persistent"

@@ -60,3 +60,22 @@ def test_strided_rows_drive_the_intended_paths():
     assert p[0]["path"][0] == oracle.PATH_TAU1
     assert p[1]["path"][0] == oracle.PATH_RECOVERY
     assert p[2]["path"][0] == oracle.PATH_TAU0 and p[2]["count"][0, 1] > 20000
+
+
+def test_recovery_rows_take_one_pass_or_fall_back():
+    """The library's recovery first tries the band between tau1 and a lower
+    threshold tau2 of the same view (target 2 * T1).  Row `one` (40 lifted
+    grid values) has enough scores above tau2 for that band to finish the
+    row; row `two` (80 lifted values) does not, so the two-pass selection
+    runs.  Both rows underfill tau1."""
+    L, s, K, T1 = 65536, 128, 2048, 3584
+    lens = torch.full((1,), L, dtype=torch.int32)
+    one = synth.strided_high_rows(lens, L, seed=2, stride=s, n_top=40, n_mid=2100)
+    two = synth.strided_high_rows(lens, L, seed=6, stride=s, n_top=80, n_mid=2100)
+    for x, enough in ((one, True), (two, False)):
+        xh, lh = x.numpy(), np.array([L], np.int32)
+        p1 = oracle.thresholds(xh, lh, K, s, 3072, T1, 0)
+        p2 = oracle.thresholds(xh, lh, K, s, 2 * T1, 2 * T1, 0)
+        assert p1["path"][0] == oracle.PATH_RECOVERY
+        assert (p2["count"][0, 1] >= K) == enough
+
