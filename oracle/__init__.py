@@ -13,10 +13,15 @@ Long-Context Sparse Attention"):
     section 问题二 (Fig. 4 stages 1-2), and codexqa.cn section
     "采样不是处处都该开" (stride 128, targets 1.5K / 1.75K).
 
+  * indexer scores (the stage that produces the rows) -- xllm-io review of
+    LiteTopK, section "核心公式", eq. (1).
+
 Parity status: the selection, the boundary values and the checker are pinned
 by brute force, closed forms and hand-built tie rows in tests/.  The
 thresholds are pinned by closed forms on strictly monotone rows; the rank rule
 itself (ceil(T * n_s / len)) is a reading of the pages, which do not print it.
+The indexer scores are pinned by a hand-derived case, the one-hot closed form,
+invariances of eq. (1) and exact dense products on tiny integer inputs.
 """
 import ctypes
 import os
@@ -56,6 +61,9 @@ def _bind(path):
     lib.oracle_thresholds.argtypes = [vp, vp, i64, i64, i32, i32, i32, i32, i64,
                                       vp, vp, vp, vp, ctypes.c_int]
     lib.oracle_thresholds.restype = ctypes.c_int
+    lib.oracle_index_scores.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, vp, i64, vp, vp,
+                                        ctypes.c_int]
+    lib.oracle_index_scores.restype = ctypes.c_int
     lib.oracle_default_threads.argtypes = []
     lib.oracle_default_threads.restype = ctypes.c_int
     return lib
@@ -182,3 +190,35 @@ def compare(scores, row_lens, K: int, got, threads: int = 0):
     _, _, tied = boundary(scores, row_lens, K, threads)
     mism = np.any(np.sort(got, axis=1) != np.sort(ref, axis=1), axis=1) & ~tied
     return {"check": codes, "tied": tied, "set_mismatch": mism}
+
+
+def index_scores(q_bits, k_bits, w, ts, ss, threads: int = 0):
+    """Indexer scores I[t, s] of eq. (1) (xllm-io LiteTopK review, "核心公式")
+    at the pairs (ts[i], ss[i]), in double.
+
+    q_bits: uint16 [T, H, D] and k_bits: uint16 [S, D], raw bfloat16 patterns;
+    w: float32 [T, H].  Returns (value, magnitude), both float64 [n]:
+    magnitude = sum_j |w_tj| * sum_d |q_tjd * k_sd|, the scale of the rounding
+    error of a lower-precision evaluation.
+    """
+    q_bits = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    k_bits = np.ascontiguousarray(k_bits, dtype=np.uint16)
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    if q_bits.ndim != 3 or k_bits.ndim != 2 or w.shape != q_bits.shape[:2]:
+        raise ValueError("need q [T, H, D], k [S, D], w [T, H]")
+    T, H, D = q_bits.shape
+    if k_bits.shape[1] != D:
+        raise ValueError("q and k disagree on D")
+    ts = np.ascontiguousarray(ts, dtype=np.int64)
+    ss = np.ascontiguousarray(ss, dtype=np.int64)
+    if ts.shape != ss.shape or ts.ndim != 1:
+        raise ValueError("ts and ss must be 1-D of one length")
+    n = ts.shape[0]
+    value = np.empty(n, dtype=np.float64)
+    mag = np.empty(n, dtype=np.float64)
+    rc = _load().oracle_index_scores(_p(q_bits), _p(k_bits), _p(w), T, k_bits.shape[0], H, D,
+                                     _p(ts), _p(ss), n, _p(value), _p(mag), threads)
+    if rc != 0:
+        raise ValueError("oracle_index_scores: bad arguments")
+    return value, mag
+

@@ -30,6 +30,9 @@
 //    here is r = ceil(T * n_s / len) clamped to [1, n_s], with samples at
 //    positions 0, s, 2s, ... below len and n_s = ceil(len / s).
 //
+//  * The indexer scores that feed the selector: eq. (1) of the xllm-io
+//    review of LiteTopK, section "核心公式" (see oracle_index_scores).
+//
 // All comparisons are plain C++ float comparisons (no bit tricks).  NaN is not
 // a supported input.
 //
@@ -284,6 +287,53 @@ int oracle_thresholds(const float* scores, const int32_t* row_lens, int64_t M, i
       cnt[2 * r] = c0;
       cnt[2 * r + 1] = c1;
       path[r] = (c0 >= K) ? 2 : (c1 >= K) ? 3 : 4;
+    }
+  });
+  return 0;
+}
+
+// Indexer scores (the score stage that produces the rows the selector
+// reads), the plain definition of eq. (1) in the xllm-io review of LiteTopK,
+// section "核心公式":
+//   I[t][s] = sum over heads j of w[t][j] * ReLU( dot(q[t][j][:], k[s][:]) ).
+// q is [T][H][D] and k is [S][D], both bfloat16 given as raw 16-bit patterns
+// (a bfloat16 is the upper half of an IEEE binary32, so widening is exact);
+// w is [T][H] float.  Everything is accumulated in double.  For each of the
+// n requested pairs (ts[i], ss[i]) writes value[i] = I and magnitude[i] =
+// sum_j |w[t][j]| * sum_d |q[t][j][d] * k[s][d]|, the scale against which a
+// lower-precision evaluation's rounding error is measured.  Returns 0, or -1
+// on bad arguments.
+static double bf16_to_double(uint16_t b) {
+  const uint32_t u = (uint32_t)b << 16;
+  float f;
+  std::memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+int oracle_index_scores(const uint16_t* q, const uint16_t* k, const float* w, int64_t T, int64_t S,
+                        int64_t H, int64_t D, const int64_t* ts, const int64_t* ss, int64_t n,
+                        double* value, double* magnitude, int threads) {
+  if (T < 0 || S < 0 || H < 1 || D < 1 || n < 0) return -1;
+  if (n > 0 && (!q || !k || !w || !ts || !ss || !value || !magnitude)) return -1;
+  for (int64_t i = 0; i < n; ++i)
+    if (ts[i] < 0 || ts[i] >= T || ss[i] < 0 || ss[i] >= S) return -1;
+  parallel_rows(n, threads, [&](int64_t i0, int64_t i1) {
+    for (int64_t i = i0; i < i1; ++i) {
+      const int64_t t = ts[i], sidx = ss[i];
+      double acc = 0.0, mag = 0.0;
+      for (int64_t j = 0; j < H; ++j) {
+        double dot = 0.0, adot = 0.0;
+        for (int64_t d = 0; d < D; ++d) {
+          const double prod = bf16_to_double(q[(t * H + j) * D + d]) * bf16_to_double(k[sidx * D + d]);
+          dot += prod;
+          adot += std::fabs(prod);
+        }
+        const double wj = (double)w[t * H + j];
+        acc += wj * (dot > 0.0 ? dot : 0.0);
+        mag += std::fabs(wj) * adot;
+      }
+      value[i] = acc;
+      magnitude[i] = mag;
     }
   });
   return 0;

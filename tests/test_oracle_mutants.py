@@ -5,7 +5,8 @@ into a temporary library (on the CPU; nothing here touches the CUDA selector).
 The pin tests in test_oracle_pins.py are then run against the mutant, and at
 least one of them must fail.  This shows that a plausible slip in the oracle
 (a flipped comparison, a wrong tie-break, an off-by-one in the rank rule, a
-strict/inclusive mix-up in the counts or the checker) would not go unnoticed.
+strict/inclusive mix-up in the counts or the checker, a dropped or misplaced
+ReLU or a transposed operand in the indexer scores) would not go unnoticed.
 """
 import os
 import subprocess
@@ -14,6 +15,7 @@ import pytest
 
 import oracle
 from oracle import build as obuild
+from tests import test_oracle_index_scores as score_pins
 from tests import test_oracle_pins as pins
 
 MUTANTS = {
@@ -29,6 +31,11 @@ MUTANTS = {
                       "for (int64_t i = 1; i < L; i += stride) samp.push_back(v[i]);"),
     "boundary_off_by_one": ("const float b = vals[(size_t)K];", "const float b = vals[(size_t)K - 1];"),
     "len_not_clamped_high": ("if (v > n_alloc) v = n_alloc;", ""),
+    "score_no_relu": ("acc += wj * (dot > 0.0 ? dot : 0.0);", "acc += wj * dot;"),
+    "score_relu_after_sum": ("acc += wj * (dot > 0.0 ? dot : 0.0);", "acc += wj * dot;\n        if (j == H - 1 && acc < 0.0) acc = 0.0;"),
+    "score_w_transposed": ("const double wj = (double)w[t * H + j];", "const double wj = (double)w[j * T + t];"),
+    "score_k_wrong_row": ("bf16_to_double(k[sidx * D + d]);", "bf16_to_double(k[t * D + d]);"),
+    "score_magnitude_signed": ("mag += std::fabs(wj) * adot;", "mag += wj * adot;"),
 }
 
 
@@ -51,6 +58,10 @@ def _run_all_pins():
     pins.test_threshold_paths_hand_built_tau1_and_recovery()
     pins.test_threshold_paths_sentinel_and_direct()
     pins.test_certification_invariants_random_rows()
+    score_pins.test_golden_case()
+    score_pins.test_one_hot_closed_form()
+    score_pins.test_invariances()
+    score_pins.test_dense_product_tiny()
 
 
 def test_unmutated_oracle_passes_every_pin():
