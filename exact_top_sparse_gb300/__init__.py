@@ -22,7 +22,7 @@ TOPK_OK = 0
 STATUS_NAMES = {
     0: "TOPK_OK", -1: "TOPK_ERR_ARG", -2: "TOPK_ERR_ALIGN", -3: "TOPK_ERR_WORKSPACE",
     -4: "TOPK_ERR_CUDA", -5: "TOPK_ERR_CAPTURE_ALLOC", -6: "TOPK_ERR_UNSUPPORTED_K",
-    -7: "TOPK_ERR_NO_DEVICE",
+    -7: "TOPK_ERR_NO_DEVICE", -8: "TOPK_ERR_UNSUPPORTED_SHAPE",
 }
 K_MAX = 4096
 
@@ -66,7 +66,8 @@ class PlanInfo(ctypes.Structure):
 EXPORTS = ("topk_ragged", "topk_ragged_diag", "topk_ragged_ws", "topk_workspace_bytes",
            "topk_ragged_host", "topk_plan", "topk_set_params", "topk_get_params",
            "topk_default_params", "topk_read_status", "topk_release_workspaces",
-           "topk_status_string", "topk_version", "topk_ragged_noalloc")
+           "topk_status_string", "topk_version", "topk_ragged_noalloc",
+           "topk_index_scores", "topk_index_topk", "topk_index_read_status")
 NOALLOC_MAX_ROWS = 64
 
 _lib = None
@@ -88,6 +89,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.topk_ragged_diag.argtypes = [vp, vp, i64, i64, i32, vp, vp, vp]
     lib.topk_ragged_ws.argtypes = [vp, vp, i64, i64, i32, vp, vp, sz, vp]
     lib.topk_ragged_noalloc.argtypes = [vp, vp, i64, i64, i32, vp, vp]
+    lib.topk_index_scores.argtypes = [vp, vp, vp, i64, i64, i32, i32, vp, vp, i64, vp]
+    lib.topk_index_topk.argtypes = [vp, vp, vp, i64, i64, i32, i32, vp, vp, i64, i32, vp, vp]
+    lib.topk_index_read_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     lib.topk_workspace_bytes.argtypes = [i64, i64, i32]
     lib.topk_workspace_bytes.restype = sz
     lib.topk_ragged_host.argtypes = [vp, vp, i64, i64, i32, vp, i64]
@@ -103,7 +107,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.topk_status_string.restype = ctypes.c_char_p
     lib.topk_version.argtypes = []
     for name in ("topk_ragged", "topk_ragged_diag", "topk_ragged_ws", "topk_ragged_host",
-                 "topk_ragged_noalloc",
+                 "topk_ragged_noalloc", "topk_index_scores", "topk_index_topk",
+                 "topk_index_read_status",
                  "topk_plan", "topk_set_params", "topk_get_params", "topk_read_status",
                  "topk_version"):
         getattr(lib, name).restype = ctypes.c_int
@@ -266,3 +271,76 @@ def release_workspaces() -> None:
 
 def version() -> int:
     return int(load_library().topk_version())
+
+
+def _index_inputs(q, k, w, row_lens, scores):
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
+                        ("w", w, torch.float32)):
+        if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == dt and t.is_contiguous()):
+            raise TypeError("%s must be a contiguous CUDA %s tensor" % (name, dt))
+    if q.dim() != 3 or k.dim() != 2 or w.dim() != 2:
+        raise TypeError("need q [T, H, D], k [S, D], w [T, H]")
+    T, H, D = q.shape
+    S = k.shape[0]
+    if k.shape[1] != D or tuple(w.shape) != (T, H):
+        raise TypeError("q, k and w disagree on H or D")
+    if not (k.device == q.device == w.device):
+        raise TypeError("q, k and w must be on one device")
+    if row_lens is not None and not (row_lens.device == q.device and row_lens.dtype == torch.int32
+                                     and tuple(row_lens.shape) == (T,)
+                                     and row_lens.is_contiguous()):
+        raise TypeError("row_lens must be a contiguous int32 [T] tensor on q's device")
+    if scores is None:
+        scores = torch.empty((T, S), dtype=torch.float32, device=q.device)
+    elif not (scores.device == q.device and scores.dtype == torch.float32 and scores.dim() == 2
+              and scores.shape[0] == T and scores.shape[1] >= S and scores.stride(1) == 1
+              and scores.stride(0) == scores.shape[1]):
+        raise TypeError("scores must be a contiguous float32 [T, >= S] tensor on q's device")
+    return T, S, H, D, scores
+
+
+def topk_index_scores(q, k, w, row_lens=None, scores=None, stream=None):
+    """Indexer scores scores[t, s] = sum_j w[t, j] * ReLU(q[t, j] . k[s]) on the
+    tensor cores; q [T, 64, 128] and k [S, 128] bfloat16, w [T, 64] float32.
+    Scores at s >= row_lens[t] are -inf when row_lens is given."""
+    lib = load_library()
+    T, S, H, D, scores = _index_inputs(q, k, w, row_lens, scores)
+    with torch.cuda.device(q.device):
+        rc = lib.topk_index_scores(q.data_ptr(), k.data_ptr(), w.data_ptr(), T, S, H, D,
+                                   row_lens.data_ptr() if row_lens is not None else None,
+                                   scores.data_ptr(), scores.shape[1],
+                                   _stream_handle(q.device, stream))
+    _check(rc, "topk_index_scores")
+    return scores
+
+
+def topk_index_topk(q, k, w, row_lens, K: int = 2048, scores=None, out=None, stream=None):
+    """Scores (as topk_index_scores) then the exact Top-K of every row's valid
+    prefix; returns (scores, out_idx [T, K] int32)."""
+    lib = load_library()
+    if row_lens is None:
+        raise TypeError("row_lens is required")
+    T, S, H, D, scores = _index_inputs(q, k, w, row_lens, scores)
+    if out is None:
+        out = torch.empty((T, K), dtype=torch.int32, device=q.device)
+    elif not (out.device == q.device and out.dtype == torch.int32 and tuple(out.shape) == (T, K)
+              and out.is_contiguous()):
+        raise TypeError("out must be a contiguous int32 [T, K] tensor on q's device")
+    with torch.cuda.device(q.device):
+        rc = lib.topk_index_topk(q.data_ptr(), k.data_ptr(), w.data_ptr(), T, S, H, D,
+                                 row_lens.data_ptr(), scores.data_ptr(), scores.shape[1], K,
+                                 out.data_ptr(), _stream_handle(q.device, stream))
+    _check(rc, "topk_index_topk")
+    return scores, out
+
+
+def index_read_status(device=None, stream=None) -> int:
+    """Read and clear the score kernel's status word (syncs the stream)."""
+    lib = load_library()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    flags = ctypes.c_uint32(0)
+    with torch.cuda.device(dev):
+        _check(lib.topk_index_read_status(_stream_handle(dev, stream), ctypes.byref(flags)),
+               "topk_index_read_status")
+    return int(flags.value)
+

@@ -523,6 +523,7 @@ const char* topk_status_string(int code) {
     case TOPK_ERR_CAPTURE_ALLOC: return "workspace allocation needed during stream capture";
     case TOPK_ERR_UNSUPPORTED_K: return "K larger than TOPK_K_MAX";
     case TOPK_ERR_NO_DEVICE: return "no usable sm_103 device";
+    case TOPK_ERR_UNSUPPORTED_SHAPE: return "indexer-score shape not supported";
     default: return "unknown status";
   }
 }

@@ -150,3 +150,22 @@ def constant_rows(lens: torch.Tensor, N_alloc: int, value: float = 1.0, device="
     x = torch.full((M, N_alloc), float(value), dtype=torch.float32, device=device)
     _mask_suffix(x, lens)
     return x
+
+
+def index_inputs(T: int, S: int, seed: int, H: int = 64, D: int = 128, device="cpu"):
+    """Inputs of the indexer-score stage: q [T, H, D] bfloat16 ~ N(0, 1/128),
+    k [S, D] bfloat16 ~ N(0, 1), w [T, H] float32 ~ U(0, 1/8), and the causal
+    valid lengths len_t = S - T + t + 1 (int32 [T], clamped to [1, S])."""
+    g = _gen(device, seed)
+    q = (torch.randn((T, H, D), generator=g, device=device) * (1.0 / 128.0) ** 0.5).to(torch.bfloat16)
+    k = torch.randn((S, D), generator=g, device=device).to(torch.bfloat16)
+    w = torch.rand((T, H), generator=g, device=device) * 0.125
+    lens = (torch.arange(T, dtype=torch.int64) + (S - T + 1)).clamp(1, S).to(torch.int32)
+    return q, k, w, lens
+
+
+def bf16_bits(x: torch.Tensor):
+    """Raw 16-bit patterns of a bfloat16 tensor as a numpy uint16 array."""
+    import numpy as np
+    return x.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+

@@ -62,7 +62,8 @@ typedef enum topk_status {
   TOPK_ERR_CUDA = -4,           /* a CUDA runtime call failed (allocation, launch, copy) */
   TOPK_ERR_CAPTURE_ALLOC = -5,  /* the call would allocate while `stream` is capturing */
   TOPK_ERR_UNSUPPORTED_K = -6,  /* K > TOPK_K_MAX */
-  TOPK_ERR_NO_DEVICE = -7       /* no usable sm_103 device is current */
+  TOPK_ERR_NO_DEVICE = -7,      /* no usable sm_103 device is current */
+  TOPK_ERR_UNSUPPORTED_SHAPE = -8 /* indexer-score shape outside what the kernel tiles (see below) */
 } topk_status;
 
 /* Largest supported K.  The sampled path is tuned for K = 2048. */
@@ -217,6 +218,41 @@ const char* topk_status_string(int code);
 
 /* Library version as major * 10000 + minor * 100 + patch. */
 int topk_version(void);
+
+/* ---------------------------------------------------------------------------
+ * Indexer scores: the stage that produces the selector's rows (eq. (1) of the
+ * xllm-io review of LiteTopK, section "核心公式"):
+ *   scores[t][s] = sum over heads j of w[t][j] * ReLU( q[t][j] . k[s] )
+ * computed with tcgen05 tensor-core MMAs (bf16 inputs, FP32 accumulation,
+ * FP32 ReLU/weight/head-sum epilogue).
+ *   q        device, bfloat16 bit patterns [T][H][D], 16-byte aligned
+ *   k        device, bfloat16 bit patterns [S][D], 16-byte aligned
+ *   w        device, float [T][H], 16-byte aligned
+ *   row_lens device int32 [T] or NULL: scores[t][s] for s >= row_lens[t]
+ *            (causal suffix) are written as -inf; values must lie in [0, S]
+ *   scores   device, float [T][ld_scores], ld_scores >= S; columns S.. are
+ *            not written
+ * Supported shapes: H == 64, D == 128, T a multiple of 4, S a multiple of
+ * 128 (else TOPK_ERR_UNSUPPORTED_SHAPE); the pointers' alignment is checked
+ * (TOPK_ERR_ALIGN).  Asynchronous on `stream`, no allocation, graph-
+ * capturable.  A bounded internal wait that gives up sets TOPK_FLAG_TIMEOUT
+ * in the status word topk_index_read_status() returns. */
+int topk_index_scores(const uint16_t* q, const uint16_t* k, const float* w, int64_t T, int64_t S,
+                      int32_t H, int32_t D, const int32_t* row_lens, float* scores,
+                      int64_t ld_scores, struct CUstream_st* stream);
+
+/* Scores and exact Top-K in one call: topk_index_scores() into `scores`,
+ * then topk_ragged(scores, row_lens, T, ld_scores, K, out_idx, stream) on the
+ * same stream (two launches; capturable into one CUDA graph after a first
+ * uncaptured call has created the selector's workspace).  row_lens is
+ * required. */
+int topk_index_topk(const uint16_t* q, const uint16_t* k, const float* w, int64_t T, int64_t S,
+                    int32_t H, int32_t D, const int32_t* row_lens, float* scores,
+                    int64_t ld_scores, int32_t K, int32_t* out_idx, struct CUstream_st* stream);
+
+/* Read and clear the score kernel's status word (TOPK_FLAG_TIMEOUT); syncs
+ * the stream. */
+int topk_index_read_status(struct CUstream_st* stream, uint32_t* flags);
 
 #ifdef __cplusplus
 }
