@@ -49,6 +49,10 @@ def parse():
     ap.add_argument("--no-matrix", action="store_true", help="skip the 128K/256K/512K lines")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-chain", action="store_true",
+                    help="skip the indexer-score + Top-K chain (tensor-core) line")
+    ap.add_argument("--chain-T", type=int, default=2048, help="queries of the chain line")
+    ap.add_argument("--chain-S", type=int, default=262144, help="keys of the chain line")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--force-kind", default="auto",
                     choices=["auto", "direct", "persistent", "kvsplit"])
@@ -71,6 +75,72 @@ def measured_peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def measured_bf16_tflops():
+    """Dense bf16 peak for a kernel timed alone (the burst figure)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if "bf16_tflops" in d:
+            return float(d["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
+def chain_leg(ets, dev, stream, reps, T=2048, S=262144, K=2048):
+    """Indexer scores (tcgen05) followed by the exact Top-K, timed with CUDA
+    events on the launching stream; the score kernel's roofline is tensor."""
+    from exact_top_sparse_gb300 import synth
+    q, k, w, lens = synth.index_inputs(T, S, seed=13, device=dev)
+    dl = lens.to(dev)
+    scores = torch.empty((T, S), dtype=torch.float32, device=dev)
+    out = torch.empty((T, K), dtype=torch.int32, device=dev)
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+        stream.synchronize()
+        ts = []
+        for _ in range(reps):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                fn()
+                b.record(stream)
+            stream.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    score_ms = timed(lambda: ets.topk_index_scores(q, k, w, row_lens=dl, scores=scores,
+                                                   stream=stream))
+    chain_ms = timed(lambda: ets.topk_index_topk(q, k, w, dl, K, scores=scores, out=out,
+                                                 stream=stream))
+    status = ets.index_read_status(dev, stream)
+    flops = 2.0 * T * S * 64 * 128
+    peak, kind = measured_bf16_tflops()
+    tflops = flops / (score_ms / 1000.0) / 1e12
+    import oracle
+    rows = np.array([0, T // 3, T - 1])
+    xr = scores[torch.as_tensor(rows, device=dev)].cpu().numpy()
+    v = oracle.compare(xr, lens.numpy()[rows], K, out[torch.as_tensor(rows, device=dev)].cpu().numpy())
+    del scores, q, k
+    torch.cuda.empty_cache()
+    return {
+        "workload": "indexer scores I[t,s] = sum_j w[t,j]*ReLU(q[t,j].k[s]) then exact Top-%d; "
+                    "T=%d queries, S=%d keys, H=64, D=128, bf16 q/k, f32 w and scores, causal "
+                    "lengths S-T+t+1" % (K, T, S),
+        "ms_per_call": chain_ms, "score_ms": score_ms, "topk_ms": chain_ms - score_ms,
+        "rows_per_s": T / (chain_ms / 1000.0), "reps": reps, "gpu_launches_per_call": 2,
+        "status_flags": status,
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": tflops / peak, "peak_kind": kind + " (bf16 dense, burst)",
+                     "flops_per_launch": flops, "kernel": "k_index_scores"},
+        "spot_check": {"rows": int(rows.size), "contract_failures": int((v["check"] != 0).sum()),
+                       "set_mismatches": int(v["set_mismatch"].sum())},
+    }
 
 
 class ClockSampler:
@@ -347,6 +417,17 @@ def run_gb300(args):
             torch.cuda.empty_cache()
         result["matrix_m8192"] = mat
         x = None
+
+    if not args.no_chain and rank == 0:
+        if x is not None:
+            del x
+            x = None
+            torch.cuda.empty_cache()
+        try:
+            result["chain"] = chain_leg(ets, dev, stream, max(5, args.steps // 2),
+                                        T=args.chain_T, S=args.chain_S)
+        except RuntimeError as e:
+            result["chain"] = {"error": str(e)[:200]}
 
     # end to end through the host-buffer C ABI: pinned host rows in, indices out
     if not args.no_e2e and rank == 0:
