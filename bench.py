@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--no-chain", action="store_true",
                     help="skip the indexer-score + Top-K chain (tensor-core) line")
     ap.add_argument("--chain-T", type=int, default=2048, help="queries of the chain line")
+    ap.add_argument("--no-trace", action="store_true",
+                    help="skip the replay of a 430K-token prefill's 71 Top-K calls")
     ap.add_argument("--chain-S", type=int, default=262144, help="keys of the chain line")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--force-kind", default="auto",
@@ -86,6 +88,64 @@ def measured_bf16_tflops():
         if "bf16_tflops" in d:
             return float(d["bf16_tflops"]), "measured"
     return 1900.0, "fallback"
+
+
+def trace_leg(ets, dev, stream, tokens=430 * 1024, K=2048):
+    """Replay the Top-K calls of one synthetic prefill (exact_top_sparse_gb300.trace):
+    first the selector alone over indexer-like score rows of each call's shape,
+    then the whole score -> select chain; each timed as one sequence of calls
+    with CUDA events on the launching stream, after one untimed pass."""
+    from exact_top_sparse_gb300 import synth, trace
+    calls = trace.calls(tokens)
+    W = trace.WORKSPACE_FLOATS
+    buf = torch.empty(W, dtype=torch.float32, device=dev)
+    rows_all = W // 65536
+    synth.indexer_rows(torch.full((rows_all,), 65536, dtype=torch.int32), 65536, seed=17,
+                       out=buf.view(rows_all, 65536))
+    lens_all = torch.arange(1, tokens + 1, dtype=torch.int32, device=dev)
+    outs = torch.empty((max(c.rows for c in calls), K), dtype=torch.int32, device=dev)
+    valid = sum(4.0 * (c.row0 * c.rows + c.rows * (c.rows + 1) / 2.0) for c in calls)
+
+    def run_topk():
+        for c in calls:
+            x = buf[:c.rows * c.width].view(c.rows, c.width)
+            ets.topk_ragged(x, lens_all[c.row0:c.row0 + c.rows], K, out=outs[:c.rows],
+                            stream=stream)
+
+    # every call's width is a multiple of 128 and its rows a multiple of 4
+    assert all(c.width % 128 == 0 and c.rows % 4 == 0 for c in calls)
+    q, k, w, _ = synth.index_inputs(tokens + (-tokens) % 4, tokens + (-tokens) % 128, seed=19,
+                                    device=dev)
+    flops = sum(2.0 * c.rows * c.width * 64 * 128 for c in calls)
+
+    def run_chain():
+        for c in calls:
+            ets.topk_index_topk(q[c.row0:c.row0 + c.rows], k[:c.width],
+                                w[c.row0:c.row0 + c.rows], lens_all[c.row0:c.row0 + c.rows], K,
+                                scores=buf[:c.rows * c.width].view(c.rows, c.width),
+                                out=outs[:c.rows], stream=stream)
+
+    res = {"tokens": tokens, "calls": len(calls), "steps": len({c.step for c in calls}),
+           "workspace_floats": W, "valid_score_bytes": valid}
+    for name, fn in (("topk", run_topk), ("chain", run_chain)):
+        with torch.cuda.stream(stream):
+            fn()
+        stream.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            fn()
+            b.record(stream)
+        stream.synchronize()
+        res[name + "_total_ms"] = a.elapsed_time(b)
+    res["topk_gbps"] = valid / (res["topk_total_ms"] / 1000.0) / 1e9
+    res["score_flops_dense"] = flops
+    res["chain_score_share_ms"] = res["chain_total_ms"] - res["topk_total_ms"]
+    res["status_flags"] = ets.read_status(dev, stream) | ets.index_read_status(dev, stream)
+    del buf, q, k, w
+    torch.cuda.empty_cache()
+    return res
 
 
 def chain_leg(ets, dev, stream, reps, T=2048, S=262144, K=2048):
@@ -428,6 +488,11 @@ def run_gb300(args):
                                         T=args.chain_T, S=args.chain_S)
         except RuntimeError as e:
             result["chain"] = {"error": str(e)[:200]}
+    if not args.no_trace and rank == 0:
+        try:
+            result["trace_430k"] = trace_leg(ets, dev, stream)
+        except RuntimeError as e:
+            result["trace_430k"] = {"error": str(e)[:200]}
 
     # end to end through the host-buffer C ABI: pinned host rows in, indices out
     if not args.no_e2e and rank == 0:

@@ -145,6 +145,21 @@ __device__ __forceinline__ void unit_coords(const Args& a, int32_t u, int32_t* q
   *t1 = min(*t0 + CHUNK_TILES, a.n_tiles);
 }
 
+// End of the key tiles a unit must compute: tiles that start at or past every
+// one of its queries' valid length hold only -inf and skip the MMA.
+__device__ __forceinline__ int32_t unit_end(const Args& a, int32_t qb, int32_t t0, int32_t t1) {
+  if (!a.lens) return t1;
+  int64_t mx = 0;
+#pragma unroll
+  for (int q = 0; q < QB; ++q) {
+    int64_t l = a.lens[qb * QB + q];
+    l = l < 0 ? 0 : (l > a.S ? a.S : l);
+    mx = l > mx ? l : mx;
+  }
+  const int32_t te = (int32_t)((mx + KT - 1) / KT);
+  return te < t0 ? t0 : (te > t1 ? t1 : te);
+}
+
 __global__ void __launch_bounds__(THREADS, 1)
     k_index_scores(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_q,
                    Args a) {
@@ -192,15 +207,18 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
-      uint32_t aseq = 0, ui = 0;
-      for (int32_t u = blockIdx.x; u < a.n_units && !*abort_flag; u += gridDim.x, ++ui) {
+      uint32_t aseq = 0, ui = 0;  // ui counts the units that compute
+      for (int32_t u = blockIdx.x; u < a.n_units && !*abort_flag; u += gridDim.x) {
         int32_t qb, t0, t1;
         unit_coords(a, u, &qb, &t0, &t1);
+        const int32_t te = unit_end(a, qb, t0, t1);
+        if (te == t0) continue;
         if (ui > 0 && !bar_wait(b_empty, (ui - 1) & 1u, abort_flag)) break;
+        ++ui;
         bar_expect(b_full, B_BYTES);
         tma_2d(base + OFF_B, &map_q, 0, qb * NCOL, b_full);
         tma_2d(base + OFF_B + B_HALF, &map_q, 64, qb * NCOL, b_full);
-        for (int32_t t = t0; t < t1; ++t, ++aseq) {
+        for (int32_t t = t0; t < te; ++t, ++aseq) {
           const uint32_t s = aseq % STAGES, use = aseq / STAGES;
           if (!bar_wait(a_empty(s), (use & 1u) ^ 1u, abort_flag)) break;
           const uint32_t dst = base + OFF_A + s * A_BYTES;
@@ -214,12 +232,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       uint32_t aseq = 0, accseq = 0, ui = 0;
-      for (int32_t u = blockIdx.x; u < a.n_units && !*abort_flag; u += gridDim.x, ++ui) {
+      for (int32_t u = blockIdx.x; u < a.n_units && !*abort_flag; u += gridDim.x) {
         int32_t qb, t0, t1;
         unit_coords(a, u, &qb, &t0, &t1);
+        const int32_t te = unit_end(a, qb, t0, t1);
+        if (te == t0) continue;
         if (!bar_wait(b_full, ui & 1u, abort_flag)) break;
+        ++ui;
         bool ok = true;
-        for (int32_t t = t0; t < t1; ++t, ++aseq, ++accseq) {
+        for (int32_t t = t0; t < te; ++t, ++aseq, ++accseq) {
           const uint32_t s = aseq % STAGES, buf = accseq & 1u;
           if (!bar_wait(a_full(s), (aseq / STAGES) & 1u, abort_flag) ||
               !bar_wait(acc_empty(buf), ((accseq >> 1) & 1u) ^ 1u, abort_flag)) {
@@ -275,7 +296,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       int32_t lenq[QB];
 #pragma unroll
       for (int q = 0; q < QB; ++q) lenq[q] = a.lens ? a.lens[qb * QB + q] : a.S;
-      for (int32_t t = t0; t < t1; ++t, ++accseq) {
+      const int32_t te = unit_end(a, qb, t0, t1);
+      // tiles past every query's valid length: -inf, no accumulator
+      for (int32_t t = te; t < t1; ++t) {
+        const int64_t key = (int64_t)t * KT + row;
+#pragma unroll
+        for (int q = 0; q < QB; ++q) a.out[((int64_t)qb * QB + q) * a.ld + key] = -INFINITY;
+      }
+      for (int32_t t = t0; t < te; ++t, ++accseq) {
         const uint32_t buf = accseq & 1u;
         const bool got = bar_wait(acc_full(buf), (accseq >> 1) & 1u, abort_flag);
         if (!__all_sync(0xffffffffu, got)) {  // keep the warp converged for tcgen05.ld

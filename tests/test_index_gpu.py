@@ -72,6 +72,28 @@ def test_several_units_and_causal_mask(ets):
     assert bool(torch.isfinite(got[~masked]).all())
 
 
+def test_short_valid_lengths_skip_tiles(ets):
+    """Query blocks whose valid lengths end early compute only the tiles they
+    need; the rest of each row, and rows of length 0, are exactly -inf."""
+    T, S = 48, 8192
+    q, k, w, _ = synth.index_inputs(T, S, seed=8, device=DEV)
+    lens = torch.tensor([0, 0, 0, 0] + [1, 2, 127, 128] + [129, 300, 1000, 4096]
+                        + [8192 - 5 * i for i in range(36)], dtype=torch.int32)
+    dl = lens.to(DEV)
+    got = ets.topk_index_scores(q, k, w, row_lens=dl)
+    torch.cuda.synchronize()
+    ts, ss = [], []
+    for t in range(T):
+        L = int(lens[t])
+        if L > 0:
+            cols = np.unique(np.concatenate([np.arange(min(L, 40)), np.arange(max(0, L - 40), L)]))
+            ts.append(np.full(cols.size, t)); ss.append(cols)
+    check_pairs(q, k, w, got, np.concatenate(ts), np.concatenate(ss))
+    cols = torch.arange(S, device=DEV)
+    masked = cols[None, :] >= dl[:, None]
+    assert bool(torch.isneginf(got[masked]).all()) and bool(torch.isfinite(got[~masked]).all())
+
+
 def test_full_size_scores_sampled(ets):
     """T = 2048 queries over S = 262144 keys (the chain's configuration):
     sampled pairs against the oracle, the causal suffix everywhere."""
