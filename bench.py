@@ -70,6 +70,21 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(value: float, ws: int, device) -> float:
+    """The largest `value` over all ranks (the slowest rank's time); a
+    no-op for one rank."""
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    if ws > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rows_per_s(ws: int, M: int, steps: int, total_ms: float) -> float:
+    """Whole-job throughput: every rank selects its own M-row batch per step
+    (weak scaling, no data-path collective), timed by the slowest rank."""
+    return ws * M * steps / (total_ms / 1000.0)
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -408,12 +423,9 @@ def run_gb300(args):
     total_ms, per, wall, out = time_steps(ets, x, d_lens, K, args.steps, args.warmup, ws, stream)
     clk = clocks.stop()
 
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if ws > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, ws, dev)
     ms_per_step = total_ms / args.steps
-    rows_per_s = ws * M * args.steps / (total_ms / 1000.0)
+    rows_per_s = job_rows_per_s(ws, M, args.steps, total_ms)
     kern_ms = statistics.mean(per)
     achieved = valid_bytes / (kern_ms / 1000.0) / 1e9
     status = ets.read_status(dev, stream)
