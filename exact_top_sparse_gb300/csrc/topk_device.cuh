@@ -531,6 +531,26 @@ struct ScanCollect {
       }
     }
   }
+  // Appends the admitted scores of two groups of four (elements ia.. of va
+  // when ha, ib.. of vb when hb) with one shared-memory atomic, visiting only
+  // the admitted elements.
+  __device__ __forceinline__ void lane_put2(int64_t ia, const float4& va, bool ha, int64_t ib,
+                                            const float4& vb, bool hb) const {
+    uint32_t m = (ha ? admit_mask(va) : 0u) | ((hb ? admit_mask(vb) : 0u) << 4);
+    if (!m) return;
+    uint32_t pos = atomicAdd(ncand, (uint32_t)__popc(m));
+    do {
+      const uint32_t e = (uint32_t)__ffs(m) - 1u;
+      m &= m - 1u;
+      const float4 v = e < 4u ? va : vb;
+      const uint32_t k = e & 3u;
+      const float x = k == 0u ? v.x : (k == 1u ? v.y : (k == 2u ? v.z : v.w));
+      const uint2 ent = make_uint2((uint32_t)((e < 4u ? ia : ib) + k), fkey(x));
+      if (pos < (uint32_t)CAP) cand[pos] = ent;
+      else if (pos < cap) spill[pos - (uint32_t)CAP] = ent;
+      ++pos;
+    } while (m);
+  }
   // Appends the admitted scores among the elements of v selected by vm
   // (element i0 + e is lane e): one shared-memory atomic reserves this lane's
   // slots.
@@ -655,8 +675,8 @@ __device__ __forceinline__ void scan_pass(Ring& R, const float* __restrict__ row
       // both loads have fed m0/m1: hand the stage back before any appends
       __syncwarp();
       if (lane == 0) mbar_arrive(&R.empty[s]);
-      if (ok0 && m0 >= thr) f.lane_put(off + 4 * (int64_t)j0, v0, 0xfu);
-      if (ok1 && m1 >= thr) f.lane_put(off + 4 * (int64_t)j1, v1, 0xfu);
+      const bool h0 = ok0 && m0 >= thr, h1 = ok1 && m1 >= thr;
+      if (h0 || h1) f.lane_put2(off + 4 * (int64_t)j0, v0, h0, off + 4 * (int64_t)j1, v1, h1);
     }
   }
   R.seq += nchunks;
