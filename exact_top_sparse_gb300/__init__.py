@@ -67,7 +67,8 @@ EXPORTS = ("topk_ragged", "topk_ragged_diag", "topk_ragged_ws", "topk_workspace_
            "topk_ragged_host", "topk_plan", "topk_set_params", "topk_get_params",
            "topk_default_params", "topk_read_status", "topk_release_workspaces",
            "topk_status_string", "topk_version", "topk_ragged_noalloc",
-           "topk_index_scores", "topk_index_topk", "topk_index_read_status")
+           "topk_index_scores", "topk_index_topk", "topk_index_read_status",
+           "topk_ragged_bf16", "topk_ragged_bf16_diag")
 NOALLOC_MAX_ROWS = 64
 
 _lib = None
@@ -89,6 +90,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.topk_ragged_diag.argtypes = [vp, vp, i64, i64, i32, vp, vp, vp]
     lib.topk_ragged_ws.argtypes = [vp, vp, i64, i64, i32, vp, vp, sz, vp]
     lib.topk_ragged_noalloc.argtypes = [vp, vp, i64, i64, i32, vp, vp]
+    lib.topk_ragged_bf16.argtypes = [vp, vp, i64, i64, i32, vp, vp]
+    lib.topk_ragged_bf16_diag.argtypes = [vp, vp, i64, i64, i32, vp, vp, vp]
     lib.topk_index_scores.argtypes = [vp, vp, vp, i64, i64, i32, i32, vp, vp, i64, vp]
     lib.topk_index_topk.argtypes = [vp, vp, vp, i64, i64, i32, i32, vp, vp, i64, i32, vp, vp]
     lib.topk_index_read_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
@@ -108,6 +111,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.topk_version.argtypes = []
     for name in ("topk_ragged", "topk_ragged_diag", "topk_ragged_ws", "topk_ragged_host",
                  "topk_ragged_noalloc", "topk_index_scores", "topk_index_topk",
+                 "topk_ragged_bf16", "topk_ragged_bf16_diag",
                  "topk_index_read_status",
                  "topk_plan", "topk_set_params", "topk_get_params", "topk_read_status",
                  "topk_version"):
@@ -126,11 +130,13 @@ def _stream_handle(device, stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _inputs(scores, row_lens, K, out):
+def _inputs(scores, row_lens, K, out, allow_bf16=False):
     if not (isinstance(scores, torch.Tensor) and scores.is_cuda):
         raise TypeError("scores must be a CUDA tensor")
-    if scores.dtype != torch.float32 or scores.dim() != 2:
-        raise TypeError("scores must be a 2-D float32 tensor [M, N_alloc]")
+    ok_types = (torch.float32, torch.bfloat16) if allow_bf16 else (torch.float32,)
+    if scores.dtype not in ok_types or scores.dim() != 2:
+        raise TypeError("scores must be a 2-D %s tensor [M, N_alloc]"
+                        % " or ".join(str(t).replace("torch.", "") for t in ok_types))
     if not scores.is_contiguous():
         raise ValueError("scores must be contiguous (row stride N_alloc)")
     if not (isinstance(row_lens, torch.Tensor) and row_lens.device == scores.device
@@ -148,12 +154,14 @@ def _inputs(scores, row_lens, K, out):
 
 def topk_ragged(scores: torch.Tensor, row_lens: torch.Tensor, K: int = 2048,
                 out: torch.Tensor = None, stream=None) -> torch.Tensor:
-    """Exact Top-K of every row's valid prefix; [M, K] int32, unsorted, -1 padded."""
+    """Exact Top-K of every row's valid prefix; [M, K] int32, unsorted, -1 padded.
+    Scores are float32, or bfloat16 (selected as their exact float32 values)."""
     lib = load_library()
-    M, N, out = _inputs(scores, row_lens, K, out)
+    M, N, out = _inputs(scores, row_lens, K, out, allow_bf16=True)
+    fn = lib.topk_ragged_bf16 if scores.dtype == torch.bfloat16 else lib.topk_ragged
     with torch.cuda.device(scores.device):
-        rc = lib.topk_ragged(scores.data_ptr(), row_lens.data_ptr(), M, N, K, out.data_ptr(),
-                             _stream_handle(scores.device, stream))
+        rc = fn(scores.data_ptr(), row_lens.data_ptr(), M, N, K, out.data_ptr(),
+                _stream_handle(scores.device, stream))
     _check(rc, "topk_ragged")
     return out
 
@@ -161,12 +169,12 @@ def topk_ragged(scores: torch.Tensor, row_lens: torch.Tensor, K: int = 2048,
 def topk_ragged_diag(scores, row_lens, K: int = 2048, out=None, stream=None):
     """topk_ragged plus per-row diagnostics (numpy structured array, host copy)."""
     lib = load_library()
-    M, N, out = _inputs(scores, row_lens, K, out)
+    M, N, out = _inputs(scores, row_lens, K, out, allow_bf16=True)
     diag = torch.empty(M * DIAG_DTYPE.itemsize, dtype=torch.uint8, device=scores.device)
+    fn = lib.topk_ragged_bf16_diag if scores.dtype == torch.bfloat16 else lib.topk_ragged_diag
     with torch.cuda.device(scores.device):
-        rc = lib.topk_ragged_diag(scores.data_ptr(), row_lens.data_ptr(), M, N, K,
-                                  out.data_ptr(), diag.data_ptr(),
-                                  _stream_handle(scores.device, stream))
+        rc = fn(scores.data_ptr(), row_lens.data_ptr(), M, N, K, out.data_ptr(), diag.data_ptr(),
+                _stream_handle(scores.device, stream))
     _check(rc, "topk_ragged_diag")
     return out, diag.cpu().numpy().view(DIAG_DTYPE)
 

@@ -120,10 +120,11 @@ int check_sizes(int64_t M, int64_t N, int32_t K) {
   return TOPK_OK;
 }
 
-int make_plan(int64_t M, int64_t N, int32_t K, const topk_params& p, const DevInfo& d, Plan* pl) {
+int make_plan(int64_t M, int64_t N, int32_t K, const topk_params& p, const DevInfo& d, Plan* pl,
+              int elem_bytes = 4) {
   (void)K;
   const int resident = d.sm_count * d.occ;
-  const bool direct_fits = tk::direct_smem_bytes(N) <= d.optin;
+  const bool direct_fits = tk::direct_smem_bytes(N, elem_bytes) <= d.optin;
   int kind = p.force_kind;
   if (kind == TOPK_KIND_DIRECT && !direct_fits) return TOPK_ERR_ARG;
   if (kind == TOPK_KIND_AUTO) {
@@ -154,7 +155,7 @@ int make_plan(int64_t M, int64_t N, int32_t K, const topk_params& p, const DevIn
   pl->ws = kHdrBytes;
   if (kind == TOPK_KIND_DIRECT) {
     pl->grid = (int)M;
-    pl->smem = tk::direct_smem_bytes(N);
+    pl->smem = tk::direct_smem_bytes(N, elem_bytes);
   } else if (kind == TOPK_KIND_PERSISTENT) {
     pl->grid = (int)(M < resident ? M : resident);
     pl->smem = tk::persistent_smem_bytes();
@@ -167,19 +168,22 @@ int make_plan(int64_t M, int64_t N, int32_t K, const topk_params& p, const DevIn
   return TOPK_OK;
 }
 
-int validate_ptrs(const float* scores, const int32_t* row_lens, int64_t M, int64_t N,
-                  int32_t* out_idx) {
+int validate_ptrs(const void* scores, const int32_t* row_lens, int64_t M, int64_t N,
+                  int32_t* out_idx, int elem_bytes = 4) {
   if (M == 0) return TOPK_OK;
   if (!row_lens || !out_idx) return TOPK_ERR_ARG;
   if (N > 0 && !scores) return TOPK_ERR_ARG;
-  if ((reinterpret_cast<uintptr_t>(scores) & 3u) || (reinterpret_cast<uintptr_t>(out_idx) & 3u) ||
+  if ((reinterpret_cast<uintptr_t>(scores) & (uintptr_t)(elem_bytes - 1)) ||
+      (reinterpret_cast<uintptr_t>(out_idx) & 3u) ||
       (reinterpret_cast<uintptr_t>(row_lens) & 3u))
     return TOPK_ERR_ALIGN;
   return TOPK_OK;
 }
 
-tk::Params kernel_params(int64_t M, int64_t N, int32_t K, const topk_params& p, const Plan& pl) {
+tk::Params kernel_params(int64_t M, int64_t N, int32_t K, const topk_params& p, const Plan& pl,
+                         int elem_bytes = 4) {
   tk::Params P;
+  P.elem_bytes = elem_bytes;
   P.M = M;
   P.N_alloc = N;
   P.K = K;
@@ -197,7 +201,7 @@ tk::Params kernel_params(int64_t M, int64_t N, int32_t K, const topk_params& p, 
   return P;
 }
 
-int launch(const Plan& pl, const tk::Params& P, const float* scores, const int32_t* row_lens,
+int launch(const Plan& pl, const tk::Params& P, const void* scores, const int32_t* row_lens,
            int32_t* out_idx, topk_row_diag* diag, void* ws, cudaStream_t st) {
   tk::RowDiag* d = reinterpret_cast<tk::RowDiag*>(diag);
   cudaError_t e;
@@ -247,12 +251,12 @@ int cached_workspace(int dev, cudaStream_t st, size_t need, void** ptr) {
   return TOPK_OK;
 }
 
-int run(const float* scores, const int32_t* row_lens, int64_t M, int64_t N, int32_t K,
+int run(const void* scores, const int32_t* row_lens, int64_t M, int64_t N, int32_t K,
         int32_t* out_idx, topk_row_diag* diag, void* ws, size_t ws_bytes, bool explicit_ws,
-        cudaStream_t st) {
+        cudaStream_t st, int elem_bytes = 4) {
   int rc = check_sizes(M, N, K);
   if (rc) return rc;
-  rc = validate_ptrs(scores, row_lens, M, N, out_idx);
+  rc = validate_ptrs(scores, row_lens, M, N, out_idx, elem_bytes);
   if (rc) return rc;
   if (M == 0) return TOPK_OK;
   if (explicit_ws) {
@@ -265,7 +269,7 @@ int run(const float* scores, const int32_t* row_lens, int64_t M, int64_t N, int3
   if (rc) return rc;
   const topk_params p = params_snapshot();
   Plan pl;
-  rc = make_plan(M, N, K, p, d, &pl);
+  rc = make_plan(M, N, K, p, d, &pl, elem_bytes);
   if (rc) return rc;
   if (explicit_ws) {
     if (ws_bytes < pl.ws) return TOPK_ERR_WORKSPACE;
@@ -273,7 +277,8 @@ int run(const float* scores, const int32_t* row_lens, int64_t M, int64_t N, int3
     rc = cached_workspace(dev, st, pl.ws, &ws);
     if (rc) return rc;
   }
-  return launch(pl, kernel_params(M, N, K, p, pl), scores, row_lens, out_idx, diag, ws, st);
+  return launch(pl, kernel_params(M, N, K, p, pl, elem_bytes), scores, row_lens, out_idx, diag, ws,
+                st);
 }
 
 }  // namespace
@@ -290,6 +295,18 @@ int topk_ragged_diag(const float* scores, const int32_t* row_lens, int64_t M, in
                      struct CUstream_st* stream) {
   if (M > 0 && !diag) return TOPK_ERR_ARG;
   return run(scores, row_lens, M, N_alloc, K, out_idx, diag, nullptr, 0, false, stream);
+}
+
+int topk_ragged_bf16(const uint16_t* scores, const int32_t* row_lens, int64_t M, int64_t N_alloc,
+                     int32_t K, int32_t* out_idx, struct CUstream_st* stream) {
+  return run(scores, row_lens, M, N_alloc, K, out_idx, nullptr, nullptr, 0, false, stream, 2);
+}
+
+int topk_ragged_bf16_diag(const uint16_t* scores, const int32_t* row_lens, int64_t M,
+                          int64_t N_alloc, int32_t K, int32_t* out_idx, topk_row_diag* diag,
+                          struct CUstream_st* stream) {
+  if (M > 0 && !diag) return TOPK_ERR_ARG;
+  return run(scores, row_lens, M, N_alloc, K, out_idx, diag, nullptr, 0, false, stream, 2);
 }
 
 int topk_ragged_ws(const float* scores, const int32_t* row_lens, int64_t M, int64_t N_alloc,

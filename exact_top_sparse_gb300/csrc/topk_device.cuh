@@ -180,6 +180,43 @@ __device__ __forceinline__ float ld_keep(const float* p, uint64_t policy) {
   return v;
 }
 
+// Score element types: FP32, or bfloat16 given as raw 16-bit patterns.  A
+// bfloat16 is the upper half of a binary32, so widening it is exact and every
+// comparison, key and threshold below works on the widened FP32 value.
+// kPer16: elements per 16 bytes (one vector load of the ring).
+template <class E>
+struct Elem;
+template <>
+struct Elem<float> {
+  static constexpr int kSize = 4, kPer16 = 4;
+  __device__ static __forceinline__ float load(const float* p) { return *p; }
+  __device__ static __forceinline__ float load_keep(const float* p, uint64_t pol) {
+    return ld_keep(p, pol);
+  }
+  // the elements of one 16-byte unit as groups of four widened values
+  __device__ static __forceinline__ void groups(const uint4& u, float4* g) {
+    g[0] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
+                       __uint_as_float(u.w));
+  }
+};
+template <>
+struct Elem<uint16_t> {
+  static constexpr int kSize = 2, kPer16 = 8;
+  __device__ static __forceinline__ float widen(uint32_t b) { return __uint_as_float(b << 16); }
+  __device__ static __forceinline__ float load(const uint16_t* p) { return widen(*p); }
+  __device__ static __forceinline__ float load_keep(const uint16_t* p, uint64_t pol) {
+    uint16_t v;
+    asm volatile("ld.global.cg.L2::cache_hint.u16 %0, [%1], %2;" : "=h"(v) : "l"(p), "l"(pol));
+    return widen(v);
+  }
+  __device__ static __forceinline__ void groups(const uint4& u, float4* g) {
+    g[0] = make_float4(widen(u.x & 0xFFFFu), widen(u.x >> 16), widen(u.y & 0xFFFFu),
+                       widen(u.y >> 16));
+    g[1] = make_float4(widen(u.z & 0xFFFFu), widen(u.z >> 16), widen(u.w & 0xFFFFu),
+                       widen(u.w >> 16));
+  }
+};
+
 // ------------------------------------------------------------ warp / block
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 
@@ -426,59 +463,98 @@ __device__ __forceinline__ void ring_init(Ring& R, Shared& S, float* buf) {
   __syncthreads();
 }
 
+// Producer side of one chunk: wait for stage q % STAGES to be free, then
+// start the bulk copy of chunk c of the 16-byte aligned body [a0, a1).
+template <class E>
+__device__ __forceinline__ void ring_issue(Ring& R, const E* __restrict__ row, int64_t a0,
+                                           int64_t a1, uint32_t c, uint32_t& lflags) {
+  constexpr int64_t CE = CHUNK_BYTES / Elem<E>::kSize;
+  const uint32_t q = R.seq + c, s = q % STAGES, use = q / STAGES;
+  if (!mbar_wait(&R.empty[s], (use & 1u) ^ 1u)) lflags |= F_TIMEOUT;
+  const int64_t off = a0 + (int64_t)c * CE;
+  const int64_t n = (a1 - off) < CE ? (a1 - off) : CE;
+  const uint32_t bytes = (uint32_t)(n * Elem<E>::kSize);
+  fence_proxy_async();
+  mbar_arrive_expect_tx(&R.full[s], bytes);
+  bulk_load(R.buf + (size_t)s * CHUNK_FLOATS, row + off, bytes, &R.full[s], R.policy);
+}
+
+// The 16-byte aligned body [a0, a1) of [start, end) and its chunk count.
+template <class E>
+__device__ __forceinline__ uint32_t ring_span(const E* row, int64_t start, int64_t end,
+                                              int64_t* a0, int64_t* a1) {
+  constexpr int P16 = Elem<E>::kPer16;
+  constexpr int64_t CE = CHUNK_BYTES / Elem<E>::kSize;
+  const uintptr_t addr = reinterpret_cast<uintptr_t>(row + start);
+  int64_t b0 = start + (int64_t)(((16u - (uint32_t)(addr & 15u)) & 15u) / Elem<E>::kSize);
+  if (b0 > end) b0 = end;
+  *a0 = b0;
+  *a1 = b0 + ((end - b0) & ~(int64_t)(P16 - 1));
+  return (uint32_t)((*a1 - b0 + CE - 1) / CE);
+}
+
+// Starts the first chunks (up to STAGES) of a later scan_pass over
+// [start, end) while the ring is idle, so that they load during the row's
+// sampling.  Every thread calls; returns the number started, which that
+// scan_pass must be given.
+template <class E>
+__device__ __forceinline__ uint32_t ring_prime(Ring& R, const E* __restrict__ row,
+                                               int64_t start, int64_t end, uint32_t& lflags) {
+  if (end <= start) return 0;
+  int64_t a0, a1;
+  const uint32_t nchunks = ring_span(row, start, end, &a0, &a1);
+  const uint32_t n = nchunks < (uint32_t)STAGES ? nchunks : (uint32_t)STAGES;
+  if (threadIdx.x == 0)
+    for (uint32_t c = 0; c < n; ++c) ring_issue(R, row, a0, a1, c, lflags);
+  return n;
+}
+
 // Streams elements [start, end) of `row` through the ring and calls
 // f.quad(i0, float4, valid_mask) on the consumer warps, warp-uniformly, for
-// every group of up to four consecutive elements (element i0 + e is lane e of
-// the float4, valid when bit e of the mask is set).  The 16-byte aligned body
-// goes through bulk copies; the unaligned head and tail (< 4 elements each)
-// are read directly.  The caller synchronises the block afterwards.
-template <class F>
-__device__ __forceinline__ void ring_pass(Ring& R, const float* __restrict__ row, int64_t start,
+// every group of up to four consecutive elements, widened to FP32 (element
+// i0 + e is lane e of the float4, valid when bit e of the mask is set).  The
+// 16-byte aligned body goes through bulk copies; the unaligned head and tail
+// (fewer than 16 bytes each) are read directly.  The caller synchronises the
+// block afterwards.
+template <class E, class F>
+__device__ __forceinline__ void ring_pass(Ring& R, const E* __restrict__ row, int64_t start,
                                           int64_t end, F& f, uint32_t& lflags) {
+  constexpr int P16 = Elem<E>::kPer16, NG = P16 / 4;
   const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31u;
   if (end <= start) return;
-  const uintptr_t addr = reinterpret_cast<uintptr_t>(row + start);
-  int64_t a0 = start + (int64_t)(((16u - (uint32_t)(addr & 15u)) & 15u) >> 2);
-  if (a0 > end) a0 = end;
-  const int64_t a1 = a0 + ((end - a0) & ~(int64_t)3);
-  const uint32_t nchunks = (uint32_t)((a1 - a0 + CHUNK_FLOATS - 1) / CHUNK_FLOATS);
+  int64_t a0, a1;
+  const uint32_t nchunks = ring_span(row, start, end, &a0, &a1);
   if (warp == 0) {
-    if (lane == 0) {
-      for (uint32_t c = 0; c < nchunks; ++c) {
-        const uint32_t q = R.seq + c, s = q % STAGES, use = q / STAGES;
-        if (!mbar_wait(&R.empty[s], (use & 1u) ^ 1u)) lflags |= F_TIMEOUT;
-        const int64_t off = a0 + (int64_t)c * CHUNK_FLOATS;
-        const int64_t n = (a1 - off) < CHUNK_FLOATS ? (a1 - off) : CHUNK_FLOATS;
-        const uint32_t bytes = (uint32_t)(n * 4);
-        fence_proxy_async();
-        mbar_arrive_expect_tx(&R.full[s], bytes);
-        bulk_load(R.buf + (size_t)s * CHUNK_FLOATS, row + off, bytes, &R.full[s], R.policy);
-      }
-    }
+    if (lane == 0)
+      for (uint32_t c = 0; c < nchunks; ++c) ring_issue(R, row, a0, a1, c, lflags);
   } else {
     if (warp == 1) {
-      // head [start, a0) on lanes 0..2, tail [a1, end) on lanes 4..6
+      // head [start, a0) on lanes 0.., tail [a1, end) on lanes 16..
       const int64_t nh = a0 - start, nt = end - a1;
       int64_t i = -1;
       if ((int64_t)lane < nh) i = start + lane;
-      else if (lane >= 4 && (int64_t)lane - 4 < nt) i = a1 + (lane - 4);
-      const float v = (i >= 0) ? row[i] : 0.0f;
+      else if (lane >= 16 && (int64_t)lane - 16 < nt) i = a1 + (lane - 16);
+      const float v = (i >= 0) ? Elem<E>::load(row + i) : 0.0f;
       f.quad(i >= 0 ? i : 0, make_float4(v, 0.f, 0.f, 0.f), i >= 0 ? 1u : 0u);
     }
     const uint32_t ct = tid - 32;
+    constexpr int64_t CE = CHUNK_BYTES / Elem<E>::kSize;
     for (uint32_t c = 0; c < nchunks; ++c) {
       const uint32_t q = R.seq + c, s = q % STAGES, use = q / STAGES;
       if (!mbar_wait(&R.full[s], use & 1u)) lflags |= F_TIMEOUT;
-      const int64_t off = a0 + (int64_t)c * CHUNK_FLOATS;
-      const int64_t n = (a1 - off) < CHUNK_FLOATS ? (a1 - off) : CHUNK_FLOATS;
-      const int nf4 = (int)(n >> 2);
-      const float4* sm4 = reinterpret_cast<const float4*>(R.buf + (size_t)s * CHUNK_FLOATS);
-      const int iters = (nf4 + CONSUMERS - 1) / CONSUMERS;
+      const int64_t off = a0 + (int64_t)c * CE;
+      const int64_t n = (a1 - off) < CE ? (a1 - off) : CE;
+      const int nu = (int)(n / P16);
+      const uint4* sm = reinterpret_cast<const uint4*>(R.buf + (size_t)s * CHUNK_FLOATS);
+      const int iters = (nu + CONSUMERS - 1) / CONSUMERS;
       for (int it = 0; it < iters; ++it) {
         const int j = (int)ct + it * CONSUMERS;
-        const bool ok = j < nf4;
-        const float4 v = ok ? sm4[j] : make_float4(0.f, 0.f, 0.f, 0.f);
-        f.quad(off + 4 * (int64_t)j, v, ok ? 0xfu : 0u);
+        const bool ok = j < nu;
+        const uint4 u = ok ? sm[j] : make_uint4(0u, 0u, 0u, 0u);
+        float4 g[NG];
+        Elem<E>::groups(u, g);
+#pragma unroll
+        for (int k = 0; k < NG; ++k) f.quad(off + (int64_t)P16 * j + 4 * k, g[k], ok ? 0xfu : 0u);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&R.empty[s]);
@@ -577,46 +653,6 @@ __device__ __forceinline__ uint32_t tally_candidates(const uint2* cand, const ui
   return c0;
 }
 
-// Producer side of one chunk: wait for stage q % STAGES to be free, then
-// start the bulk copy of chunk c of the 16-byte aligned body [a0, a1).
-__device__ __forceinline__ void ring_issue(Ring& R, const float* __restrict__ row, int64_t a0,
-                                           int64_t a1, uint32_t c, uint32_t& lflags) {
-  const uint32_t q = R.seq + c, s = q % STAGES, use = q / STAGES;
-  if (!mbar_wait(&R.empty[s], (use & 1u) ^ 1u)) lflags |= F_TIMEOUT;
-  const int64_t off = a0 + (int64_t)c * CHUNK_FLOATS;
-  const int64_t n = (a1 - off) < CHUNK_FLOATS ? (a1 - off) : CHUNK_FLOATS;
-  const uint32_t bytes = (uint32_t)(n * 4);
-  fence_proxy_async();
-  mbar_arrive_expect_tx(&R.full[s], bytes);
-  bulk_load(R.buf + (size_t)s * CHUNK_FLOATS, row + off, bytes, &R.full[s], R.policy);
-}
-
-// The 16-byte aligned body [a0, a1) of [start, end) and its chunk count.
-__device__ __forceinline__ uint32_t ring_span(const float* row, int64_t start, int64_t end,
-                                              int64_t* a0, int64_t* a1) {
-  const uintptr_t addr = reinterpret_cast<uintptr_t>(row + start);
-  int64_t b0 = start + (int64_t)(((16u - (uint32_t)(addr & 15u)) & 15u) >> 2);
-  if (b0 > end) b0 = end;
-  *a0 = b0;
-  *a1 = b0 + ((end - b0) & ~(int64_t)3);
-  return (uint32_t)((*a1 - b0 + CHUNK_FLOATS - 1) / CHUNK_FLOATS);
-}
-
-// Starts the first chunks (up to STAGES) of a later scan_pass over
-// [start, end) while the ring is idle, so that they load during the row's
-// sampling.  Every thread calls; returns the number started, which that
-// scan_pass must be given.
-__device__ __forceinline__ uint32_t ring_prime(Ring& R, const float* __restrict__ row,
-                                               int64_t start, int64_t end, uint32_t& lflags) {
-  if (end <= start) return 0;
-  int64_t a0, a1;
-  const uint32_t nchunks = ring_span(row, start, end, &a0, &a1);
-  const uint32_t n = nchunks < (uint32_t)STAGES ? nchunks : (uint32_t)STAGES;
-  if (threadIdx.x == 0)
-    for (uint32_t c = 0; c < n; ++c) ring_issue(R, row, a0, a1, c, lflags);
-  return n;
-}
-
 // The largest admission operand of four scores (raw bits as signed integers
 // when tau1 > +0; keys mapped to signed order otherwise).
 template <bool POS>
@@ -629,17 +665,27 @@ __device__ __forceinline__ int32_t max_operand(const float4& v) {
   return (int32_t)(max(max(fkey(v.x), fkey(v.y)), max(fkey(v.z), fkey(v.w))) ^ 0x80000000u);
 }
 
+// The largest of the eight bfloat16 patterns of a 16-byte unit, each read as
+// a signed 16-bit integer (for values above +0 this is their order).
+__device__ __forceinline__ int32_t max_bf16_pattern(const uint4& u) {
+  const uint32_t c = __vmaxs2(__vmaxs2(u.x, u.y), __vmaxs2(u.z, u.w));
+  return max((int32_t)(int16_t)(c & 0xFFFFu), (int32_t)(int16_t)(c >> 16));
+}
+
 // The certify+collect pass over [start, end) of `row`, whose first `primed`
-// chunks ring_prime already started.  Same ring protocol as
-// ring_pass, with the consumer side shaped for the common case: a full chunk
-// is exactly two float4 per consumer thread, all eight scores are tested with
-// one integer max, the stage is handed back as soon as the loads have fed
-// that test, and only lanes holding an admitted score (rare) append.
-template <bool POS>
-__device__ __forceinline__ void scan_pass(Ring& R, const float* __restrict__ row, int64_t start,
+// chunks ring_prime already started.  Same ring protocol as ring_pass, with
+// the consumer side shaped for the common case: a full chunk is exactly two
+// 16-byte units per consumer thread, all of their scores (8 FP32 or 16
+// bfloat16) are tested with one integer max, the stage is handed back as
+// soon as the loads have fed that test, and only lanes holding an admitted
+// score (rare) append.
+template <class E, bool POS>
+__device__ __forceinline__ void scan_pass(Ring& R, const E* __restrict__ row, int64_t start,
                                           int64_t end, ScanCollect<POS>& f, uint32_t& lflags,
                                           uint32_t primed) {
-  static_assert(CHUNK_FLOATS == 8 * CONSUMERS, "a full chunk is two float4 per consumer");
+  static_assert(CHUNK_BYTES == 32 * CONSUMERS, "a full chunk is two 16-byte units per consumer");
+  constexpr int P16 = Elem<E>::kPer16, NG = P16 / 4;
+  constexpr int64_t CE = CHUNK_BYTES / Elem<E>::kSize;
   const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31u;
   if (end <= start) return;
   int64_t a0, a1;
@@ -649,34 +695,68 @@ __device__ __forceinline__ void scan_pass(Ring& R, const float* __restrict__ row
       for (uint32_t c = primed; c < nchunks; ++c) ring_issue(R, row, a0, a1, c, lflags);
   } else {
     if (warp == 1) {
-      // head [start, a0) on lanes 0..2, tail [a1, end) on lanes 4..6
+      // head [start, a0) on lanes 0.., tail [a1, end) on lanes 16..
       const int64_t nh = a0 - start, nt = end - a1;
       int64_t i = -1;
       if ((int64_t)lane < nh) i = start + lane;
-      else if (lane >= 4 && (int64_t)lane - 4 < nt) i = a1 + (lane - 4);
-      const float v = (i >= 0) ? row[i] : 0.0f;
+      else if (lane >= 16 && (int64_t)lane - 16 < nt) i = a1 + (lane - 16);
+      const float v = (i >= 0) ? Elem<E>::load(row + i) : 0.0f;
       if (i >= 0) f.lane_put(i, make_float4(v, 0.f, 0.f, 0.f), 1u);
     }
     const uint32_t ct = tid - 32;
-    const int32_t thr = POS ? (int32_t)f.t1 : (int32_t)(f.t1 ^ 0x80000000u);
+    // the admission operand's threshold (for bfloat16 with tau1 > +0: the
+    // upper half of tau1's FP32 bits, as a signed 16-bit value)
+    const int32_t thr = (NG == 2 && POS) ? (int32_t)(int16_t)(f.t1 >> 16)
+                        : POS          ? (int32_t)f.t1
+                                       : (int32_t)(f.t1 ^ 0x80000000u);
     for (uint32_t c = 0; c < nchunks; ++c) {
       const uint32_t q = R.seq + c, s = q % STAGES, use = q / STAGES;
       if (!mbar_wait(&R.full[s], use & 1u)) lflags |= F_TIMEOUT;
-      const int64_t off = a0 + (int64_t)c * CHUNK_FLOATS;
-      const int64_t n = (a1 - off) < CHUNK_FLOATS ? (a1 - off) : CHUNK_FLOATS;
-      const int nf4 = (int)(n >> 2);
-      const float4* sm4 = reinterpret_cast<const float4*>(R.buf + (size_t)s * CHUNK_FLOATS);
+      const int64_t off = a0 + (int64_t)c * CE;
+      const int64_t n = (a1 - off) < CE ? (a1 - off) : CE;
+      const int nu = (int)(n / P16);
+      const uint4* sm = reinterpret_cast<const uint4*>(R.buf + (size_t)s * CHUNK_FLOATS);
       const int j0 = (int)ct, j1 = (int)ct + CONSUMERS;
-      const bool ok0 = j0 < nf4, ok1 = j1 < nf4;
-      const float4 v0 = ok0 ? sm4[j0] : make_float4(0.f, 0.f, 0.f, 0.f);
-      const float4 v1 = ok1 ? sm4[j1] : make_float4(0.f, 0.f, 0.f, 0.f);
-      const int32_t m0 = ok0 ? max_operand<POS>(v0) : INT32_MIN;
-      const int32_t m1 = ok1 ? max_operand<POS>(v1) : INT32_MIN;
+      const bool ok0 = j0 < nu, ok1 = j1 < nu;
+      const uint4 u0 = ok0 ? sm[j0] : make_uint4(0u, 0u, 0u, 0u);
+      const uint4 u1 = ok1 ? sm[j1] : make_uint4(0u, 0u, 0u, 0u);
+      int32_t m0, m1;
+      if constexpr (NG == 2 && POS) {
+        // bfloat16 with tau1 > +0: the raw 16-bit patterns compare as signed
+        // integers in the order of the values; two per instruction
+        m0 = max_bf16_pattern(u0);
+        m1 = max_bf16_pattern(u1);
+      } else {
+        float4 g0[NG], g1[NG];
+        Elem<E>::groups(u0, g0);
+        Elem<E>::groups(u1, g1);
+        m0 = max_operand<POS>(g0[0]);
+        m1 = max_operand<POS>(g1[0]);
+#pragma unroll
+        for (int k = 1; k < NG; ++k) {
+          m0 = max(m0, max_operand<POS>(g0[k]));
+          m1 = max(m1, max_operand<POS>(g1[k]));
+        }
+      }
+      if (!ok0) m0 = INT32_MIN;
+      if (!ok1) m1 = INT32_MIN;
       // both loads have fed m0/m1: hand the stage back before any appends
       __syncwarp();
       if (lane == 0) mbar_arrive(&R.empty[s]);
       const bool h0 = ok0 && m0 >= thr, h1 = ok1 && m1 >= thr;
-      if (h0 || h1) f.lane_put2(off + 4 * (int64_t)j0, v0, h0, off + 4 * (int64_t)j1, v1, h1);
+      if (h0 || h1) {
+        float4 g0[NG], g1[NG];
+        Elem<E>::groups(u0, g0);
+        Elem<E>::groups(u1, g1);
+        if (NG == 1) {
+          f.lane_put2(off + (int64_t)P16 * j0, g0[0], h0, off + (int64_t)P16 * j1, g1[0], h1);
+        } else {
+          if (h0) f.lane_put2(off + (int64_t)P16 * j0, g0[0], true, off + (int64_t)P16 * j0 + 4,
+                              g0[NG - 1], true);
+          if (h1) f.lane_put2(off + (int64_t)P16 * j1, g1[0], true, off + (int64_t)P16 * j1 + 4,
+                              g1[NG - 1], true);
+        }
+      }
     }
   }
   R.seq += nchunks;
@@ -824,9 +904,10 @@ struct CandSrc {  // (idx, key) entries: shared memory, then the spill area
   }
 };
 
+template <class E>
 struct StagedSrc {  // a whole row staged in shared memory; element i at buf[i]
   static constexpr bool kRow = false;
-  const float* buf;
+  const E* buf;
   uint32_t n;
   template <class F>
   __device__ __forceinline__ void for_each(F& f, uint32_t&) const {
@@ -834,16 +915,17 @@ struct StagedSrc {  // a whole row staged in shared memory; element i at buf[i]
     for (uint32_t it = 0; it < iters; ++it) {
       const uint32_t j = threadIdx.x + it * THREADS;
       const bool ok = j < n;
-      const uint32_t k = ok ? fkey(buf[j]) : 0u;
+      const uint32_t k = ok ? fkey(Elem<E>::load(buf + j)) : 0u;
       f.elem(j, k, ok);
     }
   }
 };
 
+template <class E>
 struct RowSrc {  // a row in global memory, streamed through the ring
   static constexpr bool kRow = true;
   Ring* R;
-  const float* row;
+  const E* row;
   int64_t len;
   template <class F>
   __device__ __forceinline__ void for_each(F& f, uint32_t& lflags) const {
@@ -921,12 +1003,13 @@ struct SampleSmem {
   const uint32_t* keys;
   __device__ __forceinline__ uint32_t operator()(int64_t i) const { return keys[i]; }
 };
+template <class E>
 struct SampleGlobal {
-  const float* row;
+  const E* row;
   int64_t stride;
   uint64_t policy;
   __device__ __forceinline__ uint32_t operator()(int64_t i) const {
-    return fkey(ld_keep(row + i * stride, policy));
+    return fkey(Elem<E>::load_keep(row + i * stride, policy));
   }
 };
 
@@ -1037,7 +1120,8 @@ __device__ void select_two_ranks(const uint32_t* keys, uint32_t n, uint32_t r0, 
 // Stage 1.  Samples at 0, s, 2s, ... < len; tau_j = r_j-th largest sample
 // with r_j = clamp(ceil(T_j * n_s / len), 1, n_s).  Leaves key0/key1 and the
 // sample key range in S.  Every thread must call.
-__device__ void sample_thresholds(const float* __restrict__ row, int64_t len, int32_t stride,
+template <class E>
+__device__ void sample_thresholds(const E* __restrict__ row, int64_t len, int32_t stride,
                                   uint32_t T0, uint32_t T1, uint32_t* skeys, uint32_t* hist,
                                   uint32_t* list, Shared& S) {
   const int64_t ns = (len + stride - 1) / stride;
@@ -1054,7 +1138,7 @@ __device__ void sample_thresholds(const float* __restrict__ row, int64_t len, in
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t i = i0 + (int64_t)u * THREADS;
-      v[u] = (i < ns) ? ld_keep(row + i * stride, pol) : 0.0f;
+      v[u] = (i < ns) ? Elem<E>::load_keep(row + i * stride, pol) : 0.0f;
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -1074,7 +1158,7 @@ __device__ void sample_thresholds(const float* __restrict__ row, int64_t len, in
     select_two_ranks(skeys, (uint32_t)ns, (uint32_t)r0, (uint32_t)r1, kmin, kmax, hist, list, S,
                      &key0, &key1);
   } else {
-    const SampleGlobal g{row, stride, pol};
+    const SampleGlobal<E> g{row, stride, pol};
     key1 = select_rank(g, ns, (uint32_t)r1, kmin, kmax, hist, S);
     key0 = select_rank(g, ns, (uint32_t)r0, key1, kmax, hist, S);
   }

@@ -124,7 +124,8 @@ __device__ void finish_row(Shared& S, int32_t* out, int32_t K, uint32_t lflags, 
 
 // Exact selection without sampling, streaming the row from global memory:
 // one histogram pass over the whole key range, then refinement passes.
-__device__ void exact_row_stream(const float* row, int64_t len, int32_t* out, int32_t K, Ring& R,
+template <class E>
+__device__ void exact_row_stream(const E* row, int64_t len, int32_t* out, int32_t K, Ring& R,
                                  const RowCarve& c, uint32_t& lflags) {
   Shared& S = *c.S;
   const Bins bins = make_bins(0u, 0xffffffffu);
@@ -134,7 +135,7 @@ __device__ void exact_row_stream(const float* row, int64_t len, int32_t* out, in
   HistF hf{bins, c.hist};
   ring_pass(R, row, 0, len, hf, lflags);
   __syncthreads();
-  refine(RowSrc{&R, row, len}, bins, (uint32_t)K, c.hist, c.cand, out, K, S, lflags);
+  refine(RowSrc<E>{&R, row, len}, bins, (uint32_t)K, c.hist, c.cand, out, K, S, lflags);
 }
 
 // The full-row certify+collect pass over [s0, s1): candidates in c.cand and
@@ -142,7 +143,8 @@ __device__ void exact_row_stream(const float* row, int64_t len, int32_t* out, in
 // capacity when they did not fit), the seeded histogram of the kept ones in
 // c.hist.  Returns C(tau0) over the kept candidates, which is the exact
 // count unless they overflowed.
-__device__ uint32_t scan_collect(const float* row, int64_t s0, int64_t s1, Ring& R,
+template <class E>
+__device__ uint32_t scan_collect(const E* row, int64_t s0, int64_t s1, Ring& R,
                                  const RowCarve& c, uint2* spill, uint32_t key0, uint32_t key1,
                                  const Bins& sb, uint32_t& lflags, uint32_t primed) {
   Shared& S = *c.S;
@@ -163,7 +165,8 @@ __device__ uint32_t scan_collect(const float* row, int64_t s0, int64_t s1, Ring&
 // Everything after the full-row pass of a sampled row whose candidates
 // (c.cand, then `spill`), histogram and counts are ready: refine, or re-read
 // on overflow, or recover.  Returns the row path.
-__device__ int32_t select_after_scan(const float* row, int64_t len, int32_t* out, int32_t K,
+template <class E>
+__device__ int32_t select_after_scan(const E* row, int64_t len, int32_t* out, int32_t K,
                                      Ring& R, const RowCarve& c, uint2* spill, const SampleSpec& sp,
                                      uint32_t& C0, uint32_t C1, bool overflow, uint32_t key0,
                                      uint32_t key1, uint32_t kmin, const Bins& sb,
@@ -186,7 +189,7 @@ __device__ int32_t select_after_scan(const float* row, int64_t len, int32_t* out
     __syncthreads();
     C0 = block_sum(sf.c0, S);
     path = (C0 >= (uint32_t)K) ? PATH_TAU0 : PATH_TAU1;
-    refine(RowSrc{&R, row, len}, sb, (uint32_t)K, c.hist, c.cand, out, K, S, lflags);
+    refine(RowSrc<E>{&R, row, len}, sb, (uint32_t)K, c.hist, c.cand, out, K, S, lflags);
   } else {
     // C(tau1) < K: every admitted score belongs to the answer; the remaining
     // K - C(tau1) come from the scores below tau1, selected exactly from the
@@ -235,14 +238,15 @@ __device__ int32_t select_after_scan(const float* row, int64_t len, int32_t* out
     HistF hf{rb, c.hist};
     ring_pass(R, row, 0, len, hf, lflags);
     __syncthreads();
-    refine(RowSrc{&R, row, len}, rb, (uint32_t)K - C1, c.hist, c.cand, out, K, S, lflags);
+    refine(RowSrc<E>{&R, row, len}, rb, (uint32_t)K - C1, c.hist, c.cand, out, K, S, lflags);
   }
   return path;
 }
 
 // ------------------------------------------------------------ persistent path
+template <class E>
 __global__ void __launch_bounds__(THREADS, 2)
-    k_persistent(const float* __restrict__ scores, const int32_t* __restrict__ row_lens,
+    k_persistent(const E* __restrict__ scores, const int32_t* __restrict__ row_lens,
                  int32_t* __restrict__ out_idx, RowDiag* __restrict__ diag, uint32_t* hdr,
                  uint2* __restrict__ spill_all, Params P) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -261,7 +265,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     if (r >= P.M) break;
     uint32_t lflags = 0;
     const int64_t len = clamp_len(row_lens[r], P.N_alloc, lflags);
-    const float* row = scores + r * P.N_alloc;
+    const E* row = scores + r * P.N_alloc;
     int32_t* out = out_idx + r * (int64_t)K;
     if (threadIdx.x == 0) S.nout = 0;
     __syncthreads();
@@ -309,18 +313,19 @@ __global__ void __launch_bounds__(THREADS, 2)
 }
 
 // ---------------------------------------------------------------- direct path
+template <class E>
 __global__ void __launch_bounds__(THREADS, 1)
-    k_direct(const float* __restrict__ scores, const int32_t* __restrict__ row_lens,
+    k_direct(const E* __restrict__ scores, const int32_t* __restrict__ row_lens,
              int32_t* __restrict__ out_idx, RowDiag* __restrict__ diag, Params P) {
   extern __shared__ __align__(128) uint8_t smem[];
   Shared& S = *reinterpret_cast<Shared*>(smem);
   uint32_t* hist = reinterpret_cast<uint32_t*>(smem + SH_HDR);
-  float* stage = reinterpret_cast<float*>(smem + SH_HDR + (size_t)NB * sizeof(uint32_t));
+  E* stage = reinterpret_cast<E*>(smem + SH_HDR + (size_t)NB * sizeof(uint32_t));
   const int64_t r = blockIdx.x;
   const int32_t K = P.K;
   uint32_t lflags = 0;
   const int64_t len = clamp_len(row_lens[r], P.N_alloc, lflags);
-  const float* row = scores + r * P.N_alloc;
+  const E* row = scores + r * P.N_alloc;
   int32_t* out = out_idx + r * (int64_t)K;
   const float qnan = __int_as_float(0x7fc00000);
   if (threadIdx.x == 0) {
@@ -337,12 +342,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   // Stage the row: the 16-byte aligned body by bulk copies, head and tail
   // singly.  Element i lives at buf[i] with buf = stage + sh, where sh makes
   // the body's first element land on a 16-byte boundary.
+  constexpr int P16 = Elem<E>::kPer16;
   const uintptr_t addr = reinterpret_cast<uintptr_t>(row);
-  int64_t a0 = (int64_t)(((16u - (uint32_t)(addr & 15u)) & 15u) >> 2);
+  int64_t a0 = (int64_t)(((16u - (uint32_t)(addr & 15u)) & 15u) / Elem<E>::kSize);
   if (a0 > len) a0 = len;
-  const int64_t a1 = a0 + ((len - a0) & ~(int64_t)3);
-  const int64_t sh = (4 - (a0 & 3)) & 3;
-  float* buf = stage + sh;
+  const int64_t a1 = a0 + ((len - a0) & ~(int64_t)(P16 - 1));
+  const int64_t sh = (P16 - (a0 % P16)) % P16;
+  E* buf = stage + sh;
   if (threadIdx.x == 0) {
     mbar_init(&S.full[0], 1);
     fence_mbar_init();
@@ -350,7 +356,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   if (threadIdx.x == 0) {
     const uint64_t pol = l2_policy_evict_first();
-    const uint32_t bytes = (uint32_t)((a1 - a0) * 4);
+    const uint32_t bytes = (uint32_t)((a1 - a0) * Elem<E>::kSize);
     mbar_arrive_expect_tx(&S.full[0], bytes);
     constexpr uint32_t PIECE = 32768;
     for (uint32_t o = 0; o < bytes; o += PIECE) {
@@ -366,7 +372,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   // Exact boundary over the staged keys: data-relative bins over [min, max].
   uint32_t mn = 0xffffffffu, mx = 0u;
   for (int64_t i = threadIdx.x; i < len; i += THREADS) {
-    const uint32_t k = fkey(buf[i]);
+    const uint32_t k = fkey(Elem<E>::load(buf + i));
     mn = min(mn, k);
     mx = max(mx, k);
   }
@@ -375,7 +381,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const Bins bins = make_bins(kmin, kmax);
   clear_hist(hist);
   __syncthreads();
-  const StagedSrc src{buf, (uint32_t)len};
+  const StagedSrc<E> src{buf, (uint32_t)len};
   HistF hf{bins, hist};
   src.for_each(hf, lflags);
   __syncthreads();
@@ -389,8 +395,9 @@ __device__ __forceinline__ KvHdr* kv_hdr(uint8_t* ws_rows, int64_t r) {
 }
 
 // One CTA per row: lengths, thresholds, and a fresh merge state.
+template <class E>
 __global__ void __launch_bounds__(THREADS, 1)
-    k_kv_prepare(const float* __restrict__ scores, const int32_t* __restrict__ row_lens,
+    k_kv_prepare(const E* __restrict__ scores, const int32_t* __restrict__ row_lens,
                  uint8_t* __restrict__ ws_rows, Params P) {
   extern __shared__ __align__(128) uint8_t smem[];
   Shared& S = *reinterpret_cast<Shared*>(smem);
@@ -400,7 +407,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int64_t r = blockIdx.x;
   uint32_t lflags = 0;
   const int64_t len = clamp_len(row_lens[r], P.N_alloc, lflags);
-  const float* row = scores + r * P.N_alloc;
+  const E* row = scores + r * P.N_alloc;
   uint8_t* base = ws_rows + (size_t)r * KV_ROW_BYTES;
   KvHdr* h = reinterpret_cast<KvHdr*>(base);
   uint32_t* ghist = reinterpret_cast<uint32_t*>(base + KV_HIST_OFF);
@@ -434,8 +441,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+template <class E>
 __global__ void __launch_bounds__(THREADS, 2)
-    k_kv_segment(const float* __restrict__ scores, int32_t* __restrict__ out_idx,
+    k_kv_segment(const E* __restrict__ scores, int32_t* __restrict__ out_idx,
                  RowDiag* __restrict__ diag, uint8_t* __restrict__ ws_rows, Params P) {
   extern __shared__ __align__(128) uint8_t smem[];
   const RowCarve c = carve(smem);
@@ -450,7 +458,7 @@ __global__ void __launch_bounds__(THREADS, 2)
   const uint32_t mode = h->mode;
   const int64_t len = h->len;
   const uint32_t key0 = h->key0, key1 = h->key1, kmin = h->kmin, kmax = h->kmax;
-  const float* row = scores + r * P.N_alloc;
+  const E* row = scores + r * P.N_alloc;
   const int32_t K = P.K;
   if (threadIdx.x == 0) {
     S.flags = 0;
@@ -529,8 +537,10 @@ size_t kv_segment_smem_bytes() { return SH_ROW_TOTAL; }
 size_t kv_prepare_smem_bytes() {
   return SH_HDR + (size_t)(NB + THREADS + SAMPLE_SMEM) * sizeof(uint32_t);
 }
-size_t direct_smem_bytes(int64_t n_alloc) {
-  return SH_HDR + (size_t)NB * sizeof(uint32_t) + align_up((size_t)(n_alloc + 4) * 4, 16);
+size_t direct_smem_bytes(int64_t n_alloc, int elem_bytes) {
+  // the row plus up to one 16-byte unit of alignment shift
+  return SH_HDR + (size_t)NB * sizeof(uint32_t) +
+         align_up((size_t)n_alloc * elem_bytes + 16, 16);
 }
 size_t kv_row_bytes() { return KV_ROW_BYTES; }
 size_t persistent_spill_bytes() { return (size_t)SPILL * sizeof(uint2); }
@@ -541,47 +551,82 @@ static cudaError_t set_smem(const void* fn, size_t bytes) {
 
 cudaError_t prepare_device() {
   cudaError_t e;
-  if ((e = set_smem((const void*)k_persistent, persistent_smem_bytes())) != cudaSuccess) return e;
-  if ((e = set_smem((const void*)k_kv_segment, kv_segment_smem_bytes())) != cudaSuccess) return e;
-  if ((e = set_smem((const void*)k_kv_prepare, kv_prepare_smem_bytes())) != cudaSuccess) return e;
   int dev = 0, optin = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
       cudaSuccess)
     return e;
-  return set_smem((const void*)k_direct, (size_t)optin);
+  const void* row_kernels[] = {(const void*)k_persistent<float>, (const void*)k_persistent<uint16_t>,
+                               (const void*)k_kv_segment<float>, (const void*)k_kv_segment<uint16_t>};
+  for (const void* fn : row_kernels)
+    if ((e = set_smem(fn, persistent_smem_bytes())) != cudaSuccess) return e;
+  if ((e = set_smem((const void*)k_kv_prepare<float>, kv_prepare_smem_bytes())) != cudaSuccess)
+    return e;
+  if ((e = set_smem((const void*)k_kv_prepare<uint16_t>, kv_prepare_smem_bytes())) != cudaSuccess)
+    return e;
+  if ((e = set_smem((const void*)k_direct<float>, (size_t)optin)) != cudaSuccess) return e;
+  return set_smem((const void*)k_direct<uint16_t>, (size_t)optin);
 }
 
 cudaError_t persistent_occupancy(int* blocks_per_sm) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k_persistent, THREADS,
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k_persistent<float>, THREADS,
                                                        persistent_smem_bytes());
 }
 
-cudaError_t launch_direct(const float* scores, const int32_t* row_lens, int32_t* out,
-                          RowDiag* diag, const Params& P, cudaStream_t st) {
-  k_direct<<<(unsigned)P.M, THREADS, direct_smem_bytes(P.N_alloc), st>>>(scores, row_lens, out,
-                                                                       diag, P);
+template <class E>
+static cudaError_t launch_direct_t(const E* scores, const int32_t* row_lens, int32_t* out,
+                                   RowDiag* diag, const Params& P, cudaStream_t st) {
+  k_direct<E><<<(unsigned)P.M, THREADS, direct_smem_bytes(P.N_alloc, Elem<E>::kSize), st>>>(
+      scores, row_lens, out, diag, P);
   return cudaGetLastError();
 }
 
-cudaError_t launch_persistent(const float* scores, const int32_t* row_lens, int32_t* out,
-                              RowDiag* diag, uint32_t* hdr, void* spill, int grid, const Params& P,
-                              cudaStream_t st) {
-  k_persistent<<<grid, THREADS, persistent_smem_bytes(), st>>>(
+template <class E>
+static cudaError_t launch_persistent_t(const E* scores, const int32_t* row_lens, int32_t* out,
+                                       RowDiag* diag, uint32_t* hdr, void* spill, int grid,
+                                       const Params& P, cudaStream_t st) {
+  k_persistent<E><<<grid, THREADS, persistent_smem_bytes(), st>>>(
       scores, row_lens, out, diag, hdr, static_cast<uint2*>(spill), P);
   return cudaGetLastError();
 }
 
-cudaError_t launch_kvsplit(const float* scores, const int32_t* row_lens, int32_t* out,
-                           RowDiag* diag, uint8_t* ws_rows, const Params& P, cudaStream_t st) {
-  k_kv_prepare<<<(unsigned)P.M, THREADS, kv_prepare_smem_bytes(), st>>>(scores, row_lens,
-                                                                        ws_rows, P);
+template <class E>
+static cudaError_t launch_kvsplit_t(const E* scores, const int32_t* row_lens, int32_t* out,
+                                    RowDiag* diag, uint8_t* ws_rows, const Params& P,
+                                    cudaStream_t st) {
+  k_kv_prepare<E><<<(unsigned)P.M, THREADS, kv_prepare_smem_bytes(), st>>>(scores, row_lens,
+                                                                           ws_rows, P);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t items = P.M * (int64_t)P.segments;
-  k_kv_segment<<<(unsigned)items, THREADS, kv_segment_smem_bytes(), st>>>(scores, out, diag,
-                                                                         ws_rows, P);
+  k_kv_segment<E><<<(unsigned)items, THREADS, kv_segment_smem_bytes(), st>>>(scores, out, diag,
+                                                                            ws_rows, P);
   return cudaGetLastError();
+}
+
+cudaError_t launch_direct(const void* scores, const int32_t* row_lens, int32_t* out,
+                          RowDiag* diag, const Params& P, cudaStream_t st) {
+  if (P.elem_bytes == 2)
+    return launch_direct_t(static_cast<const uint16_t*>(scores), row_lens, out, diag, P, st);
+  return launch_direct_t(static_cast<const float*>(scores), row_lens, out, diag, P, st);
+}
+
+cudaError_t launch_persistent(const void* scores, const int32_t* row_lens, int32_t* out,
+                              RowDiag* diag, uint32_t* hdr, void* spill, int grid, const Params& P,
+                              cudaStream_t st) {
+  if (P.elem_bytes == 2)
+    return launch_persistent_t(static_cast<const uint16_t*>(scores), row_lens, out, diag, hdr,
+                               spill, grid, P, st);
+  return launch_persistent_t(static_cast<const float*>(scores), row_lens, out, diag, hdr, spill,
+                             grid, P, st);
+}
+
+cudaError_t launch_kvsplit(const void* scores, const int32_t* row_lens, int32_t* out,
+                           RowDiag* diag, uint8_t* ws_rows, const Params& P, cudaStream_t st) {
+  if (P.elem_bytes == 2)
+    return launch_kvsplit_t(static_cast<const uint16_t*>(scores), row_lens, out, diag, ws_rows, P,
+                            st);
+  return launch_kvsplit_t(static_cast<const float*>(scores), row_lens, out, diag, ws_rows, P, st);
 }
 
 cudaError_t read_and_clear_status(cudaStream_t st, uint32_t* flags) {

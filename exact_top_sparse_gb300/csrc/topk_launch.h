@@ -18,6 +18,7 @@ struct Params {
   uint32_t target1;  // ceil(rho1 * K)
   int64_t sample_min_len;
   int32_t segments;  // KV-split segments per row
+  int32_t elem_bytes;  // 4: FP32 scores, 2: bfloat16 scores
   int64_t long_len;  // rows this long or longer sample with the long_* values (0: none)
   int32_t long_stride;
   uint32_t long_target0;
@@ -35,7 +36,7 @@ struct RowDiag {
 size_t persistent_smem_bytes();
 size_t kv_segment_smem_bytes();
 size_t kv_prepare_smem_bytes();
-size_t direct_smem_bytes(int64_t n_alloc);
+size_t direct_smem_bytes(int64_t n_alloc, int elem_bytes);
 size_t kv_row_bytes();
 // Bytes of KV-split merge state per row (equals kv_row_bytes()).
 constexpr size_t kKvRowBytes = 139520;
@@ -46,12 +47,12 @@ size_t persistent_spill_bytes();
 cudaError_t prepare_device();
 cudaError_t persistent_occupancy(int* blocks_per_sm);
 
-cudaError_t launch_direct(const float* scores, const int32_t* row_lens, int32_t* out,
+cudaError_t launch_direct(const void* scores, const int32_t* row_lens, int32_t* out,
                           RowDiag* diag, const Params& P, cudaStream_t st);
-cudaError_t launch_persistent(const float* scores, const int32_t* row_lens, int32_t* out,
+cudaError_t launch_persistent(const void* scores, const int32_t* row_lens, int32_t* out,
                               RowDiag* diag, uint32_t* hdr, void* spill, int grid, const Params& P,
                               cudaStream_t st);
-cudaError_t launch_kvsplit(const float* scores, const int32_t* row_lens, int32_t* out,
+cudaError_t launch_kvsplit(const void* scores, const int32_t* row_lens, int32_t* out,
                            RowDiag* diag, uint8_t* ws_rows, const Params& P, cudaStream_t st);
 
 cudaError_t read_and_clear_status(cudaStream_t st, uint32_t* flags);

@@ -150,6 +150,18 @@ int topk_ragged_diag(const float* scores, const int32_t* row_lens, int64_t M, in
                      int32_t K, int32_t* out_idx, topk_row_diag* diag,
                      struct CUstream_st* stream);
 
+/* Same as topk_ragged / topk_ragged_diag for bfloat16 score rows: `scores`
+ * holds raw bfloat16 bit patterns [M][N_alloc] (2-byte aligned).  A bfloat16
+ * widens exactly to FP32, and the selection is the exact Top-K of the
+ * widened values (same contract, same thresholds and paths), reading half the
+ * bytes.  This is an extension beyond the pages, which measure FP32 rows only
+ * (PaperDaily, section 问题四, lists lower-precision scores as untested). */
+int topk_ragged_bf16(const uint16_t* scores, const int32_t* row_lens, int64_t M, int64_t N_alloc,
+                     int32_t K, int32_t* out_idx, struct CUstream_st* stream);
+int topk_ragged_bf16_diag(const uint16_t* scores, const int32_t* row_lens, int64_t M,
+                          int64_t N_alloc, int32_t K, int32_t* out_idx, topk_row_diag* diag,
+                          struct CUstream_st* stream);
+
 /* Device workspace bytes a call with these sizes needs under the current
  * parameters (0 is a valid answer only for M == 0). */
 size_t topk_workspace_bytes(int64_t M, int64_t N_alloc, int32_t K);
