@@ -68,7 +68,7 @@ EXPORTS = ("topk_ragged", "topk_ragged_diag", "topk_ragged_ws", "topk_workspace_
            "topk_default_params", "topk_read_status", "topk_release_workspaces",
            "topk_status_string", "topk_version", "topk_ragged_noalloc",
            "topk_index_scores", "topk_index_topk", "topk_index_read_status",
-           "topk_ragged_bf16", "topk_ragged_bf16_diag")
+           "topk_ragged_bf16", "topk_ragged_bf16_diag", "topk_sort_rows", "topk_sort_rows_bf16")
 NOALLOC_MAX_ROWS = 64
 
 _lib = None
@@ -91,6 +91,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.topk_ragged_ws.argtypes = [vp, vp, i64, i64, i32, vp, vp, sz, vp]
     lib.topk_ragged_noalloc.argtypes = [vp, vp, i64, i64, i32, vp, vp]
     lib.topk_ragged_bf16.argtypes = [vp, vp, i64, i64, i32, vp, vp]
+    lib.topk_sort_rows.argtypes = [vp, i64, i64, i32, vp, vp]
+    lib.topk_sort_rows_bf16.argtypes = [vp, i64, i64, i32, vp, vp]
     lib.topk_ragged_bf16_diag.argtypes = [vp, vp, i64, i64, i32, vp, vp, vp]
     lib.topk_index_scores.argtypes = [vp, vp, vp, i64, i64, i32, i32, vp, vp, i64, vp]
     lib.topk_index_topk.argtypes = [vp, vp, vp, i64, i64, i32, i32, vp, vp, i64, i32, vp, vp]
@@ -111,7 +113,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.topk_version.argtypes = []
     for name in ("topk_ragged", "topk_ragged_diag", "topk_ragged_ws", "topk_ragged_host",
                  "topk_ragged_noalloc", "topk_index_scores", "topk_index_topk",
-                 "topk_ragged_bf16", "topk_ragged_bf16_diag",
+                 "topk_ragged_bf16", "topk_ragged_bf16_diag", "topk_sort_rows",
+                 "topk_sort_rows_bf16",
                  "topk_index_read_status",
                  "topk_plan", "topk_set_params", "topk_get_params", "topk_read_status",
                  "topk_version"):
@@ -163,6 +166,26 @@ def topk_ragged(scores: torch.Tensor, row_lens: torch.Tensor, K: int = 2048,
         rc = fn(scores.data_ptr(), row_lens.data_ptr(), M, N, K, out.data_ptr(),
                 _stream_handle(scores.device, stream))
     _check(rc, "topk_ragged")
+    return out
+
+
+def topk_sort_rows(scores, out, stream=None):
+    """Sort each row of a Top-K result in place: score descending, equal
+    scores by index, -1 sentinels last (the selection itself is unordered)."""
+    lib = load_library()
+    if not (isinstance(scores, torch.Tensor) and scores.is_cuda and scores.dim() == 2
+            and scores.dtype in (torch.float32, torch.bfloat16) and scores.is_contiguous()):
+        raise TypeError("scores must be a contiguous 2-D float32 or bfloat16 CUDA tensor")
+    if not (isinstance(out, torch.Tensor) and out.device == scores.device
+            and out.dtype == torch.int32 and out.dim() == 2 and out.shape[0] == scores.shape[0]
+            and out.is_contiguous()):
+        raise TypeError("out must be a contiguous int32 [M, K] tensor on the scores' device")
+    M, N = scores.shape
+    fn = lib.topk_sort_rows_bf16 if scores.dtype == torch.bfloat16 else lib.topk_sort_rows
+    with torch.cuda.device(scores.device):
+        rc = fn(scores.data_ptr(), M, N, out.shape[1], out.data_ptr(),
+                _stream_handle(scores.device, stream))
+    _check(rc, "topk_sort_rows")
     return out
 
 

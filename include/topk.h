@@ -231,6 +231,17 @@ const char* topk_status_string(int code);
 /* Library version as major * 10000 + minor * 100 + patch. */
 int topk_version(void);
 
+/* Optional order for a Top-K result (the contract leaves it free): sorts each
+ * of the M rows of out_idx [M][K] (device, as written by topk_ragged) in
+ * place by score, largest first, equal scores by index, -1 sentinels last.
+ * `scores` are the rows the indices refer to (device, row stride N_alloc);
+ * topk_sort_rows_bf16 takes bfloat16 patterns.  One launch on `stream`, no
+ * allocation.  Errors as topk_ragged. */
+int topk_sort_rows(const float* scores, int64_t M, int64_t N_alloc, int32_t K, int32_t* out_idx,
+                   struct CUstream_st* stream);
+int topk_sort_rows_bf16(const uint16_t* scores, int64_t M, int64_t N_alloc, int32_t K,
+                        int32_t* out_idx, struct CUstream_st* stream);
+
 /* ---------------------------------------------------------------------------
  * Indexer scores: the stage that produces the selector's rows (eq. (1) of the
  * xllm-io review of LiteTopK, section "核心公式"):
