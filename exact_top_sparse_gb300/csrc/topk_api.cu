@@ -19,7 +19,7 @@
 
 namespace {
 
-constexpr int kVersion = 10000;  // 1.0.0
+constexpr int kVersion = 10100;  // 1.1.0: bfloat16 rows, ordered output, indexer scores
 constexpr size_t kHdrBytes = 256;
 constexpr int64_t kMinSegment = 32768;  // floats per KV-split segment, at least
 // Planner crossovers, measured on GB300 over 128K-1M columns and M = 64-2048:
