@@ -53,7 +53,7 @@ def parse():
                     help="skip the indexer-score + Top-K chain (tensor-core) line")
     ap.add_argument("--chain-T", type=int, default=2048, help="queries of the chain line")
     ap.add_argument("--no-trace", action="store_true",
-                    help="skip the replay of a 430K-token prefill's 71 Top-K calls")
+                    help="skip the replays of 245K- and 430K-token prefills (26 and 71 Top-K calls)")
     ap.add_argument("--chain-S", type=int, default=262144, help="keys of the chain line")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--force-kind", default="auto",
@@ -501,10 +501,11 @@ def run_gb300(args):
         except RuntimeError as e:
             result["chain"] = {"error": str(e)[:200]}
     if not args.no_trace and rank == 0:
-        try:
-            result["trace_430k"] = trace_leg(ets, dev, stream)
-        except RuntimeError as e:
-            result["trace_430k"] = {"error": str(e)[:200]}
+        for name, tokens in (("trace_245k", 245 * 1024), ("trace_430k", 430 * 1024)):
+            try:
+                result[name] = trace_leg(ets, dev, stream, tokens=tokens)
+            except RuntimeError as e:
+                result[name] = {"error": str(e)[:200]}
 
     # end to end through the host-buffer C ABI: pinned host rows in, indices out
     if not args.no_e2e and rank == 0:
