@@ -12,7 +12,8 @@
 //     unresolved boundary bin, resolved high bins are emitted and never
 //     revisited, output order is free.
 //   * codexqa.cn "几何平均快 1.55 倍…腾讯怎么测精确 Top-K", section
-//     "采样不是处处都该开": stride 128, primary target 1.5K, nested 1.75K.
+//     "采样不是处处都该开": stride 128, primary target 1.5K, nested 1.75K on
+//     H20 (the defaults here are wider, see the parameter notes in topk.h).
 //   * arxivdaily abstract: certification and candidate formation are fused in
 //     one pass; persistent, KV-split and direct-exact execution sit behind a
 //     graph-capturable ragged-row dispatch.
@@ -24,9 +25,10 @@
 // This build differs from the pages' H20 design where GB300 pays for it: the
 // full-row pass streams the row through shared memory with 1-D bulk async
 // copies (TMA) into a 3-stage ring driven by mbarriers; candidates of the
-// nested band are collected in the same pass, so the tau1 path needs no
-// re-read; radix rounds use data-relative 11-bit digits so the first
-// histogram is not degenerate on concentrated scores.
+// nested band are collected in the same pass (into shared memory, then a
+// global spill area), so the tau1 path needs no re-read; radix rounds use
+// data-relative 11-bit digits so the first histogram is not degenerate on
+// concentrated scores; rows may be FP32 or bfloat16 (widened exactly).
 #pragma once
 
 #include <cstdint>
@@ -435,7 +437,7 @@ __device__ __forceinline__ void warp_emit(int32_t* out, int32_t K, uint32_t idx,
 }
 
 // ------------------------------------------------------------- the TMA ring
-// A 3-stage ring of 16 KB shared-memory stages filled by 1-D bulk copies.
+// A 3-stage ring of 15 KB shared-memory stages filled by 1-D bulk copies.
 // Warp 0, lane 0 produces; warps 1..15 consume.  Every thread keeps the same
 // chunk sequence number, so passes can follow one another without resetting
 // the barriers.
