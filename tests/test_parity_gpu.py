@@ -151,6 +151,23 @@ def test_long_rows_default_dispatch(ets, N, M):
     del x
 
 
+@pytest.mark.parametrize("kind", ["auto", "persistent", "kvsplit"])
+def test_rows_longer_than_the_matrix(params, kind):
+    """4M-column rows (past the operator matrix): the long sampling tier, the
+    KV-split's many segments, and the sampler's on-chip key buffer."""
+    ets = params
+    N, M = 4 * 1048576, 12
+    if kind != "auto":
+        ets.set_params(force_kind=ets.KIND_PERSISTENT if kind == "persistent" else ets.KIND_KVSPLIT)
+    lens = torch.tensor([N, N - 1, N - 3, 3 * 1048576 + 5, 2 * 1048576 + 1, 1048576, 800000,
+                         N - 12345, 4095, 2049, 1, N], dtype=torch.int32)
+    x = synth.indexer_rows(lens, N, seed=44, device=DEV)
+    got, dg = run(ets, x, lens, diag=True)
+    verify(x, lens, K, got)
+    verify_diag(ets, x, lens, K, dg, sample_min_len=ets.get_params()["sample_min_len"])
+    del x
+
+
 def test_full_size_1m_by_8192_sampled_rows(ets):
     """The benchmark's configuration (1M columns, 8192 causal rows, default
     dispatch); the oracle checks 48 sampled rows one by one."""
