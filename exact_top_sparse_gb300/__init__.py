@@ -68,7 +68,8 @@ EXPORTS = ("topk_ragged", "topk_ragged_diag", "topk_ragged_ws", "topk_workspace_
            "topk_default_params", "topk_read_status", "topk_release_workspaces",
            "topk_status_string", "topk_version", "topk_ragged_noalloc",
            "topk_index_scores", "topk_index_topk", "topk_index_read_status",
-           "topk_ragged_bf16", "topk_ragged_bf16_diag", "topk_sort_rows", "topk_sort_rows_bf16")
+           "topk_ragged_bf16", "topk_ragged_bf16_diag", "topk_sort_rows", "topk_sort_rows_bf16",
+           "topk_check_wait_timeout")
 NOALLOC_MAX_ROWS = 64
 
 _lib = None
@@ -92,6 +93,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.topk_ragged_noalloc.argtypes = [vp, vp, i64, i64, i32, vp, vp]
     lib.topk_ragged_bf16.argtypes = [vp, vp, i64, i64, i32, vp, vp]
     lib.topk_sort_rows.argtypes = [vp, i64, i64, i32, vp, vp]
+    lib.topk_check_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+    lib.topk_check_wait_timeout.restype = ctypes.c_int
     lib.topk_sort_rows_bf16.argtypes = [vp, i64, i64, i32, vp, vp]
     lib.topk_ragged_bf16_diag.argtypes = [vp, vp, i64, i64, i32, vp, vp, vp]
     lib.topk_index_scores.argtypes = [vp, vp, vp, i64, i64, i32, i32, vp, vp, i64, vp]

@@ -505,6 +505,16 @@ int topk_ragged_host(const float* h_scores, const int32_t* h_lens, int64_t M, in
   return TOPK_OK;
 }
 
+int topk_check_wait_timeout(uint64_t limit_ns, struct CUstream_st* stream) {
+  if (limit_ns == 0 || limit_ns > 10000000000ull) return TOPK_ERR_ARG;
+  DevInfo d;
+  int rc = device_info(&d, nullptr);
+  if (rc) return rc;
+  return tk::launch_wait_probe(limit_ns, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? TOPK_OK
+             : TOPK_ERR_CUDA;
+}
+
 void topk_release_workspaces(void) {
   std::lock_guard<std::mutex> lk(g_mu);
   int cur = 0;

@@ -130,14 +130,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 __device__ uint32_t g_abort;
 
 // Slow path of mbar_wait: polls until the phase completes, giving up after
-// WAIT_LIMIT_NS so that no wait can hang the GPU.
-__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity) {
+// limit_ns (WAIT_LIMIT_NS in the kernels) so that no wait can hang the GPU.
+__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity,
+                                            uint64_t limit_ns = WAIT_LIMIT_NS) {
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*reinterpret_cast<volatile uint32_t*>(&g_abort) != 0u) return false;
-      if (globaltimer() - t0 > WAIT_LIMIT_NS) {
+      if (globaltimer() - t0 > limit_ns) {
         atomicExch(&g_abort, 1u);
         return false;
       }

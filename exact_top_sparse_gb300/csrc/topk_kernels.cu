@@ -629,6 +629,24 @@ cudaError_t launch_kvsplit(const void* scores, const int32_t* row_lens, int32_t*
   return launch_kvsplit_t(static_cast<const float*>(scores), row_lens, out, diag, ws_rows, P, st);
 }
 
+// Self-test of the bounded wait: one thread waits on a barrier that nothing
+// completes, with the kernels' own wait routine and a short limit; giving up
+// sets F_TIMEOUT in the status word (and the fail-fast flag, cleared when the
+// status is read).  No copy or other memory operation is pending meanwhile.
+__global__ void k_wait_probe(uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    if (!mbar_wait_slow(&bar, 0u, limit_ns)) atomicOr(&g_status, F_TIMEOUT);
+  }
+}
+
+cudaError_t launch_wait_probe(uint64_t limit_ns, cudaStream_t st) {
+  k_wait_probe<<<1, 32, 0, st>>>(limit_ns);
+  return cudaGetLastError();
+}
+
 cudaError_t read_and_clear_status(cudaStream_t st, uint32_t* flags) {
   uint32_t h = 0, zero = 0;
   cudaError_t e = cudaMemcpyFromSymbolAsync(&h, g_status, sizeof(uint32_t), 0,

@@ -56,5 +56,6 @@ cudaError_t launch_kvsplit(const void* scores, const int32_t* row_lens, int32_t*
                            RowDiag* diag, uint8_t* ws_rows, const Params& P, cudaStream_t st);
 
 cudaError_t read_and_clear_status(cudaStream_t st, uint32_t* flags);
+cudaError_t launch_wait_probe(uint64_t limit_ns, cudaStream_t st);
 
 }  // namespace tk

@@ -228,6 +228,14 @@ void topk_release_workspaces(void);
 /* Human-readable name of a topk_status code (static string). */
 const char* topk_status_string(int code);
 
+/* Self-test of failure detection: one thread on `stream` waits, with the
+ * kernels' own bounded-wait routine, on a barrier that nothing completes;
+ * after limit_ns (1 ns .. 10 s) it gives up and sets TOPK_FLAG_TIMEOUT in the
+ * status word, which topk_read_status() returns (and clears, re-arming the
+ * kernels' fail-fast flag).  No memory operation is pending meanwhile and the
+ * context stays usable.  TOPK_ERR_ARG for a limit outside that range. */
+int topk_check_wait_timeout(uint64_t limit_ns, struct CUstream_st* stream);
+
 /* Library version as major * 10000 + minor * 100 + patch. */
 int topk_version(void);
 
