@@ -57,7 +57,7 @@ constexpr uint32_t OFF_B = 0;
 constexpr uint32_t OFF_A = OFF_B + B_BYTES;
 constexpr uint32_t OFF_W = OFF_A + STAGES * A_BYTES;       // QB * HEADS floats
 constexpr uint32_t OFF_BAR = OFF_W + QB * HEADS * 4;
-constexpr uint32_t NBAR = 2 * STAGES + 2 + 4;
+constexpr uint32_t NBAR = 2 * STAGES + 2 + 4 + 1;
 constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;      // + alignment slack
 
@@ -103,6 +103,22 @@ __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, volatile
     }
   }
 }
+// Bounded wait that ignores the abort flag: lets copies and MMAs already in
+// flight finish before the CTA releases its tensor memory and exits.
+__device__ __forceinline__ void bar_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = gtime();
+  for (;;) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (ok || gtime() - t0 > 100000000ull) return;
+  }
+}
+
 __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
                                        uint32_t bar) {
   asm volatile(
@@ -174,6 +190,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t b_full = bars + 8u * (2 * STAGES), b_empty = bars + 8u * (2 * STAGES + 1);
   auto acc_full = [&](uint32_t b) { return bars + 8u * (2 * STAGES + 2 + b); };
   auto acc_empty = [&](uint32_t b) { return bars + 8u * (2 * STAGES + 4 + b); };
+  const uint32_t drain = bars + 8u * (2 * STAGES + 6);
   uint32_t* misc = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
   volatile uint32_t* abort_flag = misc + 1;
   const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31u;
@@ -189,6 +206,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       bar_init(acc_full(b), 1);
       bar_init(acc_empty(b), 4);  // one arrival per epilogue warp
     }
+    bar_init(drain, 1);
     *abort_flag = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -227,11 +245,18 @@ __global__ void __launch_bounds__(THREADS, 1)
           tma_2d(dst + A_HALF, &map_k, 64, t * KT, a_full(s));
         }
       }
+      // the last copies of each kind have landed before the CTA exits
+      for (uint32_t k = 0; k < aseq && k < (uint32_t)STAGES; ++k) {
+        const uint32_t q = aseq - 1u - k;
+        bar_drain(a_full(q % STAGES), (q / STAGES) & 1u);
+      }
+      if (ui > 0) bar_drain(b_full, (ui - 1u) & 1u);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       uint32_t aseq = 0, accseq = 0, ui = 0;
+      bool issued = false;
       for (int32_t u = blockIdx.x; u < a.n_units && !*abort_flag; u += gridDim.x) {
         int32_t qb, t0, t1;
         unit_coords(a, u, &qb, &t0, &t1);
@@ -248,6 +273,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          issued = true;
           const uint32_t a_base = base + OFF_A + s * A_BYTES, b_base = base + OFF_B;
           const uint32_t d_tmem = tmem + buf * NCOL;
 #pragma unroll
@@ -276,6 +302,15 @@ __global__ void __launch_bounds__(THREADS, 1)
             "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                 b_empty)
             : "memory");
+      }
+      // every MMA this thread issued has completed before tensor memory is
+      // released
+      if (issued) {
+        asm volatile(
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                drain)
+            : "memory");
+        bar_drain(drain, 0u);
       }
     }
   } else {

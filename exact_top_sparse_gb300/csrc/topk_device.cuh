@@ -146,6 +146,15 @@ __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity,
   }
 }
 
+// Polls until the phase completes or limit_ns passes, whatever the fail-fast
+// flag says (used to let copies in flight land before a CTA exits).
+__device__ __noinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer() - t0 > limit_ns) return false;
+  return true;
+}
+
 // Waits for the phase of `bar` with the given parity (false after a timeout).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -510,6 +519,18 @@ __device__ __forceinline__ uint32_t ring_prime(Ring& R, const E* __restrict__ ro
   if (threadIdx.x == 0)
     for (uint32_t c = 0; c < n; ++c) ring_issue(R, row, a0, a1, c, lflags);
   return n;
+}
+
+// Before a CTA exits: waits (bounded, even after an abort) for the copies of
+// the last STAGES chunks, so that no bulk copy is still in flight into this
+// CTA's shared memory.  On the normal path every one of them has long landed.
+__device__ __forceinline__ void ring_drain(Ring& R) {
+  if (threadIdx.x != 0) return;
+  const uint32_t n = R.seq < (uint32_t)STAGES ? R.seq : (uint32_t)STAGES;
+  for (uint32_t k = 0; k < n; ++k) {
+    const uint32_t q = R.seq - 1u - k, s = q % STAGES, use = q / STAGES;
+    mbar_wait_drain(&R.full[s], use & 1u, 100000000ull);
+  }
 }
 
 // Streams elements [start, end) of `row` through the ring and calls

@@ -299,6 +299,7 @@ __global__ void __launch_bounds__(THREADS, 2)
                                            C1 > (uint32_t)CAP_ALL, key0, key1, kmin, sb, lflags);
     finish_row(S, out, K, lflags, diag, r, path, key_to_float(key0), key_to_float(key1), C0, C1);
   }
+  ring_drain(R);
   // The last CTA to leave resets the queue, so the next launch (or graph
   // replay) starts from zero without a separate memset.
   if (threadIdx.x == 0) {
@@ -367,7 +368,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   for (int64_t i = threadIdx.x; i < a0; i += THREADS) buf[i] = row[i];
   for (int64_t i = a1 + threadIdx.x; i < len; i += THREADS) buf[i] = row[i];
-  if (!mbar_wait(&S.full[0], 0)) lflags |= F_TIMEOUT;
+  if (!mbar_wait(&S.full[0], 0)) {
+    lflags |= F_TIMEOUT;
+    // gave up: still let the copies land (bounded) before this CTA moves on
+    if (threadIdx.x == 0) mbar_wait_drain(&S.full[0], 0, 100000000ull);
+  }
   __syncthreads();
   // Exact boundary over the staged keys: data-relative bins over [min, max].
   uint32_t mn = 0xffffffffu, mx = 0u;
@@ -499,7 +504,10 @@ __global__ void __launch_bounds__(THREADS, 2)
     S.last = (t == (uint32_t)P.segments - 1) ? 1u : 0u;
   }
   __syncthreads();
-  if (!S.last) return;
+  if (!S.last) {
+    ring_drain(R);
+    return;
+  }
   __threadfence();
   int32_t* out = out_idx + r * (int64_t)K;
   const float qnan = __int_as_float(0x7fc00000);
@@ -508,11 +516,13 @@ __global__ void __launch_bounds__(THREADS, 2)
     write_sentinel_row(out, K, len);
     if (threadIdx.x == 0) S.nout = (uint32_t)K;
     finish_row(S, out, K, lflags, diag, r, PATH_SENTINEL, qnan, qnan, 0, 0);
+    ring_drain(R);
     return;
   }
   if (mode == 1) {
     exact_row_stream(row, len, out, K, R, c, lflags);
     finish_row(S, out, K, lflags, diag, r, PATH_DIRECT, qnan, qnan, 0, 0);
+    ring_drain(R);
     return;
   }
   uint32_t C0 = __ldcg(&h->c0);
@@ -529,6 +539,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       select_after_scan(row, len, out, K, R, c, gcand + CAP, sample_spec(P, len), C0, C1, overflow,
                         key0, key1, kmin, sb, lflags);
   finish_row(S, out, K, lflags, diag, r, path, key_to_float(key0), key_to_float(key1), C0, C1);
+  ring_drain(R);
 }
 
 // ------------------------------------------------------------------ launchers
