@@ -46,7 +46,7 @@ def parse():
     ap.add_argument("--N", type=int, default=1048576)
     ap.add_argument("--M", type=int, default=8192)
     ap.add_argument("--K", type=int, default=K_DEFAULT)
-    ap.add_argument("--no-matrix", action="store_true", help="skip the 128K/256K/512K lines")
+    ap.add_argument("--no-matrix", action="store_true", help="skip the 20-shape operator matrix")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-chain", action="store_true",
@@ -469,26 +469,54 @@ def run_gb300(args):
         result["spot_check"] = {"rows": 8, "contract_failures": int((v["check"] != 0).sum()),
                                 "set_mismatches": int(v["set_mismatch"].sum())}
 
-    # extra widths of the operator matrix at M = 8192 (informational)
+    # the operator matrix (informational): widths 128K-1M x M in {512..8192},
+    # causal groups of M rows of the last 8192; per shape the median over
+    # groups (up to 4, spread over the window) of the median of 5 calls
     if not args.no_matrix and rank == 0 and N == 1048576 and M == 8192:
-        del x, out
+        del out
         torch.cuda.empty_cache()
         mat = {}
-        for w in (131072, 262144, 524288):
-            xw, lw = make_inputs(w, M, 0, seed=11, device=dev)
-            dl = lw.to(dev)
-            vb = 4.0 * float(lw.to(torch.int64).sum())
-            tot, perw, _, _ = time_steps(ets, xw, dl, K, max(5, args.steps // 2), 3, 1, stream)
-            km = statistics.mean(perw)
-            mat[str(w)] = {"rows_per_s": M * len(perw) / (tot / 1000.0),
-                           "ms_per_step": tot / len(perw),
-                           "gbps": vb / (km / 1000.0) / 1e9,
-                           "frac": vb / (km / 1000.0) / 1e9 / peak,
-                           "path": ets.plan(M, w, K)["kind"]}
-            del xw
+        for w in (131072, 262144, 524288, 1048576):
+            if w == N:
+                xw, lw = x, lens
+            else:
+                xw, lw = make_inputs(w, 8192, 0, seed=11, device=dev)
+            for m in (512, 1024, 2048, 4096, 8192):
+                groups = sorted({0, (8192 // m) // 3, (2 * (8192 // m)) // 3, 8192 // m - 1})
+                per_group = []
+                vb = 0.0
+                for gi in groups:
+                    xs = xw[gi * m:(gi + 1) * m]
+                    ls = lw[gi * m:(gi + 1) * m]
+                    dls = ls.to(dev)
+                    vb += 4.0 * float(ls.to(torch.int64).sum())
+                    o = torch.empty((m, K), dtype=torch.int32, device=dev)
+                    with torch.cuda.stream(stream):
+                        for _ in range(2):
+                            ets.topk_ragged(xs, dls, K, out=o, stream=stream)
+                    ts = []
+                    for _ in range(5):
+                        a0 = torch.cuda.Event(enable_timing=True)
+                        b0 = torch.cuda.Event(enable_timing=True)
+                        with torch.cuda.stream(stream):
+                            a0.record(stream)
+                            ets.topk_ragged(xs, dls, K, out=o, stream=stream)
+                            b0.record(stream)
+                        stream.synchronize()
+                        ts.append(a0.elapsed_time(b0))
+                    per_group.append(statistics.median(ts))
+                ms = statistics.median(per_group)
+                gbps = vb / len(groups) / (ms / 1000.0) / 1e9
+                mat["%dx%d" % (w, m)] = {"ms": ms, "rows_per_s": m / (ms / 1000.0), "gbps": gbps,
+                                         "frac": gbps / peak, "path": ets.plan(m, w, K)["kind"],
+                                         "groups": len(groups)}
+            if w != N:
+                del xw
             torch.cuda.empty_cache()
-        result["matrix_m8192"] = mat
+        result["operator_matrix"] = mat
+        del x
         x = None
+        torch.cuda.empty_cache()
 
     if not args.no_chain and rank == 0:
         if x is not None:
