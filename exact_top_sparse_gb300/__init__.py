@@ -28,6 +28,7 @@ K_MAX = 4096
 
 PATH_SENTINEL, PATH_DIRECT, PATH_TAU0, PATH_TAU1, PATH_RECOVERY = 0, 1, 2, 3, 4
 FLAG_LEN_CLAMPED, FLAG_OVERFLOW, FLAG_RECOVERY, FLAG_INTERNAL, FLAG_TIMEOUT = 1, 2, 4, 8, 16
+FLAG_K_CLAMPED = 32
 KIND_AUTO, KIND_DIRECT, KIND_PERSISTENT, KIND_KVSPLIT = 0, 1, 2, 3
 KIND_NAMES = {0: "auto", 1: "direct", 2: "persistent", 3: "kvsplit"}
 
@@ -69,7 +70,7 @@ EXPORTS = ("topk_ragged", "topk_ragged_diag", "topk_ragged_ws", "topk_workspace_
            "topk_status_string", "topk_version", "topk_ragged_noalloc",
            "topk_index_scores", "topk_index_topk", "topk_index_read_status",
            "topk_ragged_bf16", "topk_ragged_bf16_diag", "topk_sort_rows", "topk_sort_rows_bf16",
-           "topk_check_wait_timeout")
+           "topk_check_wait_timeout", "topk_ragged_k", "topk_ragged_k_bf16", "topk_ragged_k_diag")
 NOALLOC_MAX_ROWS = 64
 
 _lib = None
@@ -92,6 +93,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.topk_ragged_ws.argtypes = [vp, vp, i64, i64, i32, vp, vp, sz, vp]
     lib.topk_ragged_noalloc.argtypes = [vp, vp, i64, i64, i32, vp, vp]
     lib.topk_ragged_bf16.argtypes = [vp, vp, i64, i64, i32, vp, vp]
+    lib.topk_ragged_k.argtypes = [vp, vp, vp, i64, i64, i32, vp, vp]
+    lib.topk_ragged_k_bf16.argtypes = [vp, vp, vp, i64, i64, i32, vp, vp]
+    lib.topk_ragged_k_diag.argtypes = [vp, vp, vp, i64, i64, i32, vp, vp, vp]
     lib.topk_sort_rows.argtypes = [vp, i64, i64, i32, vp, vp]
     lib.topk_check_wait_timeout.argtypes = [ctypes.c_uint64, vp]
     lib.topk_check_wait_timeout.restype = ctypes.c_int
@@ -117,8 +121,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     for name in ("topk_ragged", "topk_ragged_diag", "topk_ragged_ws", "topk_ragged_host",
                  "topk_ragged_noalloc", "topk_index_scores", "topk_index_topk",
                  "topk_ragged_bf16", "topk_ragged_bf16_diag", "topk_sort_rows",
-                 "topk_sort_rows_bf16",
-                 "topk_index_read_status",
+                 "topk_sort_rows_bf16", "topk_ragged_k", "topk_ragged_k_bf16",
+                 "topk_ragged_k_diag", "topk_index_read_status",
                  "topk_plan", "topk_set_params", "topk_get_params", "topk_read_status",
                  "topk_version"):
         getattr(lib, name).restype = ctypes.c_int
@@ -170,6 +174,43 @@ def topk_ragged(scores: torch.Tensor, row_lens: torch.Tensor, K: int = 2048,
                 _stream_handle(scores.device, stream))
     _check(rc, "topk_ragged")
     return out
+
+
+def _row_k(row_k, scores):
+    if not (isinstance(row_k, torch.Tensor) and row_k.device == scores.device
+            and row_k.dtype == torch.int32 and row_k.dim() == 1
+            and row_k.shape[0] == scores.shape[0] and row_k.is_contiguous()):
+        raise TypeError("row_k must be a contiguous int32 [M] tensor on the scores' device")
+    return row_k
+
+
+def topk_ragged_k(scores: torch.Tensor, row_lens: torch.Tensor, row_k: torch.Tensor,
+                  K_max: int = 2048, out: torch.Tensor = None, stream=None) -> torch.Tensor:
+    """Per-row K: row r gets its Top-k_r, k_r = clamp(row_k[r], 0, K_max), in
+    slots [0, k_r) of an [M, K_max] int32 result; the other slots hold -1."""
+    lib = load_library()
+    M, N, out = _inputs(scores, row_lens, K_max, out, allow_bf16=True)
+    row_k = _row_k(row_k, scores)
+    fn = lib.topk_ragged_k_bf16 if scores.dtype == torch.bfloat16 else lib.topk_ragged_k
+    with torch.cuda.device(scores.device):
+        rc = fn(scores.data_ptr(), row_lens.data_ptr(), row_k.data_ptr(), M, N, K_max,
+                out.data_ptr(), _stream_handle(scores.device, stream))
+    _check(rc, "topk_ragged_k")
+    return out
+
+
+def topk_ragged_k_diag(scores, row_lens, row_k, K_max: int = 2048, out=None, stream=None):
+    """topk_ragged_k (float32 rows) plus per-row diagnostics (host copy)."""
+    lib = load_library()
+    M, N, out = _inputs(scores, row_lens, K_max, out)
+    row_k = _row_k(row_k, scores)
+    diag = torch.empty(M * DIAG_DTYPE.itemsize, dtype=torch.uint8, device=scores.device)
+    with torch.cuda.device(scores.device):
+        rc = lib.topk_ragged_k_diag(scores.data_ptr(), row_lens.data_ptr(), row_k.data_ptr(), M,
+                                    N, K_max, out.data_ptr(), diag.data_ptr(),
+                                    _stream_handle(scores.device, stream))
+    _check(rc, "topk_ragged_k_diag")
+    return out, diag.cpu().numpy().view(DIAG_DTYPE)
 
 
 def topk_sort_rows(scores, out, stream=None):

@@ -19,7 +19,8 @@
 
 namespace {
 
-constexpr int kVersion = 10100;  // 1.1.0: bfloat16 rows, ordered output, indexer scores
+constexpr int kVersion = 10200;  // 1.2.0: per-row K (1.1.0: bfloat16 rows, ordered output,
+                                 // indexer scores)
 constexpr size_t kHdrBytes = 256;
 constexpr int64_t kMinSegment = 32768;  // floats per KV-split segment, at least
 // Planner crossovers, measured on GB300 over 128K-1M columns and M = 64-2048:
@@ -198,6 +199,11 @@ tk::Params kernel_params(int64_t M, int64_t N, int32_t K, const topk_params& p, 
   if (P.long_target1 < P.long_target0) P.long_target1 = P.long_target0;
   P.sample_min_len = p.sample_min_len;
   P.segments = pl.segments;
+  P.row_k = nullptr;
+  P.rho0 = p.rho0;
+  P.rho1 = p.rho1;
+  P.long_rho0 = p.long_rho0;
+  P.long_rho1 = p.long_rho1;
   return P;
 }
 
@@ -253,12 +259,13 @@ int cached_workspace(int dev, cudaStream_t st, size_t need, void** ptr) {
 
 int run(const void* scores, const int32_t* row_lens, int64_t M, int64_t N, int32_t K,
         int32_t* out_idx, topk_row_diag* diag, void* ws, size_t ws_bytes, bool explicit_ws,
-        cudaStream_t st, int elem_bytes = 4) {
+        cudaStream_t st, int elem_bytes = 4, const int32_t* row_k = nullptr) {
   int rc = check_sizes(M, N, K);
   if (rc) return rc;
   rc = validate_ptrs(scores, row_lens, M, N, out_idx, elem_bytes);
   if (rc) return rc;
   if (M == 0) return TOPK_OK;
+  if (row_k && (reinterpret_cast<uintptr_t>(row_k) & 3u)) return TOPK_ERR_ALIGN;
   if (explicit_ws) {
     if (!ws) return TOPK_ERR_ARG;
     if (reinterpret_cast<uintptr_t>(ws) & 255u) return TOPK_ERR_ALIGN;
@@ -277,8 +284,9 @@ int run(const void* scores, const int32_t* row_lens, int64_t M, int64_t N, int32
     rc = cached_workspace(dev, st, pl.ws, &ws);
     if (rc) return rc;
   }
-  return launch(pl, kernel_params(M, N, K, p, pl, elem_bytes), scores, row_lens, out_idx, diag, ws,
-                st);
+  tk::Params P = kernel_params(M, N, K, p, pl, elem_bytes);
+  P.row_k = row_k;
+  return launch(pl, P, scores, row_lens, out_idx, diag, ws, st);
 }
 
 }  // namespace
@@ -314,6 +322,29 @@ int topk_ragged_ws(const float* scores, const int32_t* row_lens, int64_t M, int6
                    struct CUstream_st* stream) {
   return run(scores, row_lens, M, N_alloc, K, out_idx, nullptr, workspace, workspace_bytes, true,
              stream);
+}
+
+int topk_ragged_k(const float* scores, const int32_t* row_lens, const int32_t* row_k, int64_t M,
+                  int64_t N_alloc, int32_t K_max, int32_t* out_idx, struct CUstream_st* stream) {
+  if (M > 0 && !row_k) return TOPK_ERR_ARG;
+  return run(scores, row_lens, M, N_alloc, K_max, out_idx, nullptr, nullptr, 0, false, stream, 4,
+             row_k);
+}
+
+int topk_ragged_k_bf16(const uint16_t* scores, const int32_t* row_lens, const int32_t* row_k,
+                       int64_t M, int64_t N_alloc, int32_t K_max, int32_t* out_idx,
+                       struct CUstream_st* stream) {
+  if (M > 0 && !row_k) return TOPK_ERR_ARG;
+  return run(scores, row_lens, M, N_alloc, K_max, out_idx, nullptr, nullptr, 0, false, stream, 2,
+             row_k);
+}
+
+int topk_ragged_k_diag(const float* scores, const int32_t* row_lens, const int32_t* row_k,
+                       int64_t M, int64_t N_alloc, int32_t K_max, int32_t* out_idx,
+                       topk_row_diag* diag, struct CUstream_st* stream) {
+  if (M > 0 && (!row_k || !diag)) return TOPK_ERR_ARG;
+  return run(scores, row_lens, M, N_alloc, K_max, out_idx, diag, nullptr, 0, false, stream, 4,
+             row_k);
 }
 
 }  // extern "C"

@@ -61,7 +61,7 @@ constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // bounded waits give up afte
 constexpr int32_t PATH_SENTINEL = 0, PATH_DIRECT = 1, PATH_TAU0 = 2, PATH_TAU1 = 3,
                   PATH_RECOVERY = 4;
 constexpr uint32_t F_LEN_CLAMPED = 0x1u, F_OVERFLOW = 0x2u, F_RECOVERY = 0x4u,
-                   F_INTERNAL = 0x8u, F_TIMEOUT = 0x10u;
+                   F_INTERNAL = 0x8u, F_TIMEOUT = 0x10u, F_K_CLAMPED = 0x20u;
 
 constexpr unsigned FULL_MASK = 0xffffffffu;
 

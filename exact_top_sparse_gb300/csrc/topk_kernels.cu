@@ -31,9 +31,35 @@ struct SampleSpec {
   int32_t stride;
   uint32_t target0, target1;
 };
-__device__ __forceinline__ SampleSpec sample_spec(const Params& P, int64_t len) {
-  if (P.long_len > 0 && len >= P.long_len) return {P.long_stride, P.long_target0, P.long_target1};
-  return {P.stride, P.target0, P.target1};
+__device__ __forceinline__ uint32_t target_of(float rho, int32_t k) {
+  return (uint32_t)ceil((double)rho * (double)k);
+}
+// `k` is the row's own K (the call's K unless per-row K values were given).
+__device__ __forceinline__ SampleSpec sample_spec(const Params& P, int64_t len, int32_t k) {
+  const bool lg = P.long_len > 0 && len >= P.long_len;
+  if (k == P.K) {
+    if (lg) return {P.long_stride, P.long_target0, P.long_target1};
+    return {P.stride, P.target0, P.target1};
+  }
+  const uint32_t t0 = target_of(lg ? P.long_rho0 : P.rho0, k);
+  const uint32_t t1 = target_of(lg ? P.long_rho1 : P.rho1, k);
+  return {lg ? P.long_stride : P.stride, t0, t1 < t0 ? t0 : t1};
+}
+
+// The row's own K: the call's K, or clamp(row_k[r], 0, K) when per-row
+// values were given (a value outside that range is flagged).
+__device__ __forceinline__ int32_t row_k_of(const Params& P, int64_t r, uint32_t& fl) {
+  if (P.row_k == nullptr) return P.K;
+  int32_t k = P.row_k[r];
+  if (k < 0) {
+    k = 0;
+    fl |= F_K_CLAMPED;
+  }
+  if (k > P.K) {
+    k = P.K;
+    fl |= F_K_CLAMPED;
+  }
+  return k;
 }
 
 // ------------------------------------------------------- shared-memory plan
@@ -52,6 +78,7 @@ struct KvHdr {
   uint32_t key0, key1, kmin, kmax;
   uint32_t c0, ncand, ticket, ovf, flags;
   float tau0, tau1;
+  int32_t k;  // the row's own K
 };
 constexpr size_t KV_HIST_OFF = 256;
 constexpr size_t KV_CAND_OFF = KV_HIST_OFF + (size_t)NB * sizeof(uint32_t);
@@ -90,11 +117,13 @@ __device__ __forceinline__ int64_t clamp_len(int32_t raw, int64_t n_alloc, uint3
   return v;
 }
 
-// Closes a row: pads a short output (only after an internal failure), folds
-// the per-thread flags and writes the diagnostics.  Every thread must call.
-__device__ void finish_row(Shared& S, int32_t* out, int32_t K, uint32_t lflags, RowDiag* diag,
-                           int64_t r, int32_t path, float tau0, float tau1, uint32_t c0,
-                           uint32_t c1) {
+// Closes a row of K selected slots in an output row of Kout >= K slots: pads
+// a short selection (only after an internal failure) and the slots past K
+// with -1, folds the per-thread flags and writes the diagnostics.  Every
+// thread must call.
+__device__ void finish_row(Shared& S, int32_t* out, int32_t K, int32_t Kout, uint32_t lflags,
+                           RowDiag* diag, int64_t r, int32_t path, float tau0, float tau1,
+                           uint32_t c0, uint32_t c1) {
   __syncthreads();
   const uint32_t nout = S.nout;
   if (nout != (uint32_t)K) {
@@ -102,6 +131,7 @@ __device__ void finish_row(Shared& S, int32_t* out, int32_t K, uint32_t lflags, 
     for (uint32_t i = min(nout, (uint32_t)K) + threadIdx.x; i < (uint32_t)K; i += THREADS)
       out[i] = -1;
   }
+  for (int32_t i = K + (int32_t)threadIdx.x; i < Kout; i += THREADS) out[i] = -1;
   if (lflags) atomicOr(&S.flags, lflags);
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -270,22 +300,25 @@ __global__ void __launch_bounds__(THREADS, 2)
     if (threadIdx.x == 0) S.nout = 0;
     __syncthreads();
     const float qnan = __int_as_float(0x7fc00000);
-    if (len <= K) {
-      write_sentinel_row(out, K, len);
-      if (threadIdx.x == 0) S.nout = (uint32_t)K;
-      finish_row(S, out, K, lflags, diag, r, PATH_SENTINEL, qnan, qnan, 0, 0);
+    const int32_t K0 = row_k_of(P, r, lflags);
+    if (len <= K0 || K0 == 0) {
+      write_sentinel_row(out, K0, len);
+      if (threadIdx.x == 0) S.nout = (uint32_t)K0;
+      finish_row(S, out, K0, K, lflags, diag, r, PATH_SENTINEL, qnan, qnan, 0, 0);
       continue;
     }
     if (len < P.sample_min_len) {
-      exact_row_stream(row, len, out, K, R, c, lflags);
-      finish_row(S, out, K, lflags, diag, r, PATH_DIRECT, qnan, qnan, 0, 0);
+      exact_row_stream(row, len, out, K0, R, c, lflags);
+      finish_row(S, out, K0, K, lflags, diag, r, PATH_DIRECT, qnan, qnan, 0, 0);
       continue;
     }
     // the ring is idle: start the row's first chunks before sampling it
     const uint32_t primed = ring_prime(R, row, 0, len, lflags);
-    const SampleSpec sp = sample_spec(P, len);
-    sample_thresholds(row, len, sp.stride, sp.target0, sp.target1,
-                      reinterpret_cast<uint32_t*>(c.cand), c.hist, c.list, S);
+    {
+      const SampleSpec sp = sample_spec(P, len, K0);
+      sample_thresholds(row, len, sp.stride, sp.target0, sp.target1,
+                        reinterpret_cast<uint32_t*>(c.cand), c.hist, c.list, S);
+    }
     const uint32_t key0 = S.key0, key1 = S.key1, kmin = S.kmin, kmax = S.kmax;
     const Bins sb = scan_bins(key1, kmax);
     __syncthreads();
@@ -295,9 +328,14 @@ __global__ void __launch_bounds__(THREADS, 2)
     uint32_t C0 = scan_collect(row, 0, len, R, c, spill, key0, key1, sb, lflags, primed);
     const uint32_t C1 = S.ncand;
     __syncthreads();
-    const int32_t path = select_after_scan(row, len, out, K, R, c, spill, sp, C0, C1,
+    // the row's K and sampling spec again, rather than held in registers
+    // over the scan
+    const int32_t Kr = row_k_of(P, r, lflags);
+    const int32_t path = select_after_scan(row, len, out, Kr, R, c, spill, sample_spec(P, len, Kr),
+                                           C0, C1,
                                            C1 > (uint32_t)CAP_ALL, key0, key1, kmin, sb, lflags);
-    finish_row(S, out, K, lflags, diag, r, path, key_to_float(key0), key_to_float(key1), C0, C1);
+    finish_row(S, out, Kr, K, lflags, diag, r, path, key_to_float(key0), key_to_float(key1), C0,
+               C1);
   }
   ring_drain(R);
   // The last CTA to leave resets the queue, so the next launch (or graph
@@ -326,6 +364,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int32_t K = P.K;
   uint32_t lflags = 0;
   const int64_t len = clamp_len(row_lens[r], P.N_alloc, lflags);
+  const int32_t Kr = row_k_of(P, r, lflags);
   const E* row = scores + r * P.N_alloc;
   int32_t* out = out_idx + r * (int64_t)K;
   const float qnan = __int_as_float(0x7fc00000);
@@ -334,10 +373,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     S.nout = 0;
   }
   __syncthreads();
-  if (len <= K) {
-    write_sentinel_row(out, K, len);
-    if (threadIdx.x == 0) S.nout = (uint32_t)K;
-    finish_row(S, out, K, lflags, diag, r, PATH_SENTINEL, qnan, qnan, 0, 0);
+  if (len <= Kr || Kr == 0) {
+    write_sentinel_row(out, Kr, len);
+    if (threadIdx.x == 0) S.nout = (uint32_t)Kr;
+    finish_row(S, out, Kr, K, lflags, diag, r, PATH_SENTINEL, qnan, qnan, 0, 0);
     return;
   }
   // Stage the row: the 16-byte aligned body by bulk copies, head and tail
@@ -390,8 +429,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   HistF hf{bins, hist};
   src.for_each(hf, lflags);
   __syncthreads();
-  refine(src, bins, (uint32_t)K, hist, nullptr, out, K, S, lflags);
-  finish_row(S, out, K, lflags, diag, r, PATH_DIRECT, qnan, qnan, 0, 0);
+  refine(src, bins, (uint32_t)Kr, hist, nullptr, out, Kr, S, lflags);
+  finish_row(S, out, Kr, K, lflags, diag, r, PATH_DIRECT, qnan, qnan, 0, 0);
 }
 
 // --------------------------------------------------------------- KV-split path
@@ -412,17 +451,18 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int64_t r = blockIdx.x;
   uint32_t lflags = 0;
   const int64_t len = clamp_len(row_lens[r], P.N_alloc, lflags);
+  const int32_t Kr = row_k_of(P, r, lflags);
   const E* row = scores + r * P.N_alloc;
   uint8_t* base = ws_rows + (size_t)r * KV_ROW_BYTES;
   KvHdr* h = reinterpret_cast<KvHdr*>(base);
   uint32_t* ghist = reinterpret_cast<uint32_t*>(base + KV_HIST_OFF);
   for (int i = threadIdx.x; i < NB; i += THREADS) ghist[i] = 0;
   uint32_t mode = 2;
-  if (len <= P.K) mode = 0;
+  if (len <= Kr || Kr == 0) mode = 0;
   else if (len < P.sample_min_len) mode = 1;
   uint32_t key0 = 0, key1 = 0, kmin = 0, kmax = 0;
   if (mode == 2) {
-    const SampleSpec sp = sample_spec(P, len);
+    const SampleSpec sp = sample_spec(P, len, Kr);
     sample_thresholds(row, len, sp.stride, sp.target0, sp.target1, skeys, hist, list, S);
     key0 = S.key0;
     key1 = S.key1;
@@ -443,6 +483,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     h->flags = lflags;
     h->tau0 = key_to_float(key0);
     h->tau1 = key_to_float(key1);
+    h->k = Kr;
   }
 }
 
@@ -465,6 +506,7 @@ __global__ void __launch_bounds__(THREADS, 2)
   const uint32_t key0 = h->key0, key1 = h->key1, kmin = h->kmin, kmax = h->kmax;
   const E* row = scores + r * P.N_alloc;
   const int32_t K = P.K;
+  const int32_t Kr = h->k;
   if (threadIdx.x == 0) {
     S.flags = 0;
     S.nout = 0;
@@ -513,15 +555,15 @@ __global__ void __launch_bounds__(THREADS, 2)
   const float qnan = __int_as_float(0x7fc00000);
   lflags |= __ldcg(&h->flags);
   if (mode == 0) {
-    write_sentinel_row(out, K, len);
-    if (threadIdx.x == 0) S.nout = (uint32_t)K;
-    finish_row(S, out, K, lflags, diag, r, PATH_SENTINEL, qnan, qnan, 0, 0);
+    write_sentinel_row(out, Kr, len);
+    if (threadIdx.x == 0) S.nout = (uint32_t)Kr;
+    finish_row(S, out, Kr, K, lflags, diag, r, PATH_SENTINEL, qnan, qnan, 0, 0);
     ring_drain(R);
     return;
   }
   if (mode == 1) {
-    exact_row_stream(row, len, out, K, R, c, lflags);
-    finish_row(S, out, K, lflags, diag, r, PATH_DIRECT, qnan, qnan, 0, 0);
+    exact_row_stream(row, len, out, Kr, R, c, lflags);
+    finish_row(S, out, Kr, K, lflags, diag, r, PATH_DIRECT, qnan, qnan, 0, 0);
     ring_drain(R);
     return;
   }
@@ -536,9 +578,10 @@ __global__ void __launch_bounds__(THREADS, 2)
   }
   __syncthreads();
   const int32_t path =
-      select_after_scan(row, len, out, K, R, c, gcand + CAP, sample_spec(P, len), C0, C1, overflow,
-                        key0, key1, kmin, sb, lflags);
-  finish_row(S, out, K, lflags, diag, r, path, key_to_float(key0), key_to_float(key1), C0, C1);
+      select_after_scan(row, len, out, Kr, R, c, gcand + CAP, sample_spec(P, len, Kr), C0, C1,
+                        overflow, key0, key1, kmin, sb, lflags);
+  finish_row(S, out, Kr, K, lflags, diag, r, path, key_to_float(key0), key_to_float(key1), C0,
+             C1);
   ring_drain(R);
 }
 

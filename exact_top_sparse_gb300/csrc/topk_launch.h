@@ -23,6 +23,11 @@ struct Params {
   int32_t long_stride;
   uint32_t long_target0;
   uint32_t long_target1;
+  // Per-row K (nullptr: every row takes K).  Row r then selects
+  // clamp(row_k[r], 0, K) and its targets are ceil(rho * that) with the rho
+  // of its sampling tier; the output row stride stays K.
+  const int32_t* row_k;
+  float rho0, rho1, long_rho0, long_rho1;
 };
 
 // Same layout as topk_row_diag in the public header.

@@ -82,6 +82,7 @@ typedef enum topk_status {
 #define TOPK_FLAG_RECOVERY 0x4u    /* exact whole-row recovery ran */
 #define TOPK_FLAG_INTERNAL 0x8u    /* an internal invariant failed (a library bug; the row is not valid) */
 #define TOPK_FLAG_TIMEOUT 0x10u    /* a bounded wait on an asynchronous copy gave up (the row is not valid) */
+#define TOPK_FLAG_K_CLAMPED 0x20u  /* row_k[r] was outside [0, K_max] and was clamped (per-row K calls) */
 
 /* Execution paths of the host planner (topk_plan_info.kind, topk_params.force_kind). */
 #define TOPK_KIND_AUTO 0
@@ -173,6 +174,29 @@ size_t topk_workspace_bytes(int64_t M, int64_t N_alloc, int32_t K);
 int topk_ragged_ws(const float* scores, const int32_t* row_lens, int64_t M, int64_t N_alloc,
                    int32_t K, int32_t* out_idx, void* workspace, size_t workspace_bytes,
                    struct CUstream_st* stream);
+
+/* Per-row K.  Row r takes its own k_r = clamp(row_k[r], 0, K_max) (a value
+ * outside that range sets TOPK_FLAG_K_CLAMPED) and gets the result of
+ * topk_ragged() with K = k_r in slots [0, k_r) of an output row of K_max
+ * slots; slots [k_r, K_max) hold -1.  So k_r = 0 gives a row of -1, and
+ * len_r <= k_r gives 0..len_r-1 followed by -1.  A sampled row's targets are
+ * ceil(rho * k_r) with the rho of its sampling tier (topk_params).  The
+ * pages use one K for every row (PaperDaily, section 问题四: K = 2048
+ * throughout); per-row K is an extension for callers whose rows need
+ * different budgets.
+ *   row_k    device, [M] int32
+ *   K_max    1 <= K_max <= TOPK_K_MAX: the output row stride
+ *   out_idx  device, [M][K_max] int32, written completely
+ * Other arguments, workspace and errors as topk_ragged() (and
+ * topk_ragged_bf16() / topk_ragged_diag() for the _bf16 / _diag forms). */
+int topk_ragged_k(const float* scores, const int32_t* row_lens, const int32_t* row_k, int64_t M,
+                  int64_t N_alloc, int32_t K_max, int32_t* out_idx, struct CUstream_st* stream);
+int topk_ragged_k_bf16(const uint16_t* scores, const int32_t* row_lens, const int32_t* row_k,
+                       int64_t M, int64_t N_alloc, int32_t K_max, int32_t* out_idx,
+                       struct CUstream_st* stream);
+int topk_ragged_k_diag(const float* scores, const int32_t* row_lens, const int32_t* row_k,
+                       int64_t M, int64_t N_alloc, int32_t K_max, int32_t* out_idx,
+                       topk_row_diag* diag, struct CUstream_st* stream);
 
 /* Rows topk_ragged_noalloc() accepts in one call. */
 #define TOPK_NOALLOC_MAX_ROWS 64

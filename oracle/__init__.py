@@ -20,6 +20,8 @@ Parity status: the selection, the boundary values and the checker are pinned
 by brute force, closed forms and hand-built tie rows in tests/.  The
 thresholds are pinned by closed forms on strictly monotone rows; the rank rule
 itself (ceil(T * n_s / len)) is a reading of the pages, which do not print it.
+Per-row K (topk_per_row) composes the one-K selection row by row and is
+pinned by brute force on tiny rows and its closed forms (k = 0, k = K_max).
 The indexer scores are pinned by a hand-derived case, the one-hot closed form,
 invariances of eq. (1) and exact dense products on tiny integer inputs.
 """
@@ -190,6 +192,50 @@ def compare(scores, row_lens, K: int, got, threads: int = 0):
     _, _, tied = boundary(scores, row_lens, K, threads)
     mism = np.any(np.sort(got, axis=1) != np.sort(ref, axis=1), axis=1) & ~tied
     return {"check": codes, "tied": tied, "set_mismatch": mism}
+
+
+def clamp_row_k(row_k, K_max: int) -> np.ndarray:
+    """Per-row K as the library under test documents it: clamp into [0, K_max]."""
+    return np.clip(np.asarray(row_k, dtype=np.int64), 0, K_max)
+
+
+def topk_per_row(scores, row_lens, row_k, K_max: int, threads: int = 0) -> np.ndarray:
+    """Per-row K: row r holds the exact Top-k_r of its valid prefix
+    (k_r = clamp(row_k[r], 0, K_max); the set contract with K = k_r) in slots
+    [0, k_r) of an [M, K_max] int32 result, -1 in the other slots.  The pages
+    fix one K per call; this composes the one-K definition row by row."""
+    scores, row_lens = _as_inputs(scores, row_lens)
+    ks = clamp_row_k(row_k, K_max)
+    out = np.full((scores.shape[0], K_max), -1, dtype=np.int32)
+    for k in np.unique(ks):
+        if k == 0:
+            continue
+        rows = np.nonzero(ks == k)[0]
+        out[rows, :k] = topk(scores[rows], row_lens[rows], int(k), threads)
+    return out
+
+
+def compare_per_row(scores, row_lens, row_k, K_max: int, got, threads: int = 0):
+    """Parity verdict for a per-row-K result: each row's first k_r slots get
+    the one-K verdict of ``compare`` at K = k_r; ``tail`` marks rows whose
+    slots [k_r, K_max) are not all -1."""
+    scores, row_lens = _as_inputs(scores, row_lens)
+    got = np.ascontiguousarray(got, dtype=np.int32)
+    M = scores.shape[0]
+    if got.shape != (M, K_max):
+        raise ValueError("got must be [M, K_max]")
+    ks = clamp_row_k(row_k, K_max)
+    codes = np.zeros(M, dtype=np.int32)
+    tied = np.zeros(M, dtype=bool)
+    mism = np.zeros(M, dtype=bool)
+    tail = np.array([np.any(got[r, ks[r]:] != -1) for r in range(M)], dtype=bool)
+    for k in np.unique(ks):
+        if k == 0:
+            continue
+        rows = np.nonzero(ks == k)[0]
+        v = compare(scores[rows], row_lens[rows], int(k), got[rows, :k], threads)
+        codes[rows], tied[rows], mism[rows] = v["check"], v["tied"], v["set_mismatch"]
+    return {"check": codes, "tied": tied, "set_mismatch": mism, "tail": tail}
 
 
 def index_scores(q_bits, k_bits, w, ts, ss, threads: int = 0):

@@ -52,7 +52,7 @@ def test_library_is_built_for_sm103a(lib):
 
 def test_host_only_calls(lib):
     import exact_top_sparse_gb300 as ets
-    assert ets.version() == 10100
+    assert ets.version() == 10200
     assert lib.topk_status_string(0) == b"ok"
     assert lib.topk_status_string(-5).startswith(b"workspace allocation")
     d = ets.default_params()
@@ -85,6 +85,14 @@ def test_argument_errors_need_no_device(lib):
     assert lib.topk_ragged_ws(vp(16), vp(16), 1, 10, 4, vp(16), None, 0, None) == -1
     assert lib.topk_ragged_ws(vp(16), vp(16), 1, 10, 4, vp(16), vp(100), 1 << 20, None) == -2
     assert lib.topk_workspace_bytes(0, 10, 4) == 0
+    # per-row K: null row_k, K_max out of range, misaligned row_k
+    assert lib.topk_ragged_k(vp(16), vp(16), None, 1, 10, 4, vp(16), None) == -1
+    assert lib.topk_ragged_k(vp(16), vp(16), vp(16), 1, 10, 0, vp(16), None) == -1
+    assert lib.topk_ragged_k(vp(16), vp(16), vp(16), 1, 10, 4097, vp(16), None) == -6
+    assert lib.topk_ragged_k(vp(16), vp(16), vp(18), 1, 10, 4, vp(16), None) == -2
+    assert lib.topk_ragged_k(None, None, None, 0, 10, 4, None, None) == 0
+    assert lib.topk_ragged_k_bf16(vp(16), vp(16), None, 1, 10, 4, vp(16), None) == -1
+    assert lib.topk_ragged_k_diag(vp(16), vp(16), vp(16), 1, 10, 4, vp(16), None, None) == -1
 
 
 def test_no_device_is_an_error_code_not_a_crash(lib):
