@@ -275,25 +275,37 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def profiled_traffic(kind, valid_bytes):
+SAMPLING_KNOBS = ("stride", "rho0", "rho1", "sample_min_len", "long_len", "long_stride",
+                  "long_rho0", "long_rho1")
+
+
+def kernel_fingerprint(params, kind, grid):
+    """Hash of what decides a selector launch's DRAM traffic: the kernel
+    sources, the sampling parameters in effect and the launch shape."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in ("topk_device.cuh", "topk_kernels.cu", "topk_launch.h"):
+        with open(os.path.join(ROOT, "exact_top_sparse_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    launch = {"sampling": {k: params[k] for k in SAMPLING_KNOBS}, "kind": kind, "grid": grid}
+    h.update(json.dumps(launch, sort_keys=True).encode())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(params, plan, valid_bytes):
     """DRAM bytes per launch from the committed ncu capture of this kernel.
 
     profiles/k_persistent_traffic.json holds the DRAM-bytes-per-valid-byte
-    ratio of one capture and a hash of the kernel and planner sources (the
-    planner holds the sampling defaults) it was taken on;
-    the figure is reported only while those sources are unchanged (else None).
+    ratio of one capture and the kernel fingerprint (sources, sampling
+    parameters, launch shape) it was taken with; the figure is reported only
+    while the fingerprint still matches (else None).
     """
-    import hashlib
     p = os.path.join(ROOT, "profiles", "k_persistent_traffic.json")
-    if kind != "persistent" or not os.path.exists(p):
+    if plan["kind"] != "persistent" or not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    h = hashlib.sha256()
-    for name in ("topk_device.cuh", "topk_kernels.cu", "topk_launch.h", "topk_api.cu"):
-        with open(os.path.join(ROOT, "exact_top_sparse_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
-    if h.hexdigest()[:16] != d.get("kernel_sources_sha256_16"):
+    if kernel_fingerprint(params, plan["kind"], plan["grid"]) != d.get("kernel_fingerprint"):
         return None
     return float(d["dram_bytes_per_valid_byte"]) * valid_bytes
 
@@ -451,7 +463,7 @@ def run_gb300(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "traffic": (args.traffic if args.traffic is not None
-                                 else profiled_traffic(plan["kind"], valid_bytes)),
+                                 else profiled_traffic(ets.get_params(), plan, valid_bytes)),
                      "bytes_per_launch": valid_bytes,
                      "kernel": "k_kv_segment" if plan["kind"] == "kvsplit" else
                                ("k_direct" if plan["kind"] == "direct" else "k_persistent")},

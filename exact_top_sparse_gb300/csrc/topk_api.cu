@@ -64,8 +64,8 @@ void defaults(topk_params* p) {
   p->stride = 256;
   p->rho0 = 2.0f;
   p->rho1 = 2.25f;
-  p->sample_min_len = 16384;
-  p->direct_max = 49152;
+  p->sample_min_len = 12288;
+  p->direct_max = 16384;
   p->force_kind = TOPK_KIND_AUTO;
   p->kv_segments = 0;
   p->long_len = 786432;

@@ -168,6 +168,58 @@ __device__ void exact_row_stream(const E* row, int64_t len, int32_t* out, int32_
   refine(RowSrc<E>{&R, row, len}, bins, (uint32_t)K, c.hist, c.cand, out, K, S, lflags);
 }
 
+// Exact selection of a row staged in shared memory (element i at buf[i]):
+// data-relative bins over the keys' [min, max], one histogram pass, then
+// refinement rounds on chip.
+template <class E>
+__device__ void select_staged(const E* buf, int64_t len, int32_t* out, int32_t K, uint32_t* hist,
+                              Shared& S, uint32_t& lflags) {
+  uint32_t mn = 0xffffffffu, mx = 0u;
+  for (int64_t i = threadIdx.x; i < len; i += THREADS) {
+    const uint32_t k = fkey(Elem<E>::load(buf + i));
+    mn = min(mn, k);
+    mx = max(mx, k);
+  }
+  uint32_t kmin, kmax;
+  block_minmax(mn, mx, S, &kmin, &kmax);
+  const Bins bins = make_bins(kmin, kmax);
+  clear_hist(hist);
+  __syncthreads();
+  const StagedSrc<E> src{buf, (uint32_t)len};
+  HistF hf{bins, hist};
+  src.for_each(hf, lflags);
+  __syncthreads();
+  refine(src, bins, (uint32_t)K, hist, nullptr, out, K, S, lflags);
+}
+
+// Rows an unsampled row can be staged for in the candidate buffer (which
+// such a row does not otherwise use).
+template <class E>
+__device__ __forceinline__ bool fits_stage(int64_t len) {
+  return len * (int64_t)Elem<E>::kSize <= (int64_t)CAP * (int64_t)sizeof(uint2);
+}
+
+// Exact selection of a short row: one read of the row into the candidate
+// buffer, then the on-chip selection.
+template <class E>
+__device__ void exact_row_staged(const E* row, int64_t len, int32_t* out, int32_t K,
+                                 const RowCarve& c, uint32_t& lflags) {
+  E* buf = reinterpret_cast<E*>(c.cand);
+  __syncthreads();  // earlier users of the candidate buffer are done
+  int64_t i = threadIdx.x;
+#pragma unroll 1
+  for (; i + 7 * THREADS < len; i += 8 * THREADS) {
+    E v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = __ldcs(row + i + u * THREADS);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) buf[i + u * THREADS] = v[u];
+  }
+  for (; i < len; i += THREADS) buf[i] = __ldcs(row + i);
+  __syncthreads();
+  select_staged(buf, len, out, K, c.hist, *c.S, lflags);
+}
+
 // The full-row certify+collect pass over [s0, s1): candidates in c.cand and
 // past CAP in `spill` (nullptr: none), their count in S.ncand (past the
 // capacity when they did not fit), the seeded histogram of the kept ones in
@@ -308,7 +360,8 @@ __global__ void __launch_bounds__(THREADS, 2)
       continue;
     }
     if (len < P.sample_min_len) {
-      exact_row_stream(row, len, out, K0, R, c, lflags);
+      if (fits_stage<E>(len)) exact_row_staged(row, len, out, K0, c, lflags);
+      else exact_row_stream(row, len, out, K0, R, c, lflags);
       finish_row(S, out, K0, K, lflags, diag, r, PATH_DIRECT, qnan, qnan, 0, 0);
       continue;
     }
@@ -413,23 +466,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (threadIdx.x == 0) mbar_wait_drain(&S.full[0], 0, 100000000ull);
   }
   __syncthreads();
-  // Exact boundary over the staged keys: data-relative bins over [min, max].
-  uint32_t mn = 0xffffffffu, mx = 0u;
-  for (int64_t i = threadIdx.x; i < len; i += THREADS) {
-    const uint32_t k = fkey(Elem<E>::load(buf + i));
-    mn = min(mn, k);
-    mx = max(mx, k);
-  }
-  uint32_t kmin, kmax;
-  block_minmax(mn, mx, S, &kmin, &kmax);
-  const Bins bins = make_bins(kmin, kmax);
-  clear_hist(hist);
-  __syncthreads();
-  const StagedSrc<E> src{buf, (uint32_t)len};
-  HistF hf{bins, hist};
-  src.for_each(hf, lflags);
-  __syncthreads();
-  refine(src, bins, (uint32_t)Kr, hist, nullptr, out, Kr, S, lflags);
+  select_staged(buf, len, out, Kr, hist, S, lflags);
   finish_row(S, out, Kr, K, lflags, diag, r, PATH_DIRECT, qnan, qnan, 0, 0);
 }
 
@@ -562,7 +599,8 @@ __global__ void __launch_bounds__(THREADS, 2)
     return;
   }
   if (mode == 1) {
-    exact_row_stream(row, len, out, Kr, R, c, lflags);
+    if (fits_stage<E>(len)) exact_row_staged(row, len, out, Kr, c, lflags);
+    else exact_row_stream(row, len, out, Kr, R, c, lflags);
     finish_row(S, out, Kr, K, lflags, diag, r, PATH_DIRECT, qnan, qnan, 0, 0);
     ring_drain(R);
     return;

@@ -114,8 +114,9 @@ typedef struct topk_params {
   int32_t stride;          /* sample stride s >= 1 (default 256) */
   float rho0;              /* primary target as a multiple of K (default 2.0) */
   float rho1;              /* secondary target, >= rho0 (default 2.25) */
-  int64_t sample_min_len;  /* rows shorter than this skip sampling (exact boundary) */
-  int64_t direct_max;      /* N_alloc at or below which the on-chip direct kernel serves every row */
+  int64_t sample_min_len;  /* rows shorter than this skip sampling (exact boundary; default 12288) */
+  int64_t direct_max;      /* N_alloc at or below which the on-chip direct kernel serves every row
+                              (default 16384) */
   int32_t force_kind;      /* TOPK_KIND_*; AUTO lets the planner choose */
   int32_t kv_segments;     /* KV-split segments per row; 0 = planner's choice */
   int64_t long_len;        /* rows this long or longer use the long_* knobs; 0 = never (default 786432) */

@@ -59,6 +59,7 @@ def test_host_only_calls(lib):
     assert d["stride"] == 256 and d["rho0"] == 2.0 and d["rho1"] == 2.25
     assert d["long_len"] == 786432 and d["long_stride"] == 512
     assert d["long_rho0"] == 2.75 and d["long_rho1"] == 3.0
+    assert d["sample_min_len"] == 12288 and d["direct_max"] == 16384
     old = ets.set_params(stride=64)
     try:
         assert ets.get_params()["stride"] == 64

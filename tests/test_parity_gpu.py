@@ -344,6 +344,34 @@ def test_clamped_lengths_and_status(params, kind):
     assert not dg["flags"][2] & ets.FLAG_LEN_CLAMPED
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("kind", ["persistent", "kvsplit"])
+def test_unsampled_rows_staged_and_streamed(params, kind, dtype):
+    """Rows below sample_min_len on the persistent and KV-split kernels: the
+    ones whose scores fit the 48 KB candidate buffer (12288 FP32 or 24576
+    bfloat16 values) are loaded once and selected on chip, longer ones
+    stream through the ring; lengths straddle that limit, K and the row
+    lengths straddle each other."""
+    ets = params
+    ets.set_params(force_kind=ets.KIND_PERSISTENT if kind == "persistent" else ets.KIND_KVSPLIT,
+                   sample_min_len=1 << 20, kv_segments=3 if kind == "kvsplit" else 0)
+    N = 40000
+    lens = torch.tensor([2049, 2500, 4096, 8191, 12287, 12288, 12289, 20000, 24575, 24576, 24577,
+                         40000, 2048, 0, 9999, 31111], dtype=torch.int32)
+    x = synth.indexer_rows(lens, N, seed=17, device=DEV)
+    if dtype == "bf16":
+        x = x.to(torch.bfloat16)
+    got, dg = ets.topk_ragged_diag(x, lens.to(DEV), K)
+    torch.cuda.synchronize()
+    verify(x.float(), lens, K, got)
+    assert set(dg["path"].tolist()) <= {ets.PATH_SENTINEL, ets.PATH_DIRECT}
+    assert not np.any(dg["flags"] & (ets.FLAG_INTERNAL | ets.FLAG_TIMEOUT))
+    # a short K over the same rows: boundary well inside the row
+    got = ets.topk_ragged(x, lens.to(DEV), 5)
+    torch.cuda.synchronize()
+    verify(x.float(), lens, 5, got)
+
+
 @pytest.mark.parametrize("k", [1, 7, 2048, 4096])
 @pytest.mark.parametrize("kind", ["direct", "persistent", "kvsplit"])
 def test_other_k(params, k, kind):
