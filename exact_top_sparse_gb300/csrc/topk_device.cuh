@@ -173,6 +173,12 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   return p;
 }
 
+// L2 prefetch of the line holding `p` (no data returned to the thread),
+// marked evict-last.
+__device__ __forceinline__ void prefetch_l2_keep(const void* p) {
+  asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));
+}
+
 // 1-D bulk copy global -> shared, completion counted on `bar` (bytes % 16 == 0,
 // both addresses 16-byte aligned).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
@@ -260,6 +266,7 @@ struct __align__(16) Shared {
   uint32_t kmin, kmax, res;
   uint32_t key0, key1;
   uint32_t last;
+  uint32_t next, next_ok;        // a row claimed ahead of time (persistent kernel)
 };
 
 // Exclusive prefix sum over all THREADS threads (every thread must call).

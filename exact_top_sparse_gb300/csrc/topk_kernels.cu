@@ -325,6 +325,18 @@ __device__ int32_t select_after_scan(const E* row, int64_t len, int32_t* out, in
   return path;
 }
 
+// Warms L2 with the sample points of a row the CTA takes next (evict-last,
+// as the sampler's own loads), so that its sampling, latency-bound DRAM
+// loads otherwise, reads L2 instead.  Issued while the current row is
+// refined.  Every address lies inside the row's valid prefix.  Every thread
+// may call.  (Prefetching the row's first ring chunks as well measured no
+// faster.)
+template <class E>
+__device__ void warm_samples(const E* row, int64_t len, int32_t stride) {
+  const int64_t ns = (len + stride - 1) / stride;
+  for (int64_t i = threadIdx.x; i < ns; i += THREADS) prefetch_l2_keep(row + i * stride);
+}
+
 // ------------------------------------------------------------ persistent path
 template <class E>
 __global__ void __launch_bounds__(THREADS, 2)
@@ -335,12 +347,18 @@ __global__ void __launch_bounds__(THREADS, 2)
   const RowCarve c = carve(smem);
   uint2* spill = spill_all + (size_t)blockIdx.x * SPILL;
   Shared& S = *c.S;
-  if (threadIdx.x == 0) S.flags = 0;
+  if (threadIdx.x == 0) {
+    S.flags = 0;
+    S.next_ok = 0;
+  }
   Ring R;
   ring_init(R, S, c.ring);
   const int32_t K = P.K;
   for (;;) {
-    if (threadIdx.x == 0) S.row = atomicAdd(&hdr[0], 1u);
+    if (threadIdx.x == 0) {
+      S.row = S.next_ok ? S.next : atomicAdd(&hdr[0], 1u);
+      S.next_ok = 0;
+    }
     __syncthreads();
     const int64_t r = S.row;
     __syncthreads();
@@ -379,8 +397,24 @@ __global__ void __launch_bounds__(THREADS, 2)
     if (threadIdx.x == 0) S.ncand = 0;
     __syncthreads();
     uint32_t C0 = scan_collect(row, 0, len, R, c, spill, key0, key1, sb, lflags, primed);
+    // claim the next row now and warm L2 with its sample points while this
+    // one is refined
+    if (threadIdx.x == 0) {
+      S.next = atomicAdd(&hdr[0], 1u);
+      S.next_ok = 1u;
+    }
     const uint32_t C1 = S.ncand;
     __syncthreads();
+    {
+      const int64_t rn = S.next;
+      if (rn < P.M) {
+        uint32_t fl = 0;
+        const int64_t ln = clamp_len(row_lens[rn], P.N_alloc, fl);
+        const int32_t kn = row_k_of(P, rn, fl);
+        if (ln > kn && kn > 0 && ln >= P.sample_min_len)
+          warm_samples(scores + rn * P.N_alloc, ln, sample_spec(P, ln, kn).stride);
+      }
+    }
     // the row's K and sampling spec again, rather than held in registers
     // over the scan
     const int32_t Kr = row_k_of(P, r, lflags);
