@@ -70,8 +70,8 @@ void defaults(topk_params* p) {
   p->kv_segments = 0;
   p->long_len = 786432;
   p->long_stride = 512;
-  p->long_rho0 = 2.5f;
-  p->long_rho1 = 2.75f;
+  p->long_rho0 = 2.75f;
+  p->long_rho1 = 3.0f;
 }
 
 topk_params params_snapshot() {

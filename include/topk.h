@@ -121,8 +121,8 @@ typedef struct topk_params {
   int32_t kv_segments;     /* KV-split segments per row; 0 = planner's choice */
   int64_t long_len;        /* rows this long or longer use the long_* knobs; 0 = never (default 786432) */
   int32_t long_stride;     /* default 512 */
-  float long_rho0;         /* default 2.5 */
-  float long_rho1;         /* >= long_rho0, default 2.75 */
+  float long_rho0;         /* default 2.75 */
+  float long_rho1;         /* >= long_rho0, default 3.0 */
 } topk_params;
 
 typedef struct topk_plan_info {

@@ -58,7 +58,7 @@ def test_host_only_calls(lib):
     d = ets.default_params()
     assert d["stride"] == 256 and d["rho0"] == 2.0 and d["rho1"] == 2.25
     assert d["long_len"] == 786432 and d["long_stride"] == 512
-    assert d["long_rho0"] == 2.5 and d["long_rho1"] == 2.75
+    assert d["long_rho0"] == 2.75 and d["long_rho1"] == 3.0
     assert d["sample_min_len"] == 12288 and d["direct_max"] == 16384
     old = ets.set_params(stride=64)
     try:
@@ -68,7 +68,7 @@ def test_host_only_calls(lib):
     assert ets.get_params()["stride"] == old["stride"]
     for bad in ({"stride": 0}, {"rho0": 0.5}, {"rho1": 1.0}, {"force_kind": 9},
                 {"sample_min_len": -1}, {"long_stride": 0}, {"long_len": -1},
-                {"long_rho0": 0.5}, {"long_rho1": 2.25}):
+                {"long_rho0": 0.5}, {"long_rho1": 2.5}):
         with pytest.raises(ets.TopKError):
             ets.set_params(**bad)
     assert ets.get_params() == old
