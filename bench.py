@@ -284,7 +284,7 @@ def kernel_fingerprint(params, kind, grid):
     sources, the sampling parameters in effect and the launch shape."""
     import hashlib
     h = hashlib.sha256()
-    for name in ("topk_device.cuh", "topk_kernels.cu", "topk_launch.h"):
+    for name in ("score_elem.cuh", "topk_device.cuh", "topk_kernels.cu", "topk_launch.h"):
         with open(os.path.join(ROOT, "exact_top_sparse_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     launch = {"sampling": {k: params[k] for k in SAMPLING_KNOBS}, "kind": kind, "grid": grid}

@@ -70,7 +70,8 @@ EXPORTS = ("topk_ragged", "topk_ragged_diag", "topk_ragged_ws", "topk_workspace_
            "topk_status_string", "topk_version", "topk_ragged_noalloc",
            "topk_index_scores", "topk_index_topk", "topk_index_read_status",
            "topk_ragged_bf16", "topk_ragged_bf16_diag", "topk_sort_rows", "topk_sort_rows_bf16",
-           "topk_check_wait_timeout", "topk_ragged_k", "topk_ragged_k_bf16", "topk_ragged_k_diag")
+           "topk_check_wait_timeout", "topk_ragged_k", "topk_ragged_k_bf16", "topk_ragged_k_diag",
+           "topk_ragged_e4m3", "topk_ragged_e4m3_diag", "topk_ragged_k_e4m3", "topk_sort_rows_e4m3")
 NOALLOC_MAX_ROWS = 64
 
 _lib = None
@@ -96,6 +97,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.topk_ragged_k.argtypes = [vp, vp, vp, i64, i64, i32, vp, vp]
     lib.topk_ragged_k_bf16.argtypes = [vp, vp, vp, i64, i64, i32, vp, vp]
     lib.topk_ragged_k_diag.argtypes = [vp, vp, vp, i64, i64, i32, vp, vp, vp]
+    lib.topk_ragged_e4m3.argtypes = [vp, vp, i64, i64, i32, vp, vp]
+    lib.topk_ragged_e4m3_diag.argtypes = [vp, vp, i64, i64, i32, vp, vp, vp]
+    lib.topk_ragged_k_e4m3.argtypes = [vp, vp, vp, i64, i64, i32, vp, vp]
+    lib.topk_sort_rows_e4m3.argtypes = [vp, i64, i64, i32, vp, vp]
     lib.topk_sort_rows.argtypes = [vp, i64, i64, i32, vp, vp]
     lib.topk_check_wait_timeout.argtypes = [ctypes.c_uint64, vp]
     lib.topk_check_wait_timeout.restype = ctypes.c_int
@@ -122,7 +127,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                  "topk_ragged_noalloc", "topk_index_scores", "topk_index_topk",
                  "topk_ragged_bf16", "topk_ragged_bf16_diag", "topk_sort_rows",
                  "topk_sort_rows_bf16", "topk_ragged_k", "topk_ragged_k_bf16",
-                 "topk_ragged_k_diag", "topk_index_read_status",
+                 "topk_ragged_k_diag", "topk_ragged_e4m3", "topk_ragged_e4m3_diag",
+                 "topk_ragged_k_e4m3", "topk_sort_rows_e4m3", "topk_index_read_status",
                  "topk_plan", "topk_set_params", "topk_get_params", "topk_read_status",
                  "topk_version"):
         getattr(lib, name).restype = ctypes.c_int
@@ -140,10 +146,25 @@ def _stream_handle(device, stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+E4M3 = getattr(torch, "float8_e4m3fn", None)
+NARROW = tuple(t for t in (torch.bfloat16, E4M3) if t is not None)
+
+
+def _pick(lib, scores, name):
+    """The entry point for the scores' element type: name, name_bf16 / _e4m3
+    (a _diag suffix goes after the type, as in the C header)."""
+    base, diag = (name[:-5], "_diag") if name.endswith("_diag") else (name, "")
+    if scores.dtype == torch.bfloat16:
+        return getattr(lib, base + "_bf16" + diag)
+    if E4M3 is not None and scores.dtype == E4M3:
+        return getattr(lib, base + "_e4m3" + diag)
+    return getattr(lib, name)
+
+
 def _inputs(scores, row_lens, K, out, allow_bf16=False):
     if not (isinstance(scores, torch.Tensor) and scores.is_cuda):
         raise TypeError("scores must be a CUDA tensor")
-    ok_types = (torch.float32, torch.bfloat16) if allow_bf16 else (torch.float32,)
+    ok_types = (torch.float32,) + NARROW if allow_bf16 else (torch.float32,)
     if scores.dtype not in ok_types or scores.dim() != 2:
         raise TypeError("scores must be a 2-D %s tensor [M, N_alloc]"
                         % " or ".join(str(t).replace("torch.", "") for t in ok_types))
@@ -165,10 +186,11 @@ def _inputs(scores, row_lens, K, out, allow_bf16=False):
 def topk_ragged(scores: torch.Tensor, row_lens: torch.Tensor, K: int = 2048,
                 out: torch.Tensor = None, stream=None) -> torch.Tensor:
     """Exact Top-K of every row's valid prefix; [M, K] int32, unsorted, -1 padded.
-    Scores are float32, or bfloat16 (selected as their exact float32 values)."""
+    Scores are float32, bfloat16 or float8_e4m3fn (the narrow types selected as
+    their exact float32 values)."""
     lib = load_library()
     M, N, out = _inputs(scores, row_lens, K, out, allow_bf16=True)
-    fn = lib.topk_ragged_bf16 if scores.dtype == torch.bfloat16 else lib.topk_ragged
+    fn = _pick(lib, scores, "topk_ragged")
     with torch.cuda.device(scores.device):
         rc = fn(scores.data_ptr(), row_lens.data_ptr(), M, N, K, out.data_ptr(),
                 _stream_handle(scores.device, stream))
@@ -191,7 +213,7 @@ def topk_ragged_k(scores: torch.Tensor, row_lens: torch.Tensor, row_k: torch.Ten
     lib = load_library()
     M, N, out = _inputs(scores, row_lens, K_max, out, allow_bf16=True)
     row_k = _row_k(row_k, scores)
-    fn = lib.topk_ragged_k_bf16 if scores.dtype == torch.bfloat16 else lib.topk_ragged_k
+    fn = _pick(lib, scores, "topk_ragged_k")
     with torch.cuda.device(scores.device):
         rc = fn(scores.data_ptr(), row_lens.data_ptr(), row_k.data_ptr(), M, N, K_max,
                 out.data_ptr(), _stream_handle(scores.device, stream))
@@ -218,14 +240,15 @@ def topk_sort_rows(scores, out, stream=None):
     scores by index, -1 sentinels last (the selection itself is unordered)."""
     lib = load_library()
     if not (isinstance(scores, torch.Tensor) and scores.is_cuda and scores.dim() == 2
-            and scores.dtype in (torch.float32, torch.bfloat16) and scores.is_contiguous()):
-        raise TypeError("scores must be a contiguous 2-D float32 or bfloat16 CUDA tensor")
+            and scores.dtype in (torch.float32,) + NARROW and scores.is_contiguous()):
+        raise TypeError("scores must be a contiguous 2-D float32, bfloat16 or float8_e4m3fn "
+                        "CUDA tensor")
     if not (isinstance(out, torch.Tensor) and out.device == scores.device
             and out.dtype == torch.int32 and out.dim() == 2 and out.shape[0] == scores.shape[0]
             and out.is_contiguous()):
         raise TypeError("out must be a contiguous int32 [M, K] tensor on the scores' device")
     M, N = scores.shape
-    fn = lib.topk_sort_rows_bf16 if scores.dtype == torch.bfloat16 else lib.topk_sort_rows
+    fn = _pick(lib, scores, "topk_sort_rows")
     with torch.cuda.device(scores.device):
         rc = fn(scores.data_ptr(), M, N, out.shape[1], out.data_ptr(),
                 _stream_handle(scores.device, stream))
@@ -238,7 +261,7 @@ def topk_ragged_diag(scores, row_lens, K: int = 2048, out=None, stream=None):
     lib = load_library()
     M, N, out = _inputs(scores, row_lens, K, out, allow_bf16=True)
     diag = torch.empty(M * DIAG_DTYPE.itemsize, dtype=torch.uint8, device=scores.device)
-    fn = lib.topk_ragged_bf16_diag if scores.dtype == torch.bfloat16 else lib.topk_ragged_diag
+    fn = _pick(lib, scores, "topk_ragged_diag")
     with torch.cuda.device(scores.device):
         rc = fn(scores.data_ptr(), row_lens.data_ptr(), M, N, K, out.data_ptr(), diag.data_ptr(),
                 _stream_handle(scores.device, stream))

@@ -12,6 +12,7 @@
 #include <cstdint>
 
 #include "topk.h"
+#include "score_elem.cuh"
 
 namespace tks {
 
@@ -25,6 +26,9 @@ __device__ __forceinline__ uint32_t key_of(float v) {
 __device__ __forceinline__ float load_score(const float* row, int64_t i) { return row[i]; }
 __device__ __forceinline__ float load_score(const uint16_t* row, int64_t i) {
   return __uint_as_float((uint32_t)row[i] << 16);
+}
+__device__ __forceinline__ float load_score(const uint8_t* row, int64_t i) {
+  return tk::Elem<uint8_t>::widen(row[i]);
 }
 
 template <class E>
@@ -96,6 +100,11 @@ int topk_sort_rows(const float* scores, int64_t M, int64_t N_alloc, int32_t K, i
 }
 
 int topk_sort_rows_bf16(const uint16_t* scores, int64_t M, int64_t N_alloc, int32_t K,
+                        int32_t* out_idx, struct CUstream_st* stream) {
+  return tks::sort_rows(scores, N_alloc, M, K, out_idx, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int topk_sort_rows_e4m3(const uint8_t* scores, int64_t M, int64_t N_alloc, int32_t K,
                         int32_t* out_idx, struct CUstream_st* stream) {
   return tks::sort_rows(scores, N_alloc, M, K, out_idx, reinterpret_cast<cudaStream_t>(stream));
 }

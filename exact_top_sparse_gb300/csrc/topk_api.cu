@@ -19,8 +19,8 @@
 
 namespace {
 
-constexpr int kVersion = 10200;  // 1.2.0: per-row K (1.1.0: bfloat16 rows, ordered output,
-                                 // indexer scores)
+constexpr int kVersion = 10300;  // 1.3.0: FP8 E4M3 rows (1.2.0: per-row K; 1.1.0: bfloat16
+                                 // rows, ordered output, indexer scores)
 constexpr size_t kHdrBytes = 256;
 constexpr int64_t kMinSegment = 32768;  // floats per KV-split segment, at least
 // Planner crossovers, measured on GB300 over 128K-1M columns and M = 64-2048:
@@ -317,6 +317,18 @@ int topk_ragged_bf16_diag(const uint16_t* scores, const int32_t* row_lens, int64
   return run(scores, row_lens, M, N_alloc, K, out_idx, diag, nullptr, 0, false, stream, 2);
 }
 
+int topk_ragged_e4m3(const uint8_t* scores, const int32_t* row_lens, int64_t M, int64_t N_alloc,
+                     int32_t K, int32_t* out_idx, struct CUstream_st* stream) {
+  return run(scores, row_lens, M, N_alloc, K, out_idx, nullptr, nullptr, 0, false, stream, 1);
+}
+
+int topk_ragged_e4m3_diag(const uint8_t* scores, const int32_t* row_lens, int64_t M,
+                          int64_t N_alloc, int32_t K, int32_t* out_idx, topk_row_diag* diag,
+                          struct CUstream_st* stream) {
+  if (M > 0 && !diag) return TOPK_ERR_ARG;
+  return run(scores, row_lens, M, N_alloc, K, out_idx, diag, nullptr, 0, false, stream, 1);
+}
+
 int topk_ragged_ws(const float* scores, const int32_t* row_lens, int64_t M, int64_t N_alloc,
                    int32_t K, int32_t* out_idx, void* workspace, size_t workspace_bytes,
                    struct CUstream_st* stream) {
@@ -336,6 +348,14 @@ int topk_ragged_k_bf16(const uint16_t* scores, const int32_t* row_lens, const in
                        struct CUstream_st* stream) {
   if (M > 0 && !row_k) return TOPK_ERR_ARG;
   return run(scores, row_lens, M, N_alloc, K_max, out_idx, nullptr, nullptr, 0, false, stream, 2,
+             row_k);
+}
+
+int topk_ragged_k_e4m3(const uint8_t* scores, const int32_t* row_lens, const int32_t* row_k,
+                       int64_t M, int64_t N_alloc, int32_t K_max, int32_t* out_idx,
+                       struct CUstream_st* stream) {
+  if (M > 0 && !row_k) return TOPK_ERR_ARG;
+  return run(scores, row_lens, M, N_alloc, K_max, out_idx, nullptr, nullptr, 0, false, stream, 1,
              row_k);
 }
 

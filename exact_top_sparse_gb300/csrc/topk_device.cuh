@@ -28,12 +28,13 @@
 // nested band are collected in the same pass (into shared memory, then a
 // global spill area), so the tau1 path needs no re-read; radix rounds use
 // data-relative 11-bit digits so the first histogram is not degenerate on
-// concentrated scores; rows may be FP32 or bfloat16 (widened exactly).
+// concentrated scores; rows may be FP32, bfloat16 or FP8 E4M3 (widened exactly).
 #pragma once
 
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "score_elem.cuh"
 #include "topk_launch.h"
 
 namespace tk {
@@ -189,51 +190,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
       : "memory");
 }
-
-// A single score, cached in L2 only (one 32-byte sector, no L1 line fill),
-// with the given L2 eviction policy.
-__device__ __forceinline__ float ld_keep(const float* p, uint64_t policy) {
-  float v;
-  asm volatile("ld.global.cg.L2::cache_hint.f32 %0, [%1], %2;" : "=f"(v) : "l"(p), "l"(policy));
-  return v;
-}
-
-// Score element types: FP32, or bfloat16 given as raw 16-bit patterns.  A
-// bfloat16 is the upper half of a binary32, so widening it is exact and every
-// comparison, key and threshold below works on the widened FP32 value.
-// kPer16: elements per 16 bytes (one vector load of the ring).
-template <class E>
-struct Elem;
-template <>
-struct Elem<float> {
-  static constexpr int kSize = 4, kPer16 = 4;
-  __device__ static __forceinline__ float load(const float* p) { return *p; }
-  __device__ static __forceinline__ float load_keep(const float* p, uint64_t pol) {
-    return ld_keep(p, pol);
-  }
-  // the elements of one 16-byte unit as groups of four widened values
-  __device__ static __forceinline__ void groups(const uint4& u, float4* g) {
-    g[0] = make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
-                       __uint_as_float(u.w));
-  }
-};
-template <>
-struct Elem<uint16_t> {
-  static constexpr int kSize = 2, kPer16 = 8;
-  __device__ static __forceinline__ float widen(uint32_t b) { return __uint_as_float(b << 16); }
-  __device__ static __forceinline__ float load(const uint16_t* p) { return widen(*p); }
-  __device__ static __forceinline__ float load_keep(const uint16_t* p, uint64_t pol) {
-    uint16_t v;
-    asm volatile("ld.global.cg.L2::cache_hint.u16 %0, [%1], %2;" : "=h"(v) : "l"(p), "l"(pol));
-    return widen(v);
-  }
-  __device__ static __forceinline__ void groups(const uint4& u, float4* g) {
-    g[0] = make_float4(widen(u.x & 0xFFFFu), widen(u.x >> 16), widen(u.y & 0xFFFFu),
-                       widen(u.y >> 16));
-    g[1] = make_float4(widen(u.z & 0xFFFFu), widen(u.z >> 16), widen(u.w & 0xFFFFu),
-                       widen(u.w >> 16));
-  }
-};
 
 // ------------------------------------------------------------ warp / block
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
@@ -582,10 +538,11 @@ __device__ __forceinline__ void ring_pass(Ring& R, const E* __restrict__ row, in
         const int j = (int)ct + it * CONSUMERS;
         const bool ok = j < nu;
         const uint4 u = ok ? sm[j] : make_uint4(0u, 0u, 0u, 0u);
-        float4 g[NG];
-        Elem<E>::groups(u, g);
-#pragma unroll
-        for (int k = 0; k < NG; ++k) f.quad(off + (int64_t)P16 * j + 4 * k, g[k], ok ? 0xfu : 0u);
+        // one group of four widened scores at a time (the functor's work is
+        // inlined per group; more would only add live registers)
+#pragma unroll 1
+        for (int k = 0; k < NG; ++k)
+          f.quad(off + (int64_t)P16 * j + 4 * k, Elem<E>::group(u, k), ok ? 0xfu : 0u);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&R.empty[s]);
@@ -703,11 +660,19 @@ __device__ __forceinline__ int32_t max_bf16_pattern(const uint4& u) {
   return max((int32_t)(int16_t)(c & 0xFFFFu), (int32_t)(int16_t)(c >> 16));
 }
 
+// The largest of the sixteen E4M3 bytes of a 16-byte unit, each read as a
+// signed 8-bit integer (for values above +0 this is their order).
+__device__ __forceinline__ int32_t max_e4m3_pattern(const uint4& u) {
+  const uint32_t c = __vmaxs4(__vmaxs4(u.x, u.y), __vmaxs4(u.z, u.w));
+  return max(max((int32_t)(int8_t)(c & 0xFFu), (int32_t)(int8_t)((c >> 8) & 0xFFu)),
+             max((int32_t)(int8_t)((c >> 16) & 0xFFu), (int32_t)(int8_t)(c >> 24)));
+}
+
 // The certify+collect pass over [start, end) of `row`, whose first `primed`
 // chunks ring_prime already started.  Same ring protocol as ring_pass, with
 // the consumer side shaped for the common case: a full chunk is exactly two
-// 16-byte units per consumer thread, all of their scores (8 FP32 or 16
-// bfloat16) are tested with one integer max, the stage is handed back as
+// 16-byte units per consumer thread, all of their scores (8 FP32, 16
+// bfloat16 or 32 E4M3) are tested with one integer max, the stage is handed back as
 // soon as the loads have fed that test, and only lanes holding an admitted
 // score (rare) append.
 template <class E, bool POS>
@@ -736,10 +701,13 @@ __device__ __forceinline__ void scan_pass(Ring& R, const E* __restrict__ row, in
     }
     const uint32_t ct = tid - 32;
     // the admission operand's threshold (for bfloat16 with tau1 > +0: the
-    // upper half of tau1's FP32 bits, as a signed 16-bit value)
-    const int32_t thr = (NG == 2 && POS) ? (int32_t)(int16_t)(f.t1 >> 16)
-                        : POS          ? (int32_t)f.t1
-                                       : (int32_t)(f.t1 ^ 0x80000000u);
+    // upper half of tau1's FP32 bits, as a signed 16-bit value; for E4M3:
+    // tau1's byte pattern)
+    int32_t thr;
+    if constexpr (NG == 2 && POS) thr = (int32_t)(int16_t)(f.t1 >> 16);
+    else if constexpr (NG == 4 && POS)
+      thr = Elem<uint8_t>::pattern_of_positive(__uint_as_float(f.t1));
+    else thr = POS ? (int32_t)f.t1 : (int32_t)(f.t1 ^ 0x80000000u);
     for (uint32_t c = 0; c < nchunks; ++c) {
       const uint32_t q = R.seq + c, s = q % STAGES, use = q / STAGES;
       if (!mbar_wait(&R.full[s], use & 1u)) lflags |= F_TIMEOUT;
@@ -757,16 +725,17 @@ __device__ __forceinline__ void scan_pass(Ring& R, const E* __restrict__ row, in
         // integers in the order of the values; two per instruction
         m0 = max_bf16_pattern(u0);
         m1 = max_bf16_pattern(u1);
+      } else if constexpr (NG == 4 && POS) {
+        // E4M3 with tau1 > +0: the raw bytes, four per instruction
+        m0 = max_e4m3_pattern(u0);
+        m1 = max_e4m3_pattern(u1);
       } else {
-        float4 g0[NG], g1[NG];
-        Elem<E>::groups(u0, g0);
-        Elem<E>::groups(u1, g1);
-        m0 = max_operand<POS>(g0[0]);
-        m1 = max_operand<POS>(g1[0]);
+        m0 = max_operand<POS>(Elem<E>::group(u0, 0));
+        m1 = max_operand<POS>(Elem<E>::group(u1, 0));
 #pragma unroll
         for (int k = 1; k < NG; ++k) {
-          m0 = max(m0, max_operand<POS>(g0[k]));
-          m1 = max(m1, max_operand<POS>(g1[k]));
+          m0 = max(m0, max_operand<POS>(Elem<E>::group(u0, k)));
+          m1 = max(m1, max_operand<POS>(Elem<E>::group(u1, k)));
         }
       }
       if (!ok0) m0 = INT32_MIN;
@@ -776,16 +745,25 @@ __device__ __forceinline__ void scan_pass(Ring& R, const E* __restrict__ row, in
       if (lane == 0) mbar_arrive(&R.empty[s]);
       const bool h0 = ok0 && m0 >= thr, h1 = ok1 && m1 >= thr;
       if (h0 || h1) {
-        float4 g0[NG], g1[NG];
-        Elem<E>::groups(u0, g0);
-        Elem<E>::groups(u1, g1);
-        if (NG == 1) {
-          f.lane_put2(off + (int64_t)P16 * j0, g0[0], h0, off + (int64_t)P16 * j1, g1[0], h1);
+        if constexpr (NG == 1) {
+          f.lane_put2(off + (int64_t)P16 * j0, Elem<E>::group(u0, 0), h0, off + (int64_t)P16 * j1,
+                      Elem<E>::group(u1, 0), h1);
+        } else if constexpr (NG == 2) {
+          if (h0) f.lane_put2(off + (int64_t)P16 * j0, Elem<E>::group(u0, 0), true,
+                              off + (int64_t)P16 * j0 + 4, Elem<E>::group(u0, 1), true);
+          if (h1) f.lane_put2(off + (int64_t)P16 * j1, Elem<E>::group(u1, 0), true,
+                              off + (int64_t)P16 * j1 + 4, Elem<E>::group(u1, 1), true);
         } else {
-          if (h0) f.lane_put2(off + (int64_t)P16 * j0, g0[0], true, off + (int64_t)P16 * j0 + 4,
-                              g0[NG - 1], true);
-          if (h1) f.lane_put2(off + (int64_t)P16 * j1, g1[0], true, off + (int64_t)P16 * j1 + 4,
-                              g1[NG - 1], true);
+          // one unit and a pair of groups (eight scores) at a time: a single
+          // inlined append keeps few values live
+#pragma unroll 1
+          for (int t = 0; t < NG; ++t) {
+            const int v = t / (NG / 2), k = 2 * (t % (NG / 2));
+            if (!(v ? h1 : h0)) continue;
+            const uint4& u = v ? u1 : u0;
+            const int64_t i0 = off + (int64_t)P16 * (v ? j1 : j0) + 4 * k;
+            f.lane_put2(i0, Elem<E>::group(u, k), true, i0 + 4, Elem<E>::group(u, k + 1), true);
+          }
         }
       }
     }

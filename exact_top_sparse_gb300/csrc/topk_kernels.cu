@@ -682,16 +682,22 @@ cudaError_t prepare_device() {
   if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
       cudaSuccess)
     return e;
-  const void* row_kernels[] = {(const void*)k_persistent<float>, (const void*)k_persistent<uint16_t>,
-                               (const void*)k_kv_segment<float>, (const void*)k_kv_segment<uint16_t>};
+  const void* row_kernels[] = {
+      (const void*)k_persistent<float>, (const void*)k_persistent<uint16_t>,
+      (const void*)k_persistent<uint8_t>, (const void*)k_kv_segment<float>,
+      (const void*)k_kv_segment<uint16_t>, (const void*)k_kv_segment<uint8_t>};
   for (const void* fn : row_kernels)
     if ((e = set_smem(fn, persistent_smem_bytes())) != cudaSuccess) return e;
-  if ((e = set_smem((const void*)k_kv_prepare<float>, kv_prepare_smem_bytes())) != cudaSuccess)
-    return e;
-  if ((e = set_smem((const void*)k_kv_prepare<uint16_t>, kv_prepare_smem_bytes())) != cudaSuccess)
-    return e;
-  if ((e = set_smem((const void*)k_direct<float>, (size_t)optin)) != cudaSuccess) return e;
-  return set_smem((const void*)k_direct<uint16_t>, (size_t)optin);
+  const void* prep_kernels[] = {(const void*)k_kv_prepare<float>,
+                                (const void*)k_kv_prepare<uint16_t>,
+                                (const void*)k_kv_prepare<uint8_t>};
+  for (const void* fn : prep_kernels)
+    if ((e = set_smem(fn, kv_prepare_smem_bytes())) != cudaSuccess) return e;
+  const void* direct_kernels[] = {(const void*)k_direct<float>, (const void*)k_direct<uint16_t>,
+                                  (const void*)k_direct<uint8_t>};
+  for (const void* fn : direct_kernels)
+    if ((e = set_smem(fn, (size_t)optin)) != cudaSuccess) return e;
+  return cudaSuccess;
 }
 
 cudaError_t persistent_occupancy(int* blocks_per_sm) {
@@ -734,6 +740,8 @@ cudaError_t launch_direct(const void* scores, const int32_t* row_lens, int32_t* 
                           RowDiag* diag, const Params& P, cudaStream_t st) {
   if (P.elem_bytes == 2)
     return launch_direct_t(static_cast<const uint16_t*>(scores), row_lens, out, diag, P, st);
+  if (P.elem_bytes == 1)
+    return launch_direct_t(static_cast<const uint8_t*>(scores), row_lens, out, diag, P, st);
   return launch_direct_t(static_cast<const float*>(scores), row_lens, out, diag, P, st);
 }
 
@@ -743,6 +751,9 @@ cudaError_t launch_persistent(const void* scores, const int32_t* row_lens, int32
   if (P.elem_bytes == 2)
     return launch_persistent_t(static_cast<const uint16_t*>(scores), row_lens, out, diag, hdr,
                                spill, grid, P, st);
+  if (P.elem_bytes == 1)
+    return launch_persistent_t(static_cast<const uint8_t*>(scores), row_lens, out, diag, hdr,
+                               spill, grid, P, st);
   return launch_persistent_t(static_cast<const float*>(scores), row_lens, out, diag, hdr, spill,
                              grid, P, st);
 }
@@ -751,6 +762,9 @@ cudaError_t launch_kvsplit(const void* scores, const int32_t* row_lens, int32_t*
                            RowDiag* diag, uint8_t* ws_rows, const Params& P, cudaStream_t st) {
   if (P.elem_bytes == 2)
     return launch_kvsplit_t(static_cast<const uint16_t*>(scores), row_lens, out, diag, ws_rows, P,
+                            st);
+  if (P.elem_bytes == 1)
+    return launch_kvsplit_t(static_cast<const uint8_t*>(scores), row_lens, out, diag, ws_rows, P,
                             st);
   return launch_kvsplit_t(static_cast<const float*>(scores), row_lens, out, diag, ws_rows, P, st);
 }

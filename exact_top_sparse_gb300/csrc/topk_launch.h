@@ -18,7 +18,7 @@ struct Params {
   uint32_t target1;  // ceil(rho1 * K)
   int64_t sample_min_len;
   int32_t segments;  // KV-split segments per row
-  int32_t elem_bytes;  // 4: FP32 scores, 2: bfloat16 scores
+  int32_t elem_bytes;  // 4: FP32 scores, 2: bfloat16 scores, 1: FP8 E4M3 scores
   int64_t long_len;  // rows this long or longer sample with the long_* values (0: none)
   int32_t long_stride;
   uint32_t long_target0;

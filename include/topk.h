@@ -164,6 +164,20 @@ int topk_ragged_bf16_diag(const uint16_t* scores, const int32_t* row_lens, int64
                           int64_t N_alloc, int32_t K, int32_t* out_idx, topk_row_diag* diag,
                           struct CUstream_st* stream);
 
+/* Same for FP8 E4M3 score rows (the OCP 8-bit format without infinities:
+ * sign, 4 exponent bits with bias 7, 3 mantissa bits), given as raw bytes
+ * [M][N_alloc] with no alignment requirement.  Every E4M3 value widens
+ * exactly to FP32 and the selection is the exact Top-K of the widened values,
+ * reading a quarter of the FP32 bytes.  With 8 values per octave, rows hold
+ * long runs of equal scores; ties at the boundary are broken freely as the
+ * contract allows.  The NaN pattern S.1111.111 is not a supported score.  An
+ * extension beyond the pages, as the bfloat16 form. */
+int topk_ragged_e4m3(const uint8_t* scores, const int32_t* row_lens, int64_t M, int64_t N_alloc,
+                     int32_t K, int32_t* out_idx, struct CUstream_st* stream);
+int topk_ragged_e4m3_diag(const uint8_t* scores, const int32_t* row_lens, int64_t M,
+                          int64_t N_alloc, int32_t K, int32_t* out_idx, topk_row_diag* diag,
+                          struct CUstream_st* stream);
+
 /* Device workspace bytes a call with these sizes needs under the current
  * parameters (0 is a valid answer only for M == 0). */
 size_t topk_workspace_bytes(int64_t M, int64_t N_alloc, int32_t K);
@@ -189,10 +203,14 @@ int topk_ragged_ws(const float* scores, const int32_t* row_lens, int64_t M, int6
  *   K_max    1 <= K_max <= TOPK_K_MAX: the output row stride
  *   out_idx  device, [M][K_max] int32, written completely
  * Other arguments, workspace and errors as topk_ragged() (and
- * topk_ragged_bf16() / topk_ragged_diag() for the _bf16 / _diag forms). */
+ * topk_ragged_bf16(), topk_ragged_e4m3() and topk_ragged_diag() for the _bf16,
+ * _e4m3 and _diag forms). */
 int topk_ragged_k(const float* scores, const int32_t* row_lens, const int32_t* row_k, int64_t M,
                   int64_t N_alloc, int32_t K_max, int32_t* out_idx, struct CUstream_st* stream);
 int topk_ragged_k_bf16(const uint16_t* scores, const int32_t* row_lens, const int32_t* row_k,
+                       int64_t M, int64_t N_alloc, int32_t K_max, int32_t* out_idx,
+                       struct CUstream_st* stream);
+int topk_ragged_k_e4m3(const uint8_t* scores, const int32_t* row_lens, const int32_t* row_k,
                        int64_t M, int64_t N_alloc, int32_t K_max, int32_t* out_idx,
                        struct CUstream_st* stream);
 int topk_ragged_k_diag(const float* scores, const int32_t* row_lens, const int32_t* row_k,
@@ -268,11 +286,14 @@ int topk_version(void);
  * of the M rows of out_idx [M][K] (device, as written by topk_ragged) in
  * place by score, largest first, equal scores by index, -1 sentinels last.
  * `scores` are the rows the indices refer to (device, row stride N_alloc);
- * topk_sort_rows_bf16 takes bfloat16 patterns.  One launch on `stream`, no
+ * topk_sort_rows_bf16 takes bfloat16 patterns, topk_sort_rows_e4m3 FP8 E4M3
+ * bytes.  One launch on `stream`, no
  * allocation.  Errors as topk_ragged. */
 int topk_sort_rows(const float* scores, int64_t M, int64_t N_alloc, int32_t K, int32_t* out_idx,
                    struct CUstream_st* stream);
 int topk_sort_rows_bf16(const uint16_t* scores, int64_t M, int64_t N_alloc, int32_t K,
+                        int32_t* out_idx, struct CUstream_st* stream);
+int topk_sort_rows_e4m3(const uint8_t* scores, int64_t M, int64_t N_alloc, int32_t K,
                         int32_t* out_idx, struct CUstream_st* stream);
 
 /* ---------------------------------------------------------------------------

@@ -52,7 +52,7 @@ def test_library_is_built_for_sm103a(lib):
 
 def test_host_only_calls(lib):
     import exact_top_sparse_gb300 as ets
-    assert ets.version() == 10200
+    assert ets.version() == 10300
     assert lib.topk_status_string(0) == b"ok"
     assert lib.topk_status_string(-5).startswith(b"workspace allocation")
     d = ets.default_params()
