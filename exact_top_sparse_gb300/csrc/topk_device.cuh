@@ -54,6 +54,7 @@ constexpr int CHUNK_FLOATS = CHUNK_BYTES / 4;
 constexpr int CAP = 6144;                   // on-chip candidate capacity (entries of 8 B)
 constexpr int SPILL = 10240;                // further candidates kept in global memory
 constexpr int CAP_ALL = CAP + SPILL;        // candidates one full-row pass can keep
+constexpr int TIE_CAP = 4096;               // indices of scores equal to tau1 kept (>= any K)
 constexpr int SMALL = 32;                   // frontier size finished by one warp
 constexpr int SAMPLE_SMEM = 2 * CAP;        // sample keys kept on chip (they alias the candidates)
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // bounded waits give up after 2 s
@@ -223,6 +224,7 @@ struct __align__(16) Shared {
   uint32_t key0, key1;
   uint32_t last;
   uint32_t next, next_ok;        // a row claimed ahead of time (persistent kernel)
+  uint32_t neq;                  // scores equal to tau1 (counts past the tie list)
 };
 
 // Exclusive prefix sum over all THREADS threads (every thread must call).
@@ -562,37 +564,53 @@ __device__ __forceinline__ uint2 cand_at(const uint2* cand, const uint2* spill, 
 // ------------------------------------------------- certify + collect (stage 2)
 // Admission: key(v) >= key(tau1).  When tau1 > +0 the signed comparison of
 // the raw bits gives the same answer in one instruction (POS = true).
-// During the pass an admitted score is only appended, as (index, key), to the
-// shared candidate array; C(tau0) and the seeded histogram are taken from the
-// array once the pass is over (tally_candidates), which keeps the histogram
-// atomics out of the streaming loop.
-template <bool POS>
+// An admitted score above tau1 is appended, as (index, key), to the shared
+// candidate array; C(tau0) and the seeded histogram are taken from the array
+// once the pass is over (tally_candidates), which keeps the histogram atomics
+// out of the streaming loop.  A score equal to tau1 is only counted, and its
+// index kept while the tie list has room: when the K-th largest score is
+// tau1 the answer takes every score above it and any of the ties (the
+// contract lets boundary ties go either way), so the first K ties suffice.
+// E4M3 rows (8 values per octave) put long runs of ties at tau1, which would
+// otherwise overflow the candidate buffers; for FP32 and bfloat16 rows
+// (TIES = false) ties are ordinary candidates, which keeps their scan loop
+// leaner (measured 13 % and 5 % faster), and a rare long tie run takes the
+// overflow path.
+template <bool POS, bool TIES>
 struct ScanCollect {
   uint32_t t1;  // POS: bits of tau1; otherwise key(tau1)
   uint2* cand;  // CAP entries in shared memory
   uint2* spill; // entries CAP.. in global memory (nullptr: none)
   uint32_t cap; // CAP_ALL with a spill area, else CAP
-  uint32_t* ncand;
+  uint32_t* ncand;    // scores above tau1 (counts past the capacity)
+  uint32_t* ties;     // indices of scores equal to tau1, tie_cap of them
+  uint32_t tie_cap;
+  uint32_t* neq;      // scores equal to tau1 (counts past tie_cap)
 
   __device__ __forceinline__ bool admit(float x) const {
     if (POS) return (int32_t)__float_as_uint(x) >= (int32_t)t1;
     return fkey(x) >= t1;
   }
+  __device__ __forceinline__ bool tie(float x) const {
+    if (POS) return __float_as_uint(x) == t1;
+    return fkey(x) == t1;
+  }
   __device__ __forceinline__ uint32_t admit_mask(const float4& v) const {
     return (admit(v.x) ? 1u : 0u) | (admit(v.y) ? 2u : 0u) | (admit(v.z) ? 4u : 0u) |
            (admit(v.w) ? 8u : 0u);
   }
-  __device__ __forceinline__ void put(uint32_t& pos, int64_t i0, const float4& v,
-                                      uint32_t m) const {
-    const float vals[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      if (m & (1u << e)) {
-        const uint2 ent = make_uint2((uint32_t)(i0 + e), fkey(vals[e]));
-        if (pos < (uint32_t)CAP) cand[pos] = ent;
-        else if (pos < cap) spill[pos - (uint32_t)CAP] = ent;
-        ++pos;
-      }
+  __device__ __forceinline__ uint32_t tie_mask(const float4& v) const {
+    return (tie(v.x) ? 1u : 0u) | (tie(v.y) ? 2u : 0u) | (tie(v.z) ? 4u : 0u) |
+           (tie(v.w) ? 8u : 0u);
+  }
+  // Counts the ties of mask q (element e of group a for bits 0-3, of group b
+  // for bits 4-7) and keeps their indices while the tie list has room.
+  __device__ __forceinline__ void put_ties(uint32_t q, int64_t ia, int64_t ib) const {
+    uint32_t t = atomicAdd(neq, (uint32_t)__popc(q));
+    while (q && t < tie_cap) {
+      const uint32_t e = (uint32_t)__ffs(q) - 1u;
+      q &= q - 1u;
+      ties[t++] = (uint32_t)((e < 4u ? ia : ib) + (e & 3u));
     }
   }
   // Appends the admitted scores of two groups of four (elements ia.. of va
@@ -600,7 +618,17 @@ struct ScanCollect {
   // the admitted elements.
   __device__ __forceinline__ void lane_put2(int64_t ia, const float4& va, bool ha, int64_t ib,
                                             const float4& vb, bool hb) const {
-    uint32_t m = (ha ? admit_mask(va) : 0u) | ((hb ? admit_mask(vb) : 0u) << 4);
+    const uint32_t m = (ha ? admit_mask(va) : 0u) | ((hb ? admit_mask(vb) : 0u) << 4);
+    if (!m) return;
+    const uint32_t q =
+        TIES ? ((ha ? tie_mask(va) : 0u) | ((hb ? tie_mask(vb) : 0u) << 4)) : 0u;
+    put_masked(m & ~q, q, ia, va, ib, vb);
+  }
+  // Candidates of mask m and ties of mask q (bits 0-3: elements ia.. of va,
+  // bits 4-7: elements ib.. of vb).
+  __device__ __forceinline__ void put_masked(uint32_t m, uint32_t q, int64_t ia, const float4& va,
+                                             int64_t ib, const float4& vb) const {
+    if (TIES && q) put_ties(q, ia, ib);
     if (!m) return;
     uint32_t pos = atomicAdd(ncand, (uint32_t)__popc(m));
     do {
@@ -616,14 +644,12 @@ struct ScanCollect {
     } while (m);
   }
   // Appends the admitted scores among the elements of v selected by vm
-  // (element i0 + e is lane e): one shared-memory atomic reserves this lane's
-  // slots.
+  // (element i0 + e is lane e).
   __device__ __forceinline__ void lane_put(int64_t i0, const float4& v, uint32_t vm) const {
     const uint32_t m = admit_mask(v) & vm;
-    if (m) {
-      uint32_t pos = atomicAdd(ncand, (uint32_t)__popc(m));
-      put(pos, i0, v, m);
-    }
+    if (!m) return;
+    const uint32_t q = TIES ? (tie_mask(v) & vm) : 0u;
+    put_masked(m & ~q, q, i0, v, i0, v);
   }
 };
 
@@ -675,10 +701,10 @@ __device__ __forceinline__ int32_t max_e4m3_pattern(const uint4& u) {
 // bfloat16 or 32 E4M3) are tested with one integer max, the stage is handed back as
 // soon as the loads have fed that test, and only lanes holding an admitted
 // score (rare) append.
-template <class E, bool POS>
+template <class E, bool POS, bool TIES>
 __device__ __forceinline__ void scan_pass(Ring& R, const E* __restrict__ row, int64_t start,
-                                          int64_t end, ScanCollect<POS>& f, uint32_t& lflags,
-                                          uint32_t primed) {
+                                          int64_t end, ScanCollect<POS, TIES>& f,
+                                          uint32_t& lflags, uint32_t primed) {
   static_assert(CHUNK_BYTES == 32 * CONSUMERS, "a full chunk is two 16-byte units per consumer");
   constexpr int P16 = Elem<E>::kPer16, NG = P16 / 4;
   constexpr int64_t CE = CHUNK_BYTES / Elem<E>::kSize;

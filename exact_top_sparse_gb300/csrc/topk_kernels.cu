@@ -78,11 +78,16 @@ struct KvHdr {
   uint32_t key0, key1, kmin, kmax;
   uint32_t c0, ncand, ticket, ovf, flags;
   float tau0, tau1;
-  int32_t k;  // the row's own K
+  int32_t k;     // the row's own K
+  uint32_t neq;  // scores equal to tau1 over all segments
 };
 constexpr size_t KV_HIST_OFF = 256;
 constexpr size_t KV_CAND_OFF = KV_HIST_OFF + (size_t)NB * sizeof(uint32_t);
-constexpr size_t KV_ROW_BYTES = align_up(KV_CAND_OFF + (size_t)CAP_ALL * sizeof(uint2), 256);
+constexpr size_t KV_TIE_OFF = KV_CAND_OFF + (size_t)CAP_ALL * sizeof(uint2);
+constexpr size_t KV_ROW_BYTES = align_up(KV_TIE_OFF + (size_t)TIE_CAP * sizeof(uint32_t), 256);
+// persistent CTA's global area: candidate spill, then the tie list
+constexpr size_t CTA_AREA_BYTES = (size_t)SPILL * sizeof(uint2) + (size_t)TIE_CAP * sizeof(uint32_t);
+static_assert(CTA_AREA_BYTES % 256 == 0, "CTA areas keep 256-byte alignment");
 static_assert(sizeof(KvHdr) <= KV_HIST_OFF, "KV row header too large");
 static_assert(KV_ROW_BYTES == kKvRowBytes, "kKvRowBytes must match the KV-split row layout");
 
@@ -220,23 +225,36 @@ __device__ void exact_row_staged(const E* row, int64_t len, int32_t* out, int32_
   select_staged(buf, len, out, K, c.hist, *c.S, lflags);
 }
 
-// The full-row certify+collect pass over [s0, s1): candidates in c.cand and
-// past CAP in `spill` (nullptr: none), their count in S.ncand (past the
-// capacity when they did not fit), the seeded histogram of the kept ones in
-// c.hist.  Returns C(tau0) over the kept candidates, which is the exact
-// count unless they overflowed.
+// Where the scores equal to tau1 go: their indices (the first `cap` of
+// them, in global memory) and their count (shared or global memory).
+struct TieList {
+  uint32_t* idx;
+  uint32_t cap;
+  uint32_t* n;
+};
+
+// The full-row certify+collect pass over [s0, s1): candidates above tau1 in
+// c.cand and past CAP in `spill` (nullptr: none), their count in S.ncand
+// (past the capacity when they did not fit), the scores equal to tau1 in
+// `tl` (E4M3 rows; for the other types they are candidates and the tie count
+// stays 0), the seeded histogram of the kept candidates in c.hist.  Returns
+// C(tau0) over the kept candidates (without the ties, which the caller adds
+// when tau0 == tau1); exact unless the candidates overflowed.
 template <class E>
 __device__ uint32_t scan_collect(const E* row, int64_t s0, int64_t s1, Ring& R,
-                                 const RowCarve& c, uint2* spill, uint32_t key0, uint32_t key1,
-                                 const Bins& sb, uint32_t& lflags, uint32_t primed) {
+                                 const RowCarve& c, uint2* spill, const TieList& tl,
+                                 uint32_t key0, uint32_t key1, const Bins& sb, uint32_t& lflags,
+                                 uint32_t primed) {
   Shared& S = *c.S;
   const float tau1 = key_to_float(key1);
   const uint32_t cap = spill ? (uint32_t)CAP_ALL : (uint32_t)CAP;
+  constexpr bool TIES = sizeof(E) == 1;  // a tie list for E4M3 rows only
   if (tau1 > 0.0f) {
-    ScanCollect<true> f{__float_as_uint(tau1), c.cand, spill, cap, &S.ncand};
+    ScanCollect<true, TIES> f{__float_as_uint(tau1), c.cand, spill, cap, &S.ncand,
+                              tl.idx, tl.cap, tl.n};
     scan_pass(R, row, s0, s1, f, lflags, primed);
   } else {
-    ScanCollect<false> f{key1, c.cand, spill, cap, &S.ncand};
+    ScanCollect<false, TIES> f{key1, c.cand, spill, cap, &S.ncand, tl.idx, tl.cap, tl.n};
     scan_pass(R, row, s0, s1, f, lflags, primed);
   }
   __syncthreads();
@@ -244,19 +262,52 @@ __device__ uint32_t scan_collect(const E* row, int64_t s0, int64_t s1, Ring& R,
   return block_sum(c0, S);
 }
 
+// Emits out[] entries for indices src(j), j < n (every thread calls).
+template <class G>
+__device__ __forceinline__ void emit_all(const G& src, uint32_t n, int32_t* out, int32_t K,
+                                         Shared& S, uint32_t& lflags) {
+  const uint32_t iters = (n + THREADS - 1) / THREADS;
+  for (uint32_t it = 0; it < iters; ++it) {
+    const uint32_t j = threadIdx.x + it * THREADS;
+    const bool ok = j < n;
+    warp_emit(out, K, ok ? src(j) : 0u, ok, S, lflags);
+  }
+}
+struct CandIdx {  // candidate j's index (j < CAP: shared memory)
+  const uint2* cand;
+  __device__ __forceinline__ uint32_t operator()(uint32_t j) const { return cand[j].x; }
+};
+struct TieIdx {  // tie j's index (global memory written earlier in this kernel)
+  const uint32_t* idx;
+  __device__ __forceinline__ uint32_t operator()(uint32_t j) const { return __ldcg(idx + j); }
+};
+
 // Everything after the full-row pass of a sampled row whose candidates
 // (c.cand, then `spill`), histogram and counts are ready: refine, or re-read
 // on overflow, or recover.  Returns the row path.
+// Cgt: scores above tau1 (the candidates), Ceq: scores equal to tau1 (the
+// first TIE_CAP of them in `ties`); C(tau1) = Cgt + Ceq.
 template <class E>
 __device__ int32_t select_after_scan(const E* row, int64_t len, int32_t* out, int32_t K,
-                                     Ring& R, const RowCarve& c, uint2* spill, const SampleSpec& sp,
-                                     uint32_t& C0, uint32_t C1, bool overflow, uint32_t key0,
+                                     Ring& R, const RowCarve& c, uint2* spill,
+                                     const uint32_t* ties, const SampleSpec& sp, uint32_t& C0,
+                                     uint32_t Cgt, uint32_t Ceq, bool overflow, uint32_t key0,
                                      uint32_t key1, uint32_t kmin, const Bins& sb,
                                      uint32_t& lflags) {
   Shared& S = *c.S;
+  constexpr bool TIES = sizeof(E) == 1;  // only E4M3 rows keep ties apart (Ceq = 0 otherwise)
+  const uint32_t C1 = Cgt + Ceq;
   int32_t path = (C0 >= (uint32_t)K) ? PATH_TAU0 : (C1 >= (uint32_t)K ? PATH_TAU1 : PATH_RECOVERY);
   if (C1 >= (uint32_t)K && !overflow) {
-    refine(CandSrc{c.cand, spill, C1}, sb, (uint32_t)K, c.hist, c.cand, out, K, S, lflags);
+    if (!TIES || Cgt >= (uint32_t)K) {
+      // the K-th largest score is above tau1: the ties cannot be selected
+      refine(CandSrc{c.cand, spill, Cgt}, sb, (uint32_t)K, c.hist, c.cand, out, K, S, lflags);
+    } else {
+      // the K-th largest score is tau1: every score above it, then any
+      // K - Cgt of the ties (Cgt < K <= CAP: every candidate is on chip)
+      emit_all(CandIdx{c.cand}, Cgt, out, K, S, lflags);
+      emit_all(TieIdx{ties}, (uint32_t)K - Cgt, out, K, S, lflags);
+    }
   } else if (C1 >= (uint32_t)K) {
     // More admitted scores than the candidate buffers hold.  The ones past
     // them were not kept, so one pass over the row rebuilds the seeded
@@ -281,12 +332,9 @@ __device__ int32_t select_after_scan(const E* row, int64_t len, int32_t* out, in
       lflags |= F_INTERNAL;
       return path;
     }
-    const uint32_t iters = (C1 + THREADS - 1) / THREADS;
-    for (uint32_t it = 0; it < iters; ++it) {
-      const uint32_t j = threadIdx.x + it * THREADS;
-      const bool ok = j < C1;
-      warp_emit(out, K, ok ? c.cand[j].x : 0u, ok, S, lflags);
-    }
+    // C(tau1) < K <= CAP, TIE_CAP: every admitted score was kept
+    emit_all(CandIdx{c.cand}, Cgt, out, K, S, lflags);
+    if constexpr (TIES) emit_all(TieIdx{ties}, Ceq, out, K, S, lflags);
     __syncthreads();
     // One pass when it suffices: a lower threshold tau2 from the same view
     // (rank of the target 2 * T1) admits the band [tau2, tau1); if the band
@@ -345,7 +393,10 @@ __global__ void __launch_bounds__(THREADS, 2)
                  uint2* __restrict__ spill_all, Params P) {
   extern __shared__ __align__(128) uint8_t smem[];
   const RowCarve c = carve(smem);
-  uint2* spill = spill_all + (size_t)blockIdx.x * SPILL;
+  // this CTA's global area: candidate spill, then the tie list
+  uint8_t* area = reinterpret_cast<uint8_t*>(spill_all) + (size_t)blockIdx.x * CTA_AREA_BYTES;
+  uint2* spill = reinterpret_cast<uint2*>(area);
+  uint32_t* ties = reinterpret_cast<uint32_t*>(area + (size_t)SPILL * sizeof(uint2));
   Shared& S = *c.S;
   if (threadIdx.x == 0) {
     S.flags = 0;
@@ -394,16 +445,21 @@ __global__ void __launch_bounds__(THREADS, 2)
     const Bins sb = scan_bins(key1, kmax);
     __syncthreads();
     clear_hist(c.hist);
-    if (threadIdx.x == 0) S.ncand = 0;
+    if (threadIdx.x == 0) {
+      S.ncand = 0;
+      S.neq = 0;
+    }
     __syncthreads();
-    uint32_t C0 = scan_collect(row, 0, len, R, c, spill, key0, key1, sb, lflags, primed);
+    uint32_t C0 = scan_collect(row, 0, len, R, c, spill, TieList{ties, (uint32_t)TIE_CAP, &S.neq},
+                               key0, key1, sb, lflags, primed);
     // claim the next row now and warm L2 with its sample points while this
     // one is refined
     if (threadIdx.x == 0) {
       S.next = atomicAdd(&hdr[0], 1u);
       S.next_ok = 1u;
     }
-    const uint32_t C1 = S.ncand;
+    const uint32_t Cgt = S.ncand, Ceq = S.neq;
+    if (key0 == key1) C0 += Ceq;
     __syncthreads();
     {
       const int64_t rn = S.next;
@@ -418,11 +474,11 @@ __global__ void __launch_bounds__(THREADS, 2)
     // the row's K and sampling spec again, rather than held in registers
     // over the scan
     const int32_t Kr = row_k_of(P, r, lflags);
-    const int32_t path = select_after_scan(row, len, out, Kr, R, c, spill, sample_spec(P, len, Kr),
-                                           C0, C1,
-                                           C1 > (uint32_t)CAP_ALL, key0, key1, kmin, sb, lflags);
+    const int32_t path =
+        select_after_scan(row, len, out, Kr, R, c, spill, ties, sample_spec(P, len, Kr), C0, Cgt,
+                          Ceq, Cgt > (uint32_t)CAP_ALL, key0, key1, kmin, sb, lflags);
     finish_row(S, out, Kr, K, lflags, diag, r, path, key_to_float(key0), key_to_float(key1), C0,
-               C1);
+               Cgt + Ceq);
   }
   ring_drain(R);
   // The last CTA to leave resets the queue, so the next launch (or graph
@@ -549,6 +605,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     h->kmax = kmax;
     h->c0 = 0;
     h->ncand = 0;
+    h->neq = 0;
     h->ticket = 0;
     h->ovf = 0;
     h->flags = lflags;
@@ -572,6 +629,7 @@ __global__ void __launch_bounds__(THREADS, 2)
   KvHdr* h = reinterpret_cast<KvHdr*>(base);
   uint32_t* ghist = reinterpret_cast<uint32_t*>(base + KV_HIST_OFF);
   uint2* gcand = reinterpret_cast<uint2*>(base + KV_CAND_OFF);
+  uint32_t* gties = reinterpret_cast<uint32_t*>(base + KV_TIE_OFF);
   const uint32_t mode = h->mode;
   const int64_t len = h->len;
   const uint32_t key0 = h->key0, key1 = h->key1, kmin = h->kmin, kmax = h->kmax;
@@ -591,7 +649,9 @@ __global__ void __launch_bounds__(THREADS, 2)
     clear_hist(c.hist);
     if (threadIdx.x == 0) S.ncand = 0;
     __syncthreads();
-    const uint32_t C0 = scan_collect(row, s0, s1, R, c, nullptr, key0, key1, sb, lflags, 0u);
+    const uint32_t C0 = scan_collect(row, s0, s1, R, c, nullptr,
+                                     TieList{gties, (uint32_t)TIE_CAP, &h->neq}, key0, key1, sb,
+                                     lflags, 0u);
     const uint32_t nloc = S.ncand;
     if (threadIdx.x == 0) {
       atomicAdd(&h->c0, C0);
@@ -640,20 +700,21 @@ __global__ void __launch_bounds__(THREADS, 2)
     return;
   }
   uint32_t C0 = __ldcg(&h->c0);
-  const uint32_t C1 = __ldcg(&h->ncand);
-  const bool overflow = __ldcg(&h->ovf) != 0u || C1 > (uint32_t)CAP_ALL;
+  const uint32_t Cgt = __ldcg(&h->ncand), Ceq = __ldcg(&h->neq);
+  if (key0 == key1) C0 += Ceq;
+  const bool overflow = __ldcg(&h->ovf) != 0u || Cgt > (uint32_t)CAP_ALL;
   for (int i = threadIdx.x; i < NB; i += THREADS) c.hist[i] = __ldcg(&ghist[i]);
-  const uint32_t nload = min(C1, (uint32_t)CAP);
+  const uint32_t nload = min(Cgt, (uint32_t)CAP);
   for (uint32_t j = threadIdx.x; j < nload; j += THREADS) {
     const uint2* p = gcand + j;
     c.cand[j] = make_uint2(__ldcg(&p->x), __ldcg(&p->y));
   }
   __syncthreads();
   const int32_t path =
-      select_after_scan(row, len, out, Kr, R, c, gcand + CAP, sample_spec(P, len, Kr), C0, C1,
-                        overflow, key0, key1, kmin, sb, lflags);
+      select_after_scan(row, len, out, Kr, R, c, gcand + CAP, gties, sample_spec(P, len, Kr), C0,
+                        Cgt, Ceq, overflow, key0, key1, kmin, sb, lflags);
   finish_row(S, out, Kr, K, lflags, diag, r, path, key_to_float(key0), key_to_float(key1), C0,
-             C1);
+             Cgt + Ceq);
   ring_drain(R);
 }
 
@@ -669,7 +730,7 @@ size_t direct_smem_bytes(int64_t n_alloc, int elem_bytes) {
          align_up((size_t)n_alloc * elem_bytes + 16, 16);
 }
 size_t kv_row_bytes() { return KV_ROW_BYTES; }
-size_t persistent_spill_bytes() { return (size_t)SPILL * sizeof(uint2); }
+size_t persistent_spill_bytes() { return CTA_AREA_BYTES; }
 
 static cudaError_t set_smem(const void* fn, size_t bytes) {
   return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);

@@ -44,8 +44,8 @@ size_t kv_prepare_smem_bytes();
 size_t direct_smem_bytes(int64_t n_alloc, int elem_bytes);
 size_t kv_row_bytes();
 // Bytes of KV-split merge state per row (equals kv_row_bytes()).
-constexpr size_t kKvRowBytes = 139520;
-// Bytes of global candidate spill area per persistent CTA.
+constexpr size_t kKvRowBytes = 155904;
+// Bytes of global memory per persistent CTA (candidate spill area and tie list).
 size_t persistent_spill_bytes();
 
 // Sets the kernels' shared-memory limits on the current device.

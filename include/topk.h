@@ -227,7 +227,7 @@ int topk_ragged_k_diag(const float* scores, const int32_t* row_lens, const int32
  * not risk the device-wide synchronisation or out-of-memory failure an
  * allocation can bring.  It runs the KV-split path with its per-row merge
  * state in one statically sized device array (TOPK_NOALLOC_MAX_ROWS rows,
- * about 8.5 MiB) that every GPU loading this library holds until the process
+ * about 9.5 MiB) that every GPU loading this library holds until the process
  * exits.  Arguments and results are those of topk_ragged(); M above
  * TOPK_NOALLOC_MAX_ROWS returns TOPK_ERR_WORKSPACE.  The first call on a
  * device looks up the array's device address (make that first call before
