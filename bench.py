@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--K", type=int, default=K_DEFAULT)
     ap.add_argument("--no-matrix", action="store_true", help="skip the 20-shape operator matrix")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-narrow", action="store_true",
+                    help="skip the bfloat16 / FP8 E4M3 rows of the headline workload")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-chain", action="store_true",
                     help="skip the indexer-score + Top-K chain (tensor-core) line")
@@ -310,6 +312,47 @@ def profiled_traffic(params, plan, valid_bytes):
     return float(d["dram_bytes_per_valid_byte"]) * valid_bytes
 
 
+def narrow_leg(ets, dev, stream, N, M, K, peak, reps=5):
+    """The headline workload with its scores rounded to bfloat16 and to FP8
+    E4M3 (scaled by 4 and held below 448 first), selected exactly as their
+    widened values; device time of `reps` consecutive calls after two
+    untimed ones, and 4 rows spot-checked against the oracle."""
+    import oracle
+    res = {}
+    for name in ("bf16", "e4m3"):
+        x32, lens = make_inputs(N, M, 0, seed=7, device=dev)
+        if name == "bf16":
+            x = x32.to(torch.bfloat16)
+        else:
+            x = (x32 * 4.0).clamp(max=448.0).to(torch.float8_e4m3fn)
+        del x32
+        d_lens = lens.to(dev)
+        out = torch.empty((M, K), dtype=torch.int32, device=dev)
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                ets.topk_ragged(x, d_lens, K, out=out, stream=stream)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                ets.topk_ragged(x, d_lens, K, out=out, stream=stream)
+            b.record(stream)
+        stream.synchronize()
+        ms = a.elapsed_time(b) / reps
+        nbytes = float(lens.to(torch.int64).sum()) * x.element_size()
+        rows = torch.linspace(0, M - 1, 4).round().long()
+        xr = x[rows.to(dev)].float().cpu().numpy()
+        v = oracle.compare(xr, lens[rows].numpy(), K, out[rows.to(dev)].cpu().numpy())
+        res[name] = {"ms_per_call": ms, "rows_per_s": M / (ms / 1000.0),
+                     "gbps_valid_scores": nbytes / (ms / 1000.0) / 1e9,
+                     "frac": nbytes / (ms / 1000.0) / 1e9 / peak, "reps": reps,
+                     "spot_check": {"rows": 4, "contract_failures": int((v["check"] != 0).sum()),
+                                    "set_mismatches": int(v["set_mismatch"].sum())}}
+        del x, out
+        torch.cuda.empty_cache()
+    return res
+
+
 def make_inputs(N, M, group, seed, device):
     from exact_top_sparse_gb300 import synth
     lens = synth.causal_lens(N, M, group)
@@ -529,6 +572,16 @@ def run_gb300(args):
         del x
         x = None
         torch.cuda.empty_cache()
+
+    if not args.no_narrow and rank == 0 and N == 1048576 and M == 8192:
+        if x is not None:
+            del x
+            x = None
+            torch.cuda.empty_cache()
+        try:
+            result["narrow_rows"] = narrow_leg(ets, dev, stream, N, M, K, peak)
+        except RuntimeError as e:
+            result["narrow_rows"] = {"error": str(e)[:200]}
 
     if not args.no_chain and rank == 0:
         if x is not None:
