@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--K", type=int, default=K_DEFAULT)
     ap.add_argument("--no-matrix", action="store_true", help="skip the 20-shape operator matrix")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--dtype", default="f32", choices=["f32", "bf16", "e4m3"],
+                    help="score type of the timed rows (the headline is f32)")
     ap.add_argument("--no-narrow", action="store_true",
                     help="skip the bfloat16 / FP8 E4M3 rows of the headline workload")
     ap.add_argument("--no-cpu", action="store_true")
@@ -281,20 +283,22 @@ SAMPLING_KNOBS = ("stride", "rho0", "rho1", "sample_min_len", "long_len", "long_
                   "long_rho0", "long_rho1")
 
 
-def kernel_fingerprint(params, kind, grid):
+def kernel_fingerprint(params, kind, grid, elem_bytes=4):
     """Hash of what decides a selector launch's DRAM traffic: the kernel
-    sources, the sampling parameters in effect and the launch shape."""
+    sources, the sampling parameters in effect, the launch shape and the
+    score element size."""
     import hashlib
     h = hashlib.sha256()
     for name in ("score_elem.cuh", "topk_device.cuh", "topk_kernels.cu", "topk_launch.h"):
         with open(os.path.join(ROOT, "exact_top_sparse_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
-    launch = {"sampling": {k: params[k] for k in SAMPLING_KNOBS}, "kind": kind, "grid": grid}
+    launch = {"sampling": {k: params[k] for k in SAMPLING_KNOBS}, "kind": kind, "grid": grid,
+              "elem_bytes": elem_bytes}
     h.update(json.dumps(launch, sort_keys=True).encode())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(params, plan, valid_bytes):
+def profiled_traffic(params, plan, valid_bytes, elem_bytes=4):
     """DRAM bytes per launch from the committed ncu capture of this kernel.
 
     profiles/k_persistent_traffic.json holds the DRAM-bytes-per-valid-byte
@@ -307,7 +311,8 @@ def profiled_traffic(params, plan, valid_bytes):
         return None
     with open(p) as f:
         d = json.load(f)
-    if kernel_fingerprint(params, plan["kind"], plan["grid"]) != d.get("kernel_fingerprint"):
+    if (kernel_fingerprint(params, plan["kind"], plan["grid"], elem_bytes)
+            != d.get("kernel_fingerprint")):
         return None
     return float(d["dram_bytes_per_valid_byte"]) * valid_bytes
 
@@ -468,8 +473,17 @@ def run_gb300(args):
                                    "kvsplit": ets.KIND_KVSPLIT}[args.force_kind])
 
     x, lens = make_inputs(N, M, 0, seed=7 + rank, device=dev)
+    if args.dtype == "bf16":
+        x = x.to(torch.bfloat16)
+    elif args.dtype == "e4m3":
+        # scaled by 4 and held below the largest E4M3 value before rounding
+        x = (x * 4.0).clamp(max=448.0).to(torch.float8_e4m3fn)
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
     d_lens = lens.to(dev)
-    valid_bytes = 4.0 * float(lens.to(torch.int64).sum())
+    elem_bytes = x.element_size()
+    valid_bytes = float(elem_bytes) * float(lens.to(torch.int64).sum())
+    type_name = {"f32": "FP32", "bf16": "bfloat16", "e4m3": "FP8 E4M3"}[args.dtype]
     plan = ets.plan(M, N, K)
     launches_per_step = 2 if plan["kind"] == "kvsplit" else 1
 
@@ -494,10 +508,11 @@ def run_gb300(args):
     result = {
         "metric": METRIC, "value": rows_per_s, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "scaling": "weak", "vs_baseline": None, "dtype": args.dtype,
         "data": "synthetic (seeded indexer-like rows: Normal(30+N(0,1), 2.5) body, 0.2% "
                 "Exponential(mean 6) upper tail, -inf causal suffix)",
-        "config": {"workload": "causal ragged FP32 score rows N_alloc=%d M=%d K=%d" % (N, M, K),
+        "config": {"workload": "causal ragged %s score rows N_alloc=%d M=%d K=%d"
+                               % (type_name, N, M, K),
                    "N_alloc": N, "M": M, "K": K, "path": plan["kind"],
                    "grid": plan["grid"], "segments": plan["segments"],
                    "l2": "inputs (%.1f GB of valid scores) exceed the 129 MB L2; no flush"
@@ -506,7 +521,8 @@ def run_gb300(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "traffic": (args.traffic if args.traffic is not None
-                                 else profiled_traffic(ets.get_params(), plan, valid_bytes)),
+                                 else profiled_traffic(ets.get_params(), plan, valid_bytes,
+                                                       elem_bytes)),
                      "bytes_per_launch": valid_bytes,
                      "kernel": "k_kv_segment" if plan["kind"] == "kvsplit" else
                                ("k_direct" if plan["kind"] == "direct" else "k_persistent")},
@@ -519,7 +535,7 @@ def run_gb300(args):
     if rank == 0:
         import oracle
         rows = torch.linspace(0, M - 1, 8).round().long()
-        xr = x[rows.to(dev)].cpu().numpy()
+        xr = x[rows.to(dev)].float().cpu().numpy()
         v = oracle.compare(xr, lens[rows].numpy(), K, out[rows.to(dev)].cpu().numpy())
         result["spot_check"] = {"rows": 8, "contract_failures": int((v["check"] != 0).sum()),
                                 "set_mismatches": int(v["set_mismatch"].sum())}
@@ -527,7 +543,8 @@ def run_gb300(args):
     # the operator matrix (informational): widths 128K-1M x M in {512..8192},
     # causal groups of M rows of the last 8192; per shape the median over
     # groups (up to 4, spread over the window) of the median of 5 calls
-    if not args.no_matrix and rank == 0 and N == 1048576 and M == 8192:
+    full_f32 = args.dtype == "f32" and N == 1048576 and M == 8192
+    if not args.no_matrix and rank == 0 and full_f32:
         del out
         torch.cuda.empty_cache()
         mat = {}
@@ -573,7 +590,7 @@ def run_gb300(args):
         x = None
         torch.cuda.empty_cache()
 
-    if not args.no_narrow and rank == 0 and N == 1048576 and M == 8192:
+    if not args.no_narrow and rank == 0 and full_f32:
         if x is not None:
             del x
             x = None
@@ -601,7 +618,7 @@ def run_gb300(args):
                 result[name] = {"error": str(e)[:200]}
 
     # end to end through the host-buffer C ABI: pinned host rows in, indices out
-    if not args.no_e2e and rank == 0:
+    if not args.no_e2e and rank == 0 and args.dtype == "f32":
         if x is None:
             x, _ = make_inputs(N, M, 0, seed=7, device=dev)
         try:
@@ -626,7 +643,7 @@ def run_gb300(args):
             del h
         except RuntimeError as e:
             result["e2e"] = {"value": None, "unit": UNIT, "error": str(e)[:200]}
-    if not args.no_cpu and rank == 0:
+    if not args.no_cpu and rank == 0 and args.dtype == "f32":
         xs, ls = host_sample(N, M, K, rows=32)
         rate, threads, el = cpu_oracle_rate(xs, ls, K)
         result["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": threads,
