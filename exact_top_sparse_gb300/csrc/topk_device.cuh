@@ -572,7 +572,8 @@ __device__ __forceinline__ uint2 cand_at(const uint2* cand, const uint2* spill, 
 // tau1 the answer takes every score above it and any of the ties (the
 // contract lets boundary ties go either way), so the first K ties suffice.
 // E4M3 rows (8 values per octave) put long runs of ties at tau1, which would
-// otherwise overflow the candidate buffers; for FP32 and bfloat16 rows
+// otherwise overflow the candidate buffers (with tau1 > +0 their units are
+// tested byte-wise, put_e4m3_unit); for FP32 and bfloat16 rows
 // (TIES = false) ties are ordinary candidates, which keeps their scan loop
 // leaner (measured 13 % and 5 % faster), and a rare long tie run takes the
 // overflow path.
@@ -642,6 +643,44 @@ struct ScanCollect {
       else if (pos < cap) spill[pos - (uint32_t)CAP] = ent;
       ++pos;
     } while (m);
+  }
+  // E4M3 unit of 16 raw bytes from index i0 on, tau1 > +0 with byte
+  // pattern t (repeated in the four bytes of t4): bytes compare as signed
+  // integers in the order of the values, so the admission and the tie test
+  // are packed byte compares, and only the kept scores are widened.
+  __device__ __forceinline__ void put_e4m3_unit(int64_t i0, const uint4& u, uint32_t t4) const {
+    const uint32_t ge = byte_flags(__vcmpges4(u.x, t4)) | (byte_flags(__vcmpges4(u.y, t4)) << 4) |
+                        (byte_flags(__vcmpges4(u.z, t4)) << 8) |
+                        (byte_flags(__vcmpges4(u.w, t4)) << 12);
+    const uint32_t eq = byte_flags(__vcmpeq4(u.x, t4)) | (byte_flags(__vcmpeq4(u.y, t4)) << 4) |
+                        (byte_flags(__vcmpeq4(u.z, t4)) << 8) |
+                        (byte_flags(__vcmpeq4(u.w, t4)) << 12);
+    if (eq) {
+      uint32_t q = eq;
+      uint32_t t = atomicAdd(neq, (uint32_t)__popc(q));
+      while (q && t < tie_cap) {
+        const uint32_t e = (uint32_t)__ffs(q) - 1u;
+        q &= q - 1u;
+        ties[t++] = (uint32_t)(i0 + e);
+      }
+    }
+    uint32_t m = ge & ~eq;
+    if (!m) return;
+    uint32_t pos = atomicAdd(ncand, (uint32_t)__popc(m));
+    do {
+      const uint32_t e = (uint32_t)__ffs(m) - 1u;
+      m &= m - 1u;
+      const uint32_t wd = e < 8u ? (e < 4u ? u.x : u.y) : (e < 12u ? u.z : u.w);
+      const uint32_t b = (wd >> (8u * (e & 3u))) & 0xFFu;
+      const uint2 ent = make_uint2((uint32_t)(i0 + e), fkey(Elem<uint8_t>::widen(b)));
+      if (pos < (uint32_t)CAP) cand[pos] = ent;
+      else if (pos < cap) spill[pos - (uint32_t)CAP] = ent;
+      ++pos;
+    } while (m);
+  }
+  // 4-bit mask of the bytes that are 0xFF in a per-byte compare result
+  __device__ static __forceinline__ uint32_t byte_flags(uint32_t c) {
+    return ((c >> 7) & 1u) | ((c >> 14) & 2u) | ((c >> 21) & 4u) | ((c >> 28) & 8u);
   }
   // Appends the admitted scores among the elements of v selected by vm
   // (element i0 + e is lane e).
@@ -779,6 +818,11 @@ __device__ __forceinline__ void scan_pass(Ring& R, const E* __restrict__ row, in
                               off + (int64_t)P16 * j0 + 4, Elem<E>::group(u0, 1), true);
           if (h1) f.lane_put2(off + (int64_t)P16 * j1, Elem<E>::group(u1, 0), true,
                               off + (int64_t)P16 * j1 + 4, Elem<E>::group(u1, 1), true);
+        } else if constexpr (TIES && POS) {
+          // E4M3 above +0: packed byte compares against tau1's byte
+          const uint32_t t4 = (uint32_t)thr * 0x01010101u;
+          if (h0) f.put_e4m3_unit(off + (int64_t)P16 * j0, u0, t4);
+          if (h1) f.put_e4m3_unit(off + (int64_t)P16 * j1, u1, t4);
         } else {
           // one unit and a pair of groups (eight scores) at a time: a single
           // inlined append keeps few values live
