@@ -29,9 +29,7 @@ struct Elem<float> {
   __device__ static __forceinline__ float load_keep(const float* p, uint64_t pol) {
     return ld_keep(p, pol);
   }
-  // the elements of one 16-byte unit as groups of four widened values
-  __device__ static __forceinline__ void groups(const uint4& u, float4* g) { g[0] = group(u, 0); }
-  // group k alone
+  // group k of the elements of one 16-byte unit: four widened values
   __device__ static __forceinline__ float4 group(const uint4& u, int) {
     return make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
                        __uint_as_float(u.w));
@@ -46,10 +44,6 @@ struct Elem<uint16_t> {
     uint16_t v;
     asm volatile("ld.global.cg.L2::cache_hint.u16 %0, [%1], %2;" : "=h"(v) : "l"(p), "l"(pol));
     return widen(v);
-  }
-  __device__ static __forceinline__ void groups(const uint4& u, float4* g) {
-    g[0] = group(u, 0);
-    g[1] = group(u, 1);
   }
   __device__ static __forceinline__ float4 group(const uint4& u, int k) {
     const uint32_t a = k ? u.z : u.x, b = k ? u.w : u.y;
@@ -75,10 +69,6 @@ struct Elem<uint8_t> {
     uint16_t v;
     asm volatile("ld.global.cg.L2::cache_hint.u8 %0, [%1], %2;" : "=h"(v) : "l"(p), "l"(pol));
     return widen(v & 0xFFu);
-  }
-  __device__ static __forceinline__ void groups(const uint4& u, float4* g) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) g[k] = group(u, k);
   }
   __device__ static __forceinline__ float4 group(const uint4& u, int k) {
     const uint32_t w = k == 0 ? u.x : k == 1 ? u.y : k == 2 ? u.z : u.w;
