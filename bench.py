@@ -117,10 +117,7 @@ def trace_leg(ets, dev, stream, tokens=430 * 1024, K=2048):
     from exact_top_sparse_gb300 import synth, trace
     calls = trace.calls(tokens)
     W = trace.WORKSPACE_FLOATS
-    buf = torch.empty(W, dtype=torch.float32, device=dev)
-    rows_all = W // 65536
-    synth.indexer_rows(torch.full((rows_all,), 65536, dtype=torch.int32), 65536, seed=17,
-                       out=buf.view(rows_all, 65536))
+    buf = synth.trace_scores(W, seed=17, device=dev)
     lens_all = torch.arange(1, tokens + 1, dtype=torch.int32, device=dev)
     outs = torch.empty((max(c.rows for c in calls), K), dtype=torch.int32, device=dev)
     valid = sum(4.0 * (c.row0 * c.rows + c.rows * (c.rows + 1) / 2.0) for c in calls)

@@ -71,7 +71,8 @@ EXPORTS = ("topk_ragged", "topk_ragged_diag", "topk_ragged_ws", "topk_workspace_
            "topk_index_scores", "topk_index_topk", "topk_index_read_status",
            "topk_ragged_bf16", "topk_ragged_bf16_diag", "topk_sort_rows", "topk_sort_rows_bf16",
            "topk_check_wait_timeout", "topk_ragged_k", "topk_ragged_k_bf16", "topk_ragged_k_diag",
-           "topk_ragged_e4m3", "topk_ragged_e4m3_diag", "topk_ragged_k_e4m3", "topk_sort_rows_e4m3")
+           "topk_ragged_e4m3", "topk_ragged_e4m3_diag", "topk_ragged_k_e4m3", "topk_sort_rows_e4m3",
+           "topk_cached_workspace")
 NOALLOC_MAX_ROWS = 64
 
 _lib = None
@@ -113,6 +114,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.topk_workspace_bytes.restype = sz
     lib.topk_ragged_host.argtypes = [vp, vp, i64, i64, i32, vp, i64]
     lib.topk_plan.argtypes = [i64, i64, i32, ctypes.POINTER(PlanInfo)]
+    lib.topk_cached_workspace.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(sz)]
     lib.topk_set_params.argtypes = [ctypes.POINTER(Params)]
     lib.topk_get_params.argtypes = [ctypes.POINTER(Params)]
     lib.topk_default_params.argtypes = [ctypes.POINTER(Params)]
@@ -130,7 +132,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                  "topk_ragged_k_diag", "topk_ragged_e4m3", "topk_ragged_e4m3_diag",
                  "topk_ragged_k_e4m3", "topk_sort_rows_e4m3", "topk_index_read_status",
                  "topk_plan", "topk_set_params", "topk_get_params", "topk_read_status",
-                 "topk_version"):
+                 "topk_version", "topk_cached_workspace"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -361,6 +363,18 @@ def read_status(device=None, stream=None) -> int:
         _check(load_library().topk_read_status(_stream_handle(dev, stream), ctypes.byref(flags)),
                "topk_read_status")
     return int(flags.value)
+
+
+def cached_workspace(device=None, stream=None):
+    """(device address, bytes) of the library's workspace for (device, stream);
+    (0, 0) when the stream has none yet."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    ptr, nbytes = ctypes.c_void_p(0), ctypes.c_size_t(0)
+    with torch.cuda.device(dev):
+        _check(load_library().topk_cached_workspace(_stream_handle(dev, stream),
+                                                    ctypes.byref(ptr), ctypes.byref(nbytes)),
+               "topk_cached_workspace")
+    return int(ptr.value or 0), int(nbytes.value)
 
 
 def release_workspaces() -> None:

@@ -13,6 +13,7 @@
 #include <map>
 #include <mutex>
 #include <utility>
+#include <vector>
 
 #include "../../include/topk.h"
 #include "topk_launch.h"
@@ -50,8 +51,13 @@ struct Buf {
   size_t bytes = 0;
 };
 std::map<std::pair<int, uintptr_t>, Buf> g_ws;  // (device, stream) -> workspace
+// Workspaces a stream has grown out of.  A CUDA graph captured earlier on
+// that stream still holds their addresses, so they stay allocated until
+// topk_release_workspaces().
+std::vector<std::pair<int, void*>> g_retired;
 
 struct HostPipe {
+  std::mutex mu;  // one host-buffer call at a time per device
   float* scores[2] = {nullptr, nullptr};
   int32_t* lens[2] = {nullptr, nullptr};
   int32_t* out[2] = {nullptr, nullptr};
@@ -223,8 +229,12 @@ int launch(const Plan& pl, const tk::Params& P, const void* scores, const int32_
   return e == cudaSuccess ? TOPK_OK : TOPK_ERR_CUDA;
 }
 
-// Workspace for (current device, stream), grown on demand.  A new buffer is
-// zero-filled (the persistent queue counters must start at zero).
+// Workspace for (current device, stream), grown on demand (at least doubling,
+// so a stream retires few buffers).  The buffer it replaces is never freed
+// here: a graph captured on this stream may still use it, so it moves to
+// g_retired.  A new buffer is zero-filled on the call's own stream, ahead of
+// the kernels that read it (the persistent queue counters and the fail-fast
+// flag must start at zero).
 int cached_workspace(int dev, cudaStream_t st, size_t need, void** ptr) {
   std::lock_guard<std::mutex> lk(g_mu);
   Buf& b = g_ws[{dev, reinterpret_cast<uintptr_t>(st)}];
@@ -235,22 +245,18 @@ int cached_workspace(int dev, cudaStream_t st, size_t need, void** ptr) {
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return TOPK_ERR_CUDA;
   if (cs != cudaStreamCaptureStatusNone) return TOPK_ERR_CAPTURE_ALLOC;
-  if (b.ptr) {
-    if (cudaStreamSynchronize(st) != cudaSuccess) return TOPK_ERR_CUDA;
-    cudaFree(b.ptr);
-    b.ptr = nullptr;
-    b.bytes = 0;
-  }
   size_t bytes = need < (1u << 20) ? (1u << 20) : need;
+  if (b.ptr && bytes < 2 * b.bytes) bytes = 2 * b.bytes;
   void* p = nullptr;
   if (cudaMalloc(&p, bytes) != cudaSuccess) {
     cudaGetLastError();
     return TOPK_ERR_CUDA;
   }
-  if (cudaMemset(p, 0, bytes) != cudaSuccess) {
+  if (cudaMemsetAsync(p, 0, bytes, st) != cudaSuccess) {
     cudaFree(p);
     return TOPK_ERR_CUDA;
   }
+  if (b.ptr) g_retired.emplace_back(dev, b.ptr);
   b.ptr = p;
   b.bytes = bytes;
   *ptr = p;
@@ -434,6 +440,17 @@ size_t topk_workspace_bytes(int64_t M, int64_t N_alloc, int32_t K) {
   return pl.ws;
 }
 
+int topk_cached_workspace(struct CUstream_st* stream, void** ptr, size_t* bytes) {
+  if (!ptr || !bytes) return TOPK_ERR_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TOPK_ERR_NO_DEVICE;
+  std::lock_guard<std::mutex> lk(g_mu);
+  const auto it = g_ws.find({dev, reinterpret_cast<uintptr_t>(stream)});
+  *ptr = it == g_ws.end() ? nullptr : it->second.ptr;
+  *bytes = it == g_ws.end() ? 0 : it->second.bytes;
+  return TOPK_OK;
+}
+
 int topk_plan(int64_t M, int64_t N_alloc, int32_t K, topk_plan_info* info) {
   if (!info) return TOPK_ERR_ARG;
   int rc = check_sizes(M, N_alloc, K);
@@ -503,8 +520,11 @@ int topk_ragged_host(const float* h_scores, const int32_t* h_lens, int64_t M, in
   HostPipe* hp;
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    hp = &g_pipe[dev];
+    hp = &g_pipe[dev];  // map nodes stay put; only topk_release_workspaces removes them
   }
+  // Calls from several host threads on one device take turns on its buffers
+  // and streams.
+  std::lock_guard<std::mutex> pipe_lock(hp->mu);
   const size_t need_s = (size_t)rows * row_bytes, need_l = (size_t)rows * 4,
                need_o = (size_t)rows * K * 4;
   for (int i = 0; i < 2; ++i) {
@@ -577,6 +597,12 @@ void topk_release_workspaces(void) {
     cudaFree(kv.second.ptr);
   }
   g_ws.clear();
+  for (auto& r : g_retired) {
+    cudaSetDevice(r.first);
+    cudaDeviceSynchronize();
+    cudaFree(r.second);
+  }
+  g_retired.clear();
   for (auto& kv : g_pipe) {
     cudaSetDevice(kv.first);
     cudaDeviceSynchronize();

@@ -125,23 +125,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Set by the first wait that gives up; every later wait then fails at once,
-// so a kernel that lost a copy finishes quickly (its rows flagged) instead of
-// timing out wait after wait.  Cleared when the status word is read and by
-// the last CTA of each persistent launch.
-__device__ uint32_t g_abort;
-
 // Slow path of mbar_wait: polls until the phase completes, giving up after
 // limit_ns (WAIT_LIMIT_NS in the kernels) so that no wait can hang the GPU.
-__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity,
+// `abort` is the fail-fast flag of the work the waiting CTA belongs to (a
+// persistent launch's workspace header, a KV-split row's header; nullptr for
+// a CTA that works alone): the first wait that gives up sets it, and every
+// later wait on that work then fails at once, so a launch that lost a copy
+// ends quickly (its rows flagged) instead of timing out wait after wait.  The
+// flag lives in memory that belongs to one launch and is reset by it (the
+// last CTA of a persistent launch, the prepare kernel of a KV-split launch),
+// so an abort never reaches another launch.
+__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, uint32_t* abort,
                                             uint64_t limit_ns = WAIT_LIMIT_NS) {
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
-      if (*reinterpret_cast<volatile uint32_t*>(&g_abort) != 0u) return false;
+      if (abort != nullptr && *reinterpret_cast<volatile uint32_t*>(abort) != 0u) return false;
       if (globaltimer() - t0 > limit_ns) {
-        atomicExch(&g_abort, 1u);
+        if (abort != nullptr) atomicExch(abort, 1u);
         return false;
       }
     }
@@ -157,10 +159,11 @@ __device__ __noinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uin
   return true;
 }
 
-// Waits for the phase of `bar` with the given parity (false after a timeout).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Waits for the phase of `bar` with the given parity (false after a timeout
+// or once `abort` is set).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* abort) {
   if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity);
+  return mbar_wait_slow(bar, parity, abort);
 }
 
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
@@ -422,14 +425,16 @@ struct Ring {
   uint64_t* empty;
   uint32_t seq;
   uint64_t policy;
+  uint32_t* abort;  // fail-fast flag of the launch's work (see mbar_wait_slow)
 };
 
-__device__ __forceinline__ void ring_init(Ring& R, Shared& S, float* buf) {
+__device__ __forceinline__ void ring_init(Ring& R, Shared& S, float* buf, uint32_t* abort) {
   R.buf = buf;
   R.full = S.full;
   R.empty = S.empty;
   R.seq = 0;
   R.policy = l2_policy_evict_first();
+  R.abort = abort;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&S.full[s], 1);
@@ -447,7 +452,7 @@ __device__ __forceinline__ void ring_issue(Ring& R, const E* __restrict__ row, i
                                            int64_t a1, uint32_t c, uint32_t& lflags) {
   constexpr int64_t CE = CHUNK_BYTES / Elem<E>::kSize;
   const uint32_t q = R.seq + c, s = q % STAGES, use = q / STAGES;
-  if (!mbar_wait(&R.empty[s], (use & 1u) ^ 1u)) lflags |= F_TIMEOUT;
+  if (!mbar_wait(&R.empty[s], (use & 1u) ^ 1u, R.abort)) lflags |= F_TIMEOUT;
   const int64_t off = a0 + (int64_t)c * CE;
   const int64_t n = (a1 - off) < CE ? (a1 - off) : CE;
   const uint32_t bytes = (uint32_t)(n * Elem<E>::kSize);
@@ -530,7 +535,7 @@ __device__ __forceinline__ void ring_pass(Ring& R, const E* __restrict__ row, in
     constexpr int64_t CE = CHUNK_BYTES / Elem<E>::kSize;
     for (uint32_t c = 0; c < nchunks; ++c) {
       const uint32_t q = R.seq + c, s = q % STAGES, use = q / STAGES;
-      if (!mbar_wait(&R.full[s], use & 1u)) lflags |= F_TIMEOUT;
+      if (!mbar_wait(&R.full[s], use & 1u, R.abort)) lflags |= F_TIMEOUT;
       const int64_t off = a0 + (int64_t)c * CE;
       const int64_t n = (a1 - off) < CE ? (a1 - off) : CE;
       const int nu = (int)(n / P16);
@@ -775,7 +780,7 @@ __device__ __forceinline__ void scan_pass(Ring& R, const E* __restrict__ row, in
     else thr = POS ? (int32_t)f.t1 : (int32_t)(f.t1 ^ 0x80000000u);
     for (uint32_t c = 0; c < nchunks; ++c) {
       const uint32_t q = R.seq + c, s = q % STAGES, use = q / STAGES;
-      if (!mbar_wait(&R.full[s], use & 1u)) lflags |= F_TIMEOUT;
+      if (!mbar_wait(&R.full[s], use & 1u, R.abort)) lflags |= F_TIMEOUT;
       const int64_t off = a0 + (int64_t)c * CE;
       const int64_t n = (a1 - off) < CE ? (a1 - off) : CE;
       const int nu = (int)(n / P16);

@@ -80,6 +80,7 @@ struct KvHdr {
   float tau0, tau1;
   int32_t k;     // the row's own K
   uint32_t neq;  // scores equal to tau1 over all segments
+  uint32_t abort;  // fail-fast flag of the row's CTAs (reset by k_kv_prepare)
 };
 constexpr size_t KV_HIST_OFF = 256;
 constexpr size_t KV_CAND_OFF = KV_HIST_OFF + (size_t)NB * sizeof(uint32_t);
@@ -403,7 +404,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     S.next_ok = 0;
   }
   Ring R;
-  ring_init(R, S, c.ring);
+  ring_init(R, S, c.ring, hdr + 2);  // hdr[2]: this launch's fail-fast flag
   const int32_t K = P.K;
   for (;;) {
     if (threadIdx.x == 0) {
@@ -481,14 +482,15 @@ __global__ void __launch_bounds__(THREADS, 2)
                Cgt + Ceq);
   }
   ring_drain(R);
-  // The last CTA to leave resets the queue, so the next launch (or graph
-  // replay) starts from zero without a separate memset.
+  // The last CTA to leave resets the queue and the fail-fast flag, so the
+  // next launch (or graph replay) on this workspace starts from zero without
+  // a separate memset.
   if (threadIdx.x == 0) {
     __threadfence();
     if (atomicAdd(&hdr[1], 1u) == gridDim.x - 1) {
       atomicExch(&hdr[0], 0u);
       atomicExch(&hdr[1], 0u);
-      atomicExch(&g_abort, 0u);
+      atomicExch(&hdr[2], 0u);
       __threadfence();
     }
   }
@@ -550,7 +552,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   for (int64_t i = threadIdx.x; i < a0; i += THREADS) buf[i] = row[i];
   for (int64_t i = a1 + threadIdx.x; i < len; i += THREADS) buf[i] = row[i];
-  if (!mbar_wait(&S.full[0], 0)) {
+  if (!mbar_wait(&S.full[0], 0, nullptr)) {  // one wait per CTA: nothing to fail fast
     lflags |= F_TIMEOUT;
     // gave up: still let the copies land (bounded) before this CTA moves on
     if (threadIdx.x == 0) mbar_wait_drain(&S.full[0], 0, 100000000ull);
@@ -612,6 +614,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     h->tau0 = key_to_float(key0);
     h->tau1 = key_to_float(key1);
     h->k = Kr;
+    h->abort = 0;
   }
 }
 
@@ -641,7 +644,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     S.nout = 0;
   }
   Ring R;
-  ring_init(R, S, c.ring);
+  ring_init(R, S, c.ring, &h->abort);
   uint32_t lflags = 0;
   const Bins sb = scan_bins(key1, kmax);
   if (mode == 2) {
@@ -832,14 +835,17 @@ cudaError_t launch_kvsplit(const void* scores, const int32_t* row_lens, int32_t*
 
 // Self-test of the bounded wait: one thread waits on a barrier that nothing
 // completes, with the kernels' own wait routine and a short limit; giving up
-// sets F_TIMEOUT in the status word (and the fail-fast flag, cleared when the
-// status is read).  No copy or other memory operation is pending meanwhile.
+// sets F_TIMEOUT in the status word.  The probe's fail-fast flag is its own
+// (a local), so no later launch sees it.  No copy or other memory operation
+// is pending meanwhile.
 __global__ void k_wait_probe(uint64_t limit_ns) {
   __shared__ uint64_t bar;
+  __shared__ uint32_t abort;
   if (threadIdx.x == 0) {
+    abort = 0u;
     mbar_init(&bar, 1);
     fence_mbar_init();
-    if (!mbar_wait_slow(&bar, 0u, limit_ns)) atomicOr(&g_status, F_TIMEOUT);
+    if (!mbar_wait_slow(&bar, 0u, &abort, limit_ns)) atomicOr(&g_status, F_TIMEOUT);
   }
 }
 
@@ -854,8 +860,6 @@ cudaError_t read_and_clear_status(cudaStream_t st, uint32_t* flags) {
                                             cudaMemcpyDeviceToHost, st);
   if (e != cudaSuccess) return e;
   e = cudaMemcpyToSymbolAsync(g_status, &zero, sizeof(uint32_t), 0, cudaMemcpyHostToDevice, st);
-  if (e != cudaSuccess) return e;
-  e = cudaMemcpyToSymbolAsync(g_abort, &zero, sizeof(uint32_t), 0, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return e;
   e = cudaStreamSynchronize(st);
   *flags = h;

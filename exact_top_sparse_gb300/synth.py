@@ -90,6 +90,23 @@ def indexer_rows(lens: torch.Tensor, N_alloc: int, seed: int, device="cpu",
     return out
 
 
+TRACE_ROW = 65536
+
+
+def trace_scores(n_floats: int, seed: int, device="cpu") -> torch.Tensor:
+    """A flat float32 buffer of n_floats indexer-like scores for a trace
+    replay: full-length rows of TRACE_ROW scores laid end to end (the body and
+    tail of indexer_rows), which each Top-K call of the trace views as its own
+    [rows, width] score matrix (n_floats a multiple of TRACE_ROW)."""
+    if n_floats % TRACE_ROW:
+        raise ValueError("n_floats must be a multiple of %d" % TRACE_ROW)
+    rows = n_floats // TRACE_ROW
+    buf = torch.empty(n_floats, dtype=torch.float32, device=device)
+    indexer_rows(torch.full((rows,), TRACE_ROW, dtype=torch.int32), TRACE_ROW, seed=seed,
+                 out=buf.view(rows, TRACE_ROW))
+    return buf
+
+
 def uniform_rows(lens: torch.Tensor, N_alloc: int, seed: int, device="cpu") -> torch.Tensor:
     """[M, N_alloc] float32, flat Uniform(0, 1) body with no tail, -inf suffix."""
     M = int(lens.numel())

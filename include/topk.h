@@ -40,6 +40,15 @@
  *     host, so they can be captured in a CUDA graph once the library's
  *     workspace for that stream exists (a call that would have to allocate
  *     during capture returns TOPK_ERR_CAPTURE_ALLOC);
+ *   - the library's workspace for a (device, stream) only grows; when a
+ *     larger call replaces it, the old buffer is kept allocated (a graph
+ *     captured earlier may still use it) until topk_release_workspaces(), so
+ *     a captured graph stays valid until then, whatever eager calls run on
+ *     its stream in between;
+ *   - a bounded wait inside a kernel that gives up flags its rows
+ *     (TOPK_FLAG_TIMEOUT) and makes the other waits of the same launch give
+ *     up at once; that state belongs to the launch and never reaches a
+ *     later call, whether or not the status word is read;
  *   - on an error code nothing has been enqueued.
  */
 #ifndef EXACT_TOPK_GB300_TOPK_H
@@ -179,13 +188,26 @@ int topk_ragged_e4m3_diag(const uint8_t* scores, const int32_t* row_lens, int64_
                           struct CUstream_st* stream);
 
 /* Device workspace bytes a call with these sizes needs under the current
- * parameters (0 is a valid answer only for M == 0). */
+ * parameters (0 is a valid answer only for M == 0).  The workspace is
+ * O(M) (KV-split merge state per row) or O(CTAs) (persistent spill areas),
+ * never O(M * N_alloc): the codexqa.cn article, section "20 个形状都最快",
+ * contrasts the method with a spill strategy that reserves 2 * M * N 32-bit
+ * entries and runs out of memory at long widths.  The size depends on the
+ * plan (topk_plan) and the parameters (topk_set_params). */
 size_t topk_workspace_bytes(int64_t M, int64_t N_alloc, int32_t K);
 
-/* Explicit-workspace form.  `workspace` is device memory of at least
- * topk_workspace_bytes(M, N_alloc, K) bytes, 256-byte aligned, zero-filled
- * before its first use; every call leaves it ready for the next.  Calls that
- * share one workspace must be ordered (same stream, or synchronised). */
+/* Explicit-workspace form of topk_ragged() (same contract and errors), for
+ * callers that manage device memory themselves; the workspace is the only
+ * memory the call uses beyond its inputs and outputs, and it is bounded as
+ * topk_workspace_bytes() states (codexqa.cn, section "20 个形状都最快").
+ *   workspace        device memory of at least topk_workspace_bytes(M,
+ *                    N_alloc, K) bytes, 256-byte aligned (else
+ *                    TOPK_ERR_ALIGN), zero-filled before its first use; every
+ *                    call leaves it ready for the next; owned by the caller
+ *   workspace_bytes  its size; smaller than needed -> TOPK_ERR_WORKSPACE
+ * Calls that share one workspace must be ordered (same stream, or
+ * synchronised).  Never allocates, so it can be captured in a CUDA graph
+ * whenever the workspace outlives the graph. */
 int topk_ragged_ws(const float* scores, const int32_t* row_lens, int64_t M, int64_t N_alloc,
                    int32_t K, int32_t* out_idx, void* workspace, size_t workspace_bytes,
                    struct CUstream_st* stream);
@@ -244,10 +266,17 @@ int topk_ragged_noalloc(const float* scores, const int32_t* row_lens, int64_t M,
  *   h_lens    host [M] int32
  *   h_out     host [M][K] int32
  *   rows_per_chunk  rows per device chunk; 0 picks about 1 GiB of scores per chunk
- * Synchronous: returns after h_out is written.  Device buffers are cached
- * per device until topk_release_workspaces(). */
+ * Synchronous: returns after h_out is written.  Device buffers and the two
+ * streams are cached per device until topk_release_workspaces(); calls from
+ * several host threads on one device take turns on them (a lock held for the
+ * whole call). */
 int topk_ragged_host(const float* h_scores, const int32_t* h_lens, int64_t M, int64_t N_alloc,
                      int32_t K, int32_t* h_out, int64_t rows_per_chunk);
+
+/* The library's cached workspace for (current device, `stream`): its device
+ * address and size in *ptr and *bytes (NULL and 0 when none exists yet).
+ * Read-only; for callers that check what a captured graph refers to. */
+int topk_cached_workspace(struct CUstream_st* stream, void** ptr, size_t* bytes);
 
 /* Read-only planning: what a call with these sizes would launch. */
 int topk_plan(int64_t M, int64_t N_alloc, int32_t K, topk_plan_info* info);
@@ -261,11 +290,21 @@ int topk_get_params(topk_params* p);
 void topk_default_params(topk_params* p);
 
 /* Read and clear the current device's status word: the OR of TOPK_FLAG_* over
- * every row selected since the last read.  Synchronises `stream` first. */
+ * every row selected since the last read (host memory *flags).  The set
+ * contract treats failures as their own outcome, never as a slower correct
+ * run (codexqa.cn, sections "什么叫精确，时间怎么量" and "这组数字不能外推的
+ * 地方": illegal results, illegal accesses and out-of-memory are reported
+ * apart); this word is where a call reports rows it could not serve
+ * exactly (TOPK_FLAG_INTERNAL, TOPK_FLAG_TIMEOUT) apart from informational
+ * bits (clamped lengths or K, overflow and recovery paths taken).  Enqueues a
+ * copy on `stream` and synchronises it; TOPK_ERR_ARG for a null `flags`,
+ * TOPK_ERR_CUDA if the copy or the synchronisation fails. */
 int topk_read_status(struct CUstream_st* stream, uint32_t* flags);
 
-/* Free every cached workspace and host-path buffer of this process
- * (synchronises the devices that own them). */
+/* Free every cached workspace (including those a stream has grown out of)
+ * and host-path buffer of this process (synchronises the devices that own
+ * them).  Graphs captured over the library's workspaces must not be replayed
+ * afterwards, and no call may be in flight on another host thread. */
 void topk_release_workspaces(void);
 
 /* Human-readable name of a topk_status code (static string). */
@@ -274,9 +313,10 @@ const char* topk_status_string(int code);
 /* Self-test of failure detection: one thread on `stream` waits, with the
  * kernels' own bounded-wait routine, on a barrier that nothing completes;
  * after limit_ns (1 ns .. 10 s) it gives up and sets TOPK_FLAG_TIMEOUT in the
- * status word, which topk_read_status() returns (and clears, re-arming the
- * kernels' fail-fast flag).  No memory operation is pending meanwhile and the
- * context stays usable.  TOPK_ERR_ARG for a limit outside that range. */
+ * status word, which topk_read_status() returns (and clears).  Its fail-fast
+ * flag is its own, so later calls run normally whether or not the status is
+ * read.  No memory operation is pending meanwhile and the context stays
+ * usable.  TOPK_ERR_ARG for a limit outside that range. */
 int topk_check_wait_timeout(uint64_t limit_ns, struct CUstream_st* stream);
 
 /* Library version as major * 10000 + minor * 100 + patch. */

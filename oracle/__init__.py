@@ -22,6 +22,8 @@ thresholds are pinned by closed forms on strictly monotone rows; the rank rule
 itself (ceil(T * n_s / len)) is a reading of the pages, which do not print it.
 Per-row K (topk_per_row) composes the one-K selection row by row and is
 pinned by brute force on tiny rows and its closed forms (k = 0, k = K_max).
+The ordered output (order) is pinned by a hand-derived golden case, by
+numpy's argsort on rows of distinct values and by its invariants.
 The indexer scores are pinned by a hand-derived case, the one-hot closed form,
 invariances of eq. (1) and exact dense products on tiny integer inputs.
 """
@@ -66,6 +68,8 @@ def _bind(path):
     lib.oracle_index_scores.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, vp, i64, vp, vp,
                                         ctypes.c_int]
     lib.oracle_index_scores.restype = ctypes.c_int
+    lib.oracle_order.argtypes = [vp, vp, i64, i64, i32, vp, vp, ctypes.c_int]
+    lib.oracle_order.restype = ctypes.c_int
     lib.oracle_default_threads.argtypes = []
     lib.oracle_default_threads.restype = ctypes.c_int
     return lib
@@ -192,6 +196,23 @@ def compare(scores, row_lens, K: int, got, threads: int = 0):
     _, _, tied = boundary(scores, row_lens, K, threads)
     mism = np.any(np.sort(got, axis=1) != np.sort(ref, axis=1), axis=1) & ~tied
     return {"check": codes, "tied": tied, "set_mismatch": mism}
+
+
+def order(scores, row_lens, K: int, idx, threads: int = 0) -> np.ndarray:
+    """The ordered form of an [M, K] index result: each row's indices by score,
+    largest first, equal scores by smaller index, -1 sentinels last (the
+    contract leaves the order free; this is the optional ordered output).
+    Raises ValueError if a row holds an index outside its valid prefix."""
+    scores, row_lens = _as_inputs(scores, row_lens)
+    M, N = scores.shape
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    if idx.shape != (M, K):
+        raise ValueError("idx must be [M, K]")
+    out = np.empty((M, K), dtype=np.int32)
+    rc = _load().oracle_order(_p(scores), _p(row_lens), M, N, K, _p(idx), _p(out), threads)
+    if rc != 0:
+        raise ValueError("oracle_order: bad arguments or an index outside its row")
+    return out
 
 
 def clamp_row_k(row_k, K_max: int) -> np.ndarray:

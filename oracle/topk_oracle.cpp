@@ -339,6 +339,46 @@ int oracle_index_scores(const uint16_t* q, const uint16_t* k, const float* w, in
   return 0;
 }
 
+// The optional ordered output.  The contract leaves the order of a Top-K
+// result free (codexqa.cn section "什么叫精确，时间怎么量"; PaperDaily
+// section 问题二: the result is a set, not sorted by score); an ordered
+// result is the same set listed by score, largest first, equal scores by
+// smaller index first, with the -1 sentinel slots last.  in_idx and out_idx
+// are [M][K] int32 (they may be the same array); every entry of in_idx is -1
+// or an index below row_lens[r] (clamped), else the call returns -1 without
+// writing that row's output.  Returns 0, or -1 on bad arguments or a bad
+// index.
+int oracle_order(const float* scores, const int32_t* row_lens, int64_t M, int64_t N_alloc,
+                 int32_t K, const int32_t* in_idx, int32_t* out_idx, int threads) {
+  if (M < 0 || N_alloc < 0 || K < 1) return -1;
+  if (M > 0 && (!scores || !row_lens || !in_idx || !out_idx)) return -1;
+  std::vector<uint8_t> bad((size_t)(M > 0 ? M : 0), 0);
+  parallel_rows(M, threads, [&](int64_t r0, int64_t r1) {
+    std::vector<int32_t> idx;
+    for (int64_t r = r0; r < r1; ++r) {
+      const float* v = scores + r * N_alloc;
+      const int32_t* in = in_idx + r * (int64_t)K;
+      const int64_t L = clamp_len(row_lens[r], N_alloc);
+      idx.clear();
+      for (int64_t i = 0; i < K; ++i) {
+        if (in[i] == -1) continue;
+        if (in[i] < 0 || (int64_t)in[i] >= L) {
+          bad[(size_t)r] = 1;
+          break;
+        }
+        idx.push_back(in[i]);
+      }
+      if (bad[(size_t)r]) continue;
+      std::sort(idx.begin(), idx.end(), Before{v});
+      int32_t* o = out_idx + r * (int64_t)K;
+      for (int64_t i = 0; i < K; ++i) o[i] = i < (int64_t)idx.size() ? idx[(size_t)i] : -1;
+    }
+  });
+  for (int64_t r = 0; r < M; ++r)
+    if (bad[(size_t)r]) return -1;
+  return 0;
+}
+
 // Hardware threads this library uses when threads <= 0 is passed.
 int oracle_default_threads(void) {
   int t = (int)std::thread::hardware_concurrency();

@@ -6,7 +6,8 @@ The pin tests in test_oracle_pins.py are then run against the mutant, and at
 least one of them must fail.  This shows that a plausible slip in the oracle
 (a flipped comparison, a wrong tie-break, an off-by-one in the rank rule, a
 strict/inclusive mix-up in the counts or the checker, a dropped or misplaced
-ReLU or a transposed operand in the indexer scores) would not go unnoticed.
+ReLU or a transposed operand in the indexer scores, a reversed or index-keyed
+ordered output) would not go unnoticed.
 """
 import os
 import subprocess
@@ -16,6 +17,7 @@ import pytest
 import oracle
 from oracle import build as obuild
 from tests import test_oracle_index_scores as score_pins
+from tests import test_oracle_order as order_pins
 from tests import test_oracle_pins as pins
 
 MUTANTS = {
@@ -36,6 +38,15 @@ MUTANTS = {
     "score_w_transposed": ("const double wj = (double)w[t * H + j];", "const double wj = (double)w[j * T + t];"),
     "score_k_wrong_row": ("bf16_to_double(k[sidx * D + d]);", "bf16_to_double(k[t * D + d]);"),
     "score_magnitude_signed": ("mag += std::fabs(wj) * adot;", "mag += wj * adot;"),
+    "order_reversed": ("std::sort(idx.begin(), idx.end(), Before{v});",
+                       "std::sort(idx.begin(), idx.end(), [&](int32_t a, int32_t b) "
+                       "{ return Before{v}(b, a); });"),
+    "order_by_index": ("std::sort(idx.begin(), idx.end(), Before{v});",
+                       "std::sort(idx.begin(), idx.end());"),
+    "order_sentinels_first": (
+        "for (int64_t i = 0; i < K; ++i) o[i] = i < (int64_t)idx.size() ? idx[(size_t)i] : -1;",
+        "for (int64_t i = 0; i < K; ++i) o[i] = i < K - (int64_t)idx.size() ? -1 : "
+        "idx[(size_t)(i - (K - (int64_t)idx.size()))];"),
 }
 
 
@@ -62,6 +73,10 @@ def _run_all_pins():
     score_pins.test_one_hot_closed_form()
     score_pins.test_invariances()
     score_pins.test_dense_product_tiny()
+    for case in order_pins.ORDER_CASES:
+        order_pins.test_golden_order_cases(case)
+    order_pins.test_distinct_values_follow_argsort()
+    order_pins.test_invariants_on_tied_rows()
 
 
 def test_unmutated_oracle_passes_every_pin():

@@ -168,30 +168,6 @@ def test_rows_longer_than_the_matrix(params, kind):
     del x
 
 
-def test_full_size_1m_by_8192_sampled_rows(ets):
-    """The benchmark's configuration (1M columns, 8192 causal rows, default
-    dispatch); the oracle checks 48 sampled rows one by one."""
-    N, M = 1048576, 8192
-    plan = ets.plan(M, N, K)
-    lens = synth.causal_lens(N, M, 0)
-    x = synth.indexer_rows(lens, N, seed=7, device=DEV)
-    got, dg = run(ets, x, lens, diag=True)
-    g = torch.Generator().manual_seed(3)
-    rows = torch.cat([torch.tensor([0, M - 1]), torch.randperm(M, generator=g)[:46]])
-    rows = rows.sort().values
-    verify(x, lens, K, got, rows=rows)
-    verify_diag(ets, x, lens, K, dg, rows=rows.numpy(),
-                sample_min_len=ets.get_params()["sample_min_len"])
-    # every row: K distinct indices inside its prefix (property that holds at any size)
-    gs = got.sort(dim=1).values
-    assert bool((gs[:, 0] >= 0).all())
-    assert bool((gs[:, 1:] != gs[:, :-1]).all())
-    assert bool((gs[:, -1] < lens.to(DEV)).all())
-    assert plan["kind"] == "persistent"
-    assert not np.any(dg["flags"] & (ets.FLAG_INTERNAL | ets.FLAG_TIMEOUT))
-    del x
-
-
 # ------------------------------------------------------------------ config 4
 @pytest.mark.parametrize("N", [16384, 24576, 32768, 40960, 49152, 57344, 65536])
 @pytest.mark.parametrize("M", [64, 512])

@@ -1,10 +1,12 @@
 """The optional ordering pass (GPU only): each row of a Top-K result sorted
 by score, largest first, equal scores by index, -1 sentinels last.  The set
-is unchanged; the order is checked against a sort on the CPU."""
+is unchanged; the order must equal the oracle's ordered output (oracle.order)
+of the same set, entry by entry."""
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from exact_top_sparse_gb300 import synth
 from tests.test_parity_gpu import verify
 
@@ -21,12 +23,6 @@ def ets():
     return m
 
 
-def expected_order(xh, idx_row):
-    valid = idx_row[idx_row >= 0]
-    order = np.lexsort((valid, -xh[valid].astype(np.float64)))
-    return np.concatenate([valid[order], np.full(idx_row.size - valid.size, -1, np.int32)])
-
-
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("K", [1, 7, 2048, 3000, 4096])
 def test_sorted_rows(ets, dtype, K):
@@ -41,9 +37,8 @@ def test_sorted_rows(ets, dtype, K):
     xf = x.float()
     verify(xf, lens, K, got)
     assert torch.equal(got.sort(dim=1).values, before.sort(dim=1).values)
-    xh, gh = xf.cpu().numpy(), got.cpu().numpy()
-    for r in range(M):
-        assert np.array_equal(gh[r], expected_order(xh[r], gh[r])), r
+    want = oracle.order(xf.cpu().numpy(), lens.numpy(), K, before.cpu().numpy())
+    assert np.array_equal(got.cpu().numpy(), want)
 
 
 def test_sort_argument_errors(ets):
