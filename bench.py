@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--M", type=int, default=8192)
     ap.add_argument("--K", type=int, default=K_DEFAULT)
     ap.add_argument("--no-matrix", action="store_true", help="skip the 20-shape operator matrix")
+    ap.add_argument("--no-ablation", action="store_true",
+                    help="skip the sampled-vs-exact proposal ablation and the rho / stride sweep")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--dtype", default="f32", choices=["f32", "bf16", "e4m3"],
                     help="score type of the timed rows (the headline is f32)")
@@ -109,11 +111,204 @@ def measured_bf16_tflops():
     return 1900.0, "fallback"
 
 
+# The pages' timing protocol (codexqa.cn, section "什么叫精确，时间怎么量"):
+# CUDA-graph replays, timed per call with CUDA events on the stream, median
+# per call after warm-up and conditioning replays; mechanism runs take 10
+# warm-up replays, 2 blocks of 50 conditioning replays and 7 rounds of 100
+# timed replays rotated over the shape's groups.
+PROTOCOL = {"warmup": 10, "condition": (2, 50), "rounds": 7, "per_round": 100}
+
+
+def capture_graphs(stream, calls):
+    """One CUDA graph per zero-argument call (each enqueues its launches on
+    the current stream), captured on `stream` after one eager run of every
+    call (which creates the library's workspace before any capture)."""
+    with torch.cuda.stream(stream):
+        for fn in calls:
+            fn()
+    stream.synchronize()
+    graphs = []
+    for fn in calls:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        graphs.append(g)
+    stream.synchronize()
+    return graphs
+
+
+def replay_median(stream, graphs, warmup, condition, rounds, per_round):
+    """Median device time (ms) of one replay: `warmup` replays, then
+    condition[0] blocks of condition[1] replays, then `rounds` rounds of
+    `per_round` timed replays; every replay takes the next graph in turn."""
+    n = len(graphs)
+    k = 0
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            graphs[k % n].replay()
+            k += 1
+        for _ in range(condition[0]):
+            for _ in range(condition[1]):
+                graphs[k % n].replay()
+                k += 1
+            stream.synchronize()
+    times = []
+    for _ in range(rounds):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(per_round)]
+        with torch.cuda.stream(stream):
+            for a, b in evs:
+                a.record(stream)
+                graphs[k % n].replay()
+                b.record(stream)
+                k += 1
+        stream.synchronize()
+        times += [a.elapsed_time(b) for a, b in evs]
+    return statistics.median(times), len(times)
+
+
+def operator_matrix_leg(ets, dev, stream, peak, K, inputs_1m=None):
+    """The pages' operator matrix (codexqa.cn, section "20 个形状都最快"):
+    widths 128K-1M x M in {512 .. 8192}; each width's last 8192 causal rows
+    are cut into non-overlapping groups of M rows, every group is captured as
+    one graph, and the shape's latency is the median per call over the
+    protocol's replays rotated across the groups."""
+    mat = {}
+    for w in (131072, 262144, 524288, 1048576):
+        if w == 1048576 and inputs_1m is not None:
+            xw, lw = inputs_1m
+        else:
+            xw, lw = make_inputs(w, 8192, 0, seed=11, device=dev)
+        dlw = lw.to(dev)
+        outw = torch.empty((8192, K), dtype=torch.int32, device=dev)
+        for m in (512, 1024, 2048, 4096, 8192):
+            ng = 8192 // m
+            calls = [(lambda g0=g0: ets.topk_ragged(xw[g0:g0 + m], dlw[g0:g0 + m], K,
+                                                    out=outw[g0:g0 + m]))
+                     for g0 in range(0, 8192, m)]
+            graphs = capture_graphs(stream, calls)
+            ms, n = replay_median(stream, graphs, **PROTOCOL)
+            del graphs
+            vb = 4.0 * float(lw.to(torch.int64).sum()) / ng  # mean valid bytes of a group
+            gbps = vb / (ms / 1000.0) / 1e9
+            mat["%dx%d" % (w, m)] = {"ms": ms, "rows_per_s": m / (ms / 1000.0), "gbps": gbps,
+                                     "frac": gbps / peak, "path": ets.plan(m, w, K)["kind"],
+                                     "groups": ng, "replays_timed": n,
+                                     "protocol": "graph-replay median"}
+        del xw, lw, dlw, outw
+        ets.release_workspaces()
+        torch.cuda.empty_cache()
+    return mat
+
+
+def proposal_ablation_leg(ets, dev, stream, peak, K):
+    """Sampled proposal against the exact one, the selector otherwise
+    unchanged (codexqa.cn, section "采样不是处处都该开"): the exact form
+    serves every row on the library's exact path (a histogram pass over the
+    whole row, then refinement passes), which is what a selector without a
+    sampled proposal has to do to find its boundary.  Graph replays, median
+    per call (3 warm-up, 2 x 20 conditioning, 3 x 40 timed)."""
+    from exact_top_sparse_gb300 import synth
+    res = {}
+    for w, m, gi in ((131072, 2048, 1), (1048576, 1024, 3)):
+        lens = synth.causal_lens(w, m, gi)
+        x = synth.indexer_rows(lens, w, seed=23, device=dev)
+        dl = lens.to(dev)
+        o = torch.empty((m, K), dtype=torch.int32, device=dev)
+        vb = 4.0 * float(lens.to(torch.int64).sum())
+        cell = {}
+        old = ets.get_params()
+        try:
+            for name, kw in (("sampled", {}), ("exact", {"sample_min_len": w + 1})):
+                ets.set_params(**kw)
+                graphs = capture_graphs(stream, [lambda: ets.topk_ragged(x, dl, K, out=o)])
+                ms, _ = replay_median(stream, graphs, 3, (2, 20), 3, 40)
+                del graphs
+                with torch.cuda.stream(stream):
+                    _, dg = ets.topk_ragged_diag(x, dl, K, stream=stream)
+                cell[name] = {"ms": ms, "gbps": vb / (ms / 1000.0) / 1e9,
+                              "frac": vb / (ms / 1000.0) / 1e9 / peak,
+                              "row_paths": path_counts(ets, dg)}
+                ets.set_params(**old)
+        finally:
+            ets.set_params(**old)
+        cell["exact_over_sampled"] = cell["exact"]["ms"] / cell["sampled"]["ms"]
+        res["%dx%d" % (w, m)] = cell
+        del x, o
+        ets.release_workspaces()
+        torch.cuda.empty_cache()
+    return res
+
+
+def sampling_sweep_leg(ets, dev, stream, K):
+    """Primary targets rho0 and strides s swept with the selector unchanged
+    (codexqa.cn, section "采样不是处处都该开": rho = 1 leaves about a third of
+    the rows to recovery, 1.25K 5.7-7.8 %, 1.5K under 1 %; at 1.5K, s = 16
+    recovers almost nothing, s = 64 under 0.01 %, s = 128 under 0.9 %,
+    s = 256 2.48-3.26 %; H20, captured Hy4-Preview rows).  Every row uses
+    the swept values (no long tier); rho1 = rho0 + 0.25.  Per cell: the
+    primary miss rate (rows with C(tau0) < K: served by tau1 or recovery),
+    the exact-recovery rate (C(tau1) < K) and the median of 5 calls."""
+    from exact_top_sparse_gb300 import synth
+    res = {"pages_context": {"rho_1.0": "~1/3", "rho_1.25": "5.7-7.8 %", "rho_1.5": "< 1 %",
+                             "s_16": "~0", "s_64": "< 0.01 %", "s_128": "< 0.9 %",
+                             "s_256": "2.48-3.26 %"}}
+    cells = [(128, r_) for r_ in (1.0, 1.25, 1.5, 1.75, 2.0)] + \
+            [(s_, 1.5) for s_ in (16, 64, 256, 512)]
+    for w, m in ((131072, 2048), (1048576, 1024)):
+        lens = synth.causal_lens(w, m, 0)
+        x = synth.indexer_rows(lens, w, seed=29, device=dev)
+        dl = lens.to(dev)
+        o = torch.empty((m, K), dtype=torch.int32, device=dev)
+        old = ets.get_params()
+        out = {}
+        try:
+            for s_, r_ in cells:
+                ets.set_params(stride=s_, rho0=r_, rho1=r_ + 0.25, long_len=0)
+                with torch.cuda.stream(stream):
+                    _, dg = ets.topk_ragged_diag(x, dl, K, stream=stream)
+                    ts = []
+                    for _ in range(6):
+                        a = torch.cuda.Event(enable_timing=True)
+                        b = torch.cuda.Event(enable_timing=True)
+                        a.record(stream)
+                        ets.topk_ragged(x, dl, K, out=o, stream=stream)
+                        b.record(stream)
+                        ts.append((a, b))
+                stream.synchronize()
+                ms = statistics.median([a.elapsed_time(b) for a, b in ts[1:]])
+                pc = path_counts(ets, dg)
+                sampled = pc["tau0"] + pc["tau1"] + pc["recovery"]
+                out["s%d_rho%.2f" % (s_, r_)] = {
+                    "stride": s_, "rho0": r_, "rho1": r_ + 0.25, "ms": ms,
+                    "primary_miss_rate": (pc["tau1"] + pc["recovery"]) / max(1, sampled),
+                    "exact_recovery_rate": pc["recovery"] / max(1, sampled),
+                    "overflow_rows": pc["overflow"], "sampled_rows": sampled}
+        finally:
+            ets.set_params(**old)
+        res["%dx%d" % (w, m)] = out
+        del x, o
+        torch.cuda.empty_cache()
+    return res
+
+
+def path_counts(ets, dg):
+    """Rows per path (and rows that overflowed) of one call's diagnostics."""
+    paths = {name: int((dg["path"] == code).sum()) for name, code in
+             (("sentinel", 0), ("direct", 1), ("tau0", 2), ("tau1", 3), ("recovery", 4))}
+    paths["overflow"] = int(((dg["flags"] & ets.FLAG_OVERFLOW) != 0).sum())
+    return paths
+
+
 def trace_leg(ets, dev, stream, tokens=430 * 1024, K=2048):
     """Replay the Top-K calls of one synthetic prefill (exact_top_sparse_gb300.trace):
     first the selector alone over indexer-like score rows of each call's shape,
-    then the whole score -> select chain; each timed as one sequence of calls
-    with CUDA events on the launching stream, after one untimed pass."""
+    then the whole score -> select chain.  As the pages report a trace (codexqa.cn,
+    section "什么叫精确，时间怎么量": trace latency is the sum of per-call medians),
+    every call is captured as a CUDA graph and timed by replays (selector: 3
+    warm-up, 20 timed; chain: 2 warm-up, 5 timed), and the totals are the sums
+    of the per-call medians.  The whole sequence of eager calls is also timed
+    once (`*_sequence_ms`)."""
     from exact_top_sparse_gb300 import synth, trace
     calls = trace.calls(tokens)
     W = trace.WORKSPACE_FLOATS
@@ -142,7 +337,8 @@ def trace_leg(ets, dev, stream, tokens=430 * 1024, K=2048):
                                 out=outs[:c.rows], stream=stream)
 
     res = {"tokens": tokens, "calls": len(calls), "steps": len({c.step for c in calls}),
-           "workspace_floats": W, "valid_score_bytes": valid}
+           "workspace_floats": W, "valid_score_bytes": valid,
+           "protocol": "sum of per-call graph-replay medians"}
     for name, fn in (("topk", run_topk), ("chain", run_chain)):
         with torch.cuda.stream(stream):
             fn()
@@ -154,7 +350,27 @@ def trace_leg(ets, dev, stream, tokens=430 * 1024, K=2048):
             fn()
             b.record(stream)
         stream.synchronize()
-        res[name + "_total_ms"] = a.elapsed_time(b)
+        res[name + "_sequence_ms"] = a.elapsed_time(b)
+
+    def one_topk(c):
+        return lambda: ets.topk_ragged(buf[:c.rows * c.width].view(c.rows, c.width),
+                                       lens_all[c.row0:c.row0 + c.rows], K, out=outs[:c.rows])
+
+    def one_chain(c):
+        return lambda: ets.topk_index_topk(
+            q[c.row0:c.row0 + c.rows], k[:c.width], w[c.row0:c.row0 + c.rows],
+            lens_all[c.row0:c.row0 + c.rows], K,
+            scores=buf[:c.rows * c.width].view(c.rows, c.width), out=outs[:c.rows])
+
+    for name, make, reps in (("topk", one_topk, (3, 20)), ("chain", one_chain, (2, 5))):
+        medians = []
+        for c in calls:
+            g = capture_graphs(stream, [make(c)])
+            ms, _ = replay_median(stream, g, reps[0], (0, 0), 1, reps[1])
+            medians.append(ms)
+            del g
+        res[name + "_total_ms"] = sum(medians)
+        res[name + "_call_medians_ms"] = [round(v, 4) for v in medians]
     res["topk_gbps"] = valid / (res["topk_total_ms"] / 1000.0) / 1e9
     res["score_flops_dense"] = flops
     res["chain_score_share_ms"] = res["chain_total_ms"] - res["topk_total_ms"]
@@ -498,9 +714,7 @@ def run_gb300(args):
     # per-row paths of one (untimed) call with diagnostics
     with torch.cuda.stream(stream):
         _, dg = ets.topk_ragged_diag(x, d_lens, K)
-    paths = {name: int((dg["path"] == code).sum()) for name, code in
-             (("sentinel", 0), ("direct", 1), ("tau0", 2), ("tau1", 3), ("recovery", 4))}
-    paths["overflow"] = int(((dg["flags"] & ets.FLAG_OVERFLOW) != 0).sum())
+    paths = path_counts(ets, dg)
 
     result = {
         "metric": METRIC, "value": rows_per_s, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -537,55 +751,24 @@ def run_gb300(args):
         result["spot_check"] = {"rows": 8, "contract_failures": int((v["check"] != 0).sum()),
                                 "set_mismatches": int(v["set_mismatch"].sum())}
 
-    # the operator matrix (informational): widths 128K-1M x M in {512..8192},
-    # causal groups of M rows of the last 8192; per shape the median over
-    # groups (up to 4, spread over the window) of the median of 5 calls
+    # the operator matrix (informational) with the pages' timing protocol,
+    # then the proposal ablation and the sampling sweep
     full_f32 = args.dtype == "f32" and N == 1048576 and M == 8192
     if not args.no_matrix and rank == 0 and full_f32:
         del out
         torch.cuda.empty_cache()
-        mat = {}
-        for w in (131072, 262144, 524288, 1048576):
-            if w == N:
-                xw, lw = x, lens
-            else:
-                xw, lw = make_inputs(w, 8192, 0, seed=11, device=dev)
-            for m in (512, 1024, 2048, 4096, 8192):
-                groups = sorted({0, (8192 // m) // 3, (2 * (8192 // m)) // 3, 8192 // m - 1})
-                per_group = []
-                vb = 0.0
-                for gi in groups:
-                    xs = xw[gi * m:(gi + 1) * m]
-                    ls = lw[gi * m:(gi + 1) * m]
-                    dls = ls.to(dev)
-                    vb += 4.0 * float(ls.to(torch.int64).sum())
-                    o = torch.empty((m, K), dtype=torch.int32, device=dev)
-                    with torch.cuda.stream(stream):
-                        for _ in range(2):
-                            ets.topk_ragged(xs, dls, K, out=o, stream=stream)
-                    ts = []
-                    for _ in range(5):
-                        a0 = torch.cuda.Event(enable_timing=True)
-                        b0 = torch.cuda.Event(enable_timing=True)
-                        with torch.cuda.stream(stream):
-                            a0.record(stream)
-                            ets.topk_ragged(xs, dls, K, out=o, stream=stream)
-                            b0.record(stream)
-                        stream.synchronize()
-                        ts.append(a0.elapsed_time(b0))
-                    per_group.append(statistics.median(ts))
-                ms = statistics.median(per_group)
-                gbps = vb / len(groups) / (ms / 1000.0) / 1e9
-                mat["%dx%d" % (w, m)] = {"ms": ms, "rows_per_s": m / (ms / 1000.0), "gbps": gbps,
-                                         "frac": gbps / peak, "path": ets.plan(m, w, K)["kind"],
-                                         "groups": len(groups)}
-            if w != N:
-                del xw
-            torch.cuda.empty_cache()
-        result["operator_matrix"] = mat
+        result["operator_matrix"] = operator_matrix_leg(ets, dev, stream, peak, K,
+                                                        inputs_1m=(x, lens))
         del x
         x = None
         torch.cuda.empty_cache()
+    if not args.no_ablation and rank == 0 and full_f32:
+        if x is not None:
+            del x
+            x = None
+            torch.cuda.empty_cache()
+        result["proposal_ablation"] = proposal_ablation_leg(ets, dev, stream, peak, K)
+        result["sampling_sweep"] = sampling_sweep_leg(ets, dev, stream, K)
 
     if not args.no_narrow and rank == 0 and full_f32:
         if x is not None:

@@ -37,6 +37,9 @@ constexpr int64_t kKvSegmentTarget = 262144;
 std::mutex g_mu;
 topk_params g_params;
 bool g_params_init = false;
+// L2 prefetch distances of the full-row pass (see tk::Params).
+uint32_t g_knob_pf_ahead = 0;
+uint32_t g_knob_pf_next_bytes = 0;
 
 struct DevInfo {
   bool ready = false;
@@ -210,6 +213,8 @@ tk::Params kernel_params(int64_t M, int64_t N, int32_t K, const topk_params& p, 
   P.rho1 = p.rho1;
   P.long_rho0 = p.long_rho0;
   P.long_rho1 = p.long_rho1;
+  P.pf_ahead = g_knob_pf_ahead;
+  P.pf_next_bytes = g_knob_pf_next_bytes;
   return P;
 }
 
@@ -633,5 +638,16 @@ const char* topk_status_string(int code) {
 }
 
 int topk_version(void) { return kVersion; }
+
+#ifdef TOPK_PHASE_TIMING
+// Tuning hook of a build with -DTOPK_PHASE_TIMING: sets the L2 prefetch
+// distances of the full-row pass (chunks ahead of the ring, bytes of the next
+// row).  Not thread-safe with calls in flight.
+int topk_debug_set_prefetch(uint32_t ahead_chunks, uint32_t next_bytes) {
+  g_knob_pf_ahead = ahead_chunks;
+  g_knob_pf_next_bytes = next_bytes & ~15u;
+  return TOPK_OK;
+}
+#endif
 
 }  // extern "C"

@@ -184,6 +184,12 @@ __device__ __forceinline__ void prefetch_l2_keep(const void* p) {
   asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));
 }
 
+// Bulk prefetch of [src, src + bytes) into L2 (no data to the CTA; src
+// 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // 1-D bulk copy global -> shared, completion counted on `bar` (bytes % 16 == 0,
 // both addresses 16-byte aligned).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
@@ -228,7 +234,27 @@ struct __align__(16) Shared {
   uint32_t last;
   uint32_t next, next_ok;        // a row claimed ahead of time (persistent kernel)
   uint32_t neq;                  // scores equal to tau1 (counts past the tie list)
+#ifdef TOPK_PHASE_TIMING
+  unsigned long long ph[12];     // cycles per phase of the persistent kernel (thread 0's clock)
+  long long ph_t;                // thread 0's clock at the last mark
+#endif
 };
+
+// Phase timing, compiled only with -DTOPK_PHASE_TIMING: thread 0 adds the
+// cycles since its previous mark to phase i.  Marks sit right after a block
+// barrier, so thread 0's clock stands for the whole block there.
+__device__ __forceinline__ void phase_mark(Shared& S, int i) {
+#ifdef TOPK_PHASE_TIMING
+  if (threadIdx.x == 0) {
+    const long long t = clock64();
+    S.ph[i] += (unsigned long long)(t - S.ph_t);
+    S.ph_t = t;
+  }
+#else
+  (void)S;
+  (void)i;
+#endif
+}
 
 // Exclusive prefix sum over all THREADS threads (every thread must call).
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, Shared& S, uint32_t* total) {
@@ -426,6 +452,7 @@ struct Ring {
   uint32_t seq;
   uint64_t policy;
   uint32_t* abort;  // fail-fast flag of the launch's work (see mbar_wait_slow)
+  uint32_t pf_ahead;  // chunks ahead of the ring a certify pass prefetches into L2
 };
 
 __device__ __forceinline__ void ring_init(Ring& R, Shared& S, float* buf, uint32_t* abort) {
@@ -435,6 +462,7 @@ __device__ __forceinline__ void ring_init(Ring& R, Shared& S, float* buf, uint32
   R.seq = 0;
   R.policy = l2_policy_evict_first();
   R.abort = abort;
+  R.pf_ahead = 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&S.full[s], 1);
@@ -464,6 +492,23 @@ __device__ __forceinline__ void ring_issue(Ring& R, const E* __restrict__ row, i
 // The 16-byte aligned body [a0, a1) of [start, end) and its chunk count.
 template <class E>
 __device__ __forceinline__ uint32_t ring_span(const E* row, int64_t start, int64_t end,
+                                              int64_t* a0, int64_t* a1);
+
+// L2 prefetch of the first max_bytes of the 16-byte aligned body of row
+// [0, len) (one bulk prefetch; nothing past len is touched).
+template <class E>
+__device__ __forceinline__ void prefetch_row_head(const E* row, int64_t len, uint32_t max_bytes) {
+  int64_t a0, a1;
+  ring_span(row, 0, len, &a0, &a1);
+  int64_t n = a1 - a0;
+  if (n > (int64_t)(max_bytes / Elem<E>::kSize)) n = (int64_t)(max_bytes / Elem<E>::kSize);
+  const uint32_t bytes = (uint32_t)(n * Elem<E>::kSize) & ~15u;
+  if (bytes) bulk_prefetch_l2(row + a0, bytes);
+}
+
+// The 16-byte aligned body [a0, a1) of [start, end) and its chunk count.
+template <class E>
+__device__ __forceinline__ uint32_t ring_span(const E* row, int64_t start, int64_t end,
                                               int64_t* a0, int64_t* a1) {
   constexpr int P16 = Elem<E>::kPer16;
   constexpr int64_t CE = CHUNK_BYTES / Elem<E>::kSize;
@@ -486,8 +531,17 @@ __device__ __forceinline__ uint32_t ring_prime(Ring& R, const E* __restrict__ ro
   int64_t a0, a1;
   const uint32_t nchunks = ring_span(row, start, end, &a0, &a1);
   const uint32_t n = nchunks < (uint32_t)STAGES ? nchunks : (uint32_t)STAGES;
-  if (threadIdx.x == 0)
+  if (threadIdx.x == 0) {
     for (uint32_t c = 0; c < n; ++c) ring_issue(R, row, a0, a1, c, lflags);
+    // and the next pf_ahead chunks into L2, which the pass would ask for
+    // first (scan_pass then starts its own prefetches past them)
+    constexpr int64_t CE = CHUNK_BYTES / Elem<E>::kSize;
+    if (R.pf_ahead > 0 && n < nchunks) {
+      const int64_t p0 = a0 + (int64_t)n * CE;
+      const int64_t p1 = min(a1, a0 + (int64_t)(n + R.pf_ahead) * CE);
+      bulk_prefetch_l2(row + p0, (uint32_t)((p1 - p0) * Elem<E>::kSize));
+    }
+  }
   return n;
 }
 
@@ -757,8 +811,24 @@ __device__ __forceinline__ void scan_pass(Ring& R, const E* __restrict__ row, in
   int64_t a0, a1;
   const uint32_t nchunks = ring_span(row, start, end, &a0, &a1);
   if (warp == 0) {
-    if (lane == 0)
-      for (uint32_t c = primed; c < nchunks; ++c) ring_issue(R, row, a0, a1, c, lflags);
+    if (lane == 0) {
+      // chunks [primed, primed + D) in one L2 prefetch, then chunk c + D as
+      // chunk c is issued: D chunks of the row stay requested beyond the ring
+      const uint32_t D = R.pf_ahead;
+      if (D > 0 && primed == 0 && primed < nchunks) {
+        const int64_t p0 = a0 + (int64_t)primed * CE;
+        const int64_t p1 = min(a1, a0 + (int64_t)(primed + D) * CE);
+        bulk_prefetch_l2(row + p0, (uint32_t)((p1 - p0) * Elem<E>::kSize));
+      }
+      for (uint32_t c = primed; c < nchunks; ++c) {
+        if (D > 0 && c + D < nchunks) {
+          const int64_t p0 = a0 + (int64_t)(c + D) * CE;
+          const int64_t p1 = min(a1, p0 + CE);
+          bulk_prefetch_l2(row + p0, (uint32_t)((p1 - p0) * Elem<E>::kSize));
+        }
+        ring_issue(R, row, a0, a1, c, lflags);
+      }
+    }
   } else {
     if (warp == 1) {
       // head [start, a0) on lanes 0.., tail [a1, end) on lanes 16..
@@ -1237,6 +1307,7 @@ __device__ void sample_thresholds(const E* __restrict__ row, int64_t len, int32_
   }
   uint32_t kmin, kmax;
   block_minmax(mn, mx, S, &kmin, &kmax);
+  phase_mark(S, 8);
   uint32_t key1, key0;
   if (on_chip) {
     select_two_ranks(skeys, (uint32_t)ns, (uint32_t)r0, (uint32_t)r1, kmin, kmax, hist, list, S,

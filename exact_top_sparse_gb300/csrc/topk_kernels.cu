@@ -26,6 +26,16 @@ namespace tk {
 
 __device__ uint32_t g_status;  // OR of row flags since the last read
 
+#ifdef TOPK_PHASE_TIMING
+// Cycles per phase of k_persistent summed over its CTAs (thread 0's clock):
+// 0 row claim, 8 first chunks and sample loads, 1 rank selection of the
+// sample, 2 certify+collect pass, 3 tally, 4 next-row claim and prefetches,
+// 5 selection after the pass, 6 closing the row, 7 rows served without
+// sampling.
+constexpr int NPHASE = 12;
+__device__ unsigned long long g_phase[NPHASE];
+#endif
+
 // Sampling stride and targets of a row of `len` elements.
 struct SampleSpec {
   int32_t stride;
@@ -259,8 +269,11 @@ __device__ uint32_t scan_collect(const E* row, int64_t s0, int64_t s1, Ring& R,
     scan_pass(R, row, s0, s1, f, lflags, primed);
   }
   __syncthreads();
+  phase_mark(S, 2);
   const uint32_t c0 = tally_candidates(c.cand, spill, min(S.ncand, cap), key0, sb, c.hist);
-  return block_sum(c0, S);
+  const uint32_t total = block_sum(c0, S);
+  phase_mark(S, 3);
+  return total;
 }
 
 // Emits out[] entries for indices src(j), j < n (every thread calls).
@@ -402,9 +415,14 @@ __global__ void __launch_bounds__(THREADS, 2)
   if (threadIdx.x == 0) {
     S.flags = 0;
     S.next_ok = 0;
+#ifdef TOPK_PHASE_TIMING
+    for (int i = 0; i < NPHASE; ++i) S.ph[i] = 0;
+    S.ph_t = clock64();
+#endif
   }
   Ring R;
   ring_init(R, S, c.ring, hdr + 2);  // hdr[2]: this launch's fail-fast flag
+  R.pf_ahead = P.pf_ahead;
   const int32_t K = P.K;
   for (;;) {
     if (threadIdx.x == 0) {
@@ -414,6 +432,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     __syncthreads();
     const int64_t r = S.row;
     __syncthreads();
+    phase_mark(S, 0);
     if (r >= P.M) break;
     uint32_t lflags = 0;
     const int64_t len = clamp_len(row_lens[r], P.N_alloc, lflags);
@@ -427,12 +446,14 @@ __global__ void __launch_bounds__(THREADS, 2)
       write_sentinel_row(out, K0, len);
       if (threadIdx.x == 0) S.nout = (uint32_t)K0;
       finish_row(S, out, K0, K, lflags, diag, r, PATH_SENTINEL, qnan, qnan, 0, 0);
+      phase_mark(S, 7);
       continue;
     }
     if (len < P.sample_min_len) {
       if (fits_stage<E>(len)) exact_row_staged(row, len, out, K0, c, lflags);
       else exact_row_stream(row, len, out, K0, R, c, lflags);
       finish_row(S, out, K0, K, lflags, diag, r, PATH_DIRECT, qnan, qnan, 0, 0);
+      phase_mark(S, 7);
       continue;
     }
     // the ring is idle: start the row's first chunks before sampling it
@@ -442,6 +463,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       sample_thresholds(row, len, sp.stride, sp.target0, sp.target1,
                         reinterpret_cast<uint32_t*>(c.cand), c.hist, c.list, S);
     }
+    phase_mark(S, 1);
     const uint32_t key0 = S.key0, key1 = S.key1, kmin = S.kmin, kmax = S.kmax;
     const Bins sb = scan_bins(key1, kmax);
     __syncthreads();
@@ -468,19 +490,29 @@ __global__ void __launch_bounds__(THREADS, 2)
         uint32_t fl = 0;
         const int64_t ln = clamp_len(row_lens[rn], P.N_alloc, fl);
         const int32_t kn = row_k_of(P, rn, fl);
-        if (ln > kn && kn > 0 && ln >= P.sample_min_len)
+        if (ln > kn && kn > 0 && ln >= P.sample_min_len) {
           warm_samples(scores + rn * P.N_alloc, ln, sample_spec(P, ln, kn).stride);
+          if (threadIdx.x == 0 && P.pf_next_bytes)
+            prefetch_row_head(scores + rn * P.N_alloc, ln, P.pf_next_bytes);
+        }
       }
     }
+    phase_mark(S, 4);
     // the row's K and sampling spec again, rather than held in registers
     // over the scan
     const int32_t Kr = row_k_of(P, r, lflags);
     const int32_t path =
         select_after_scan(row, len, out, Kr, R, c, spill, ties, sample_spec(P, len, Kr), C0, Cgt,
                           Ceq, Cgt > (uint32_t)CAP_ALL, key0, key1, kmin, sb, lflags);
+    phase_mark(S, 5);
     finish_row(S, out, Kr, K, lflags, diag, r, path, key_to_float(key0), key_to_float(key1), C0,
                Cgt + Ceq);
+    phase_mark(S, 6);
   }
+#ifdef TOPK_PHASE_TIMING
+  if (threadIdx.x == 0)
+    for (int i = 0; i < NPHASE; ++i) atomicAdd(&g_phase[i], S.ph[i]);
+#endif
   ring_drain(R);
   // The last CTA to leave resets the queue and the fail-fast flag, so the
   // next launch (or graph replay) on this workspace starts from zero without
@@ -645,6 +677,7 @@ __global__ void __launch_bounds__(THREADS, 2)
   }
   Ring R;
   ring_init(R, S, c.ring, &h->abort);
+  R.pf_ahead = P.pf_ahead;
   uint32_t lflags = 0;
   const Bins sb = scan_bins(key1, kmax);
   if (mode == 2) {
@@ -867,3 +900,17 @@ cudaError_t read_and_clear_status(cudaStream_t st, uint32_t* flags) {
 }
 
 }  // namespace tk
+
+#ifdef TOPK_PHASE_TIMING
+// Reads (and with reset != 0 clears) the phase cycle sums of k_persistent on
+// the current device.  Exported only by a build with -DTOPK_PHASE_TIMING.
+extern "C" int topk_debug_phase_cycles(unsigned long long* out, int reset) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return -4;
+  if (cudaMemcpyFromSymbol(out, tk::g_phase, sizeof(tk::g_phase)) != cudaSuccess) return -4;
+  if (reset) {
+    static const unsigned long long zero[tk::NPHASE] = {};
+    if (cudaMemcpyToSymbol(tk::g_phase, zero, sizeof(zero)) != cudaSuccess) return -4;
+  }
+  return 0;
+}
+#endif

@@ -28,6 +28,12 @@ struct Params {
   // of its sampling tier; the output row stride stays K.
   const int32_t* row_k;
   float rho0, rho1, long_rho0, long_rho1;
+  // L2 prefetch of the row a full-row pass streams: the producer keeps
+  // pf_ahead chunks ahead of its shared-memory ring prefetched into L2 (0:
+  // none), and a persistent CTA prefetches the first pf_next_bytes of the
+  // row it takes next as soon as its current row's pass ends (0: none).
+  uint32_t pf_ahead;
+  uint32_t pf_next_bytes;
 };
 
 // Same layout as topk_row_diag in the public header.

@@ -3,12 +3,24 @@
 The kernel evaluates eq. (1) of the xllm-io LiteTopK review ("核心公式"),
 I[t][s] = sum_j w[t][j] * ReLU(q[t][j] . k[s]), from bfloat16 q and k with
 FP32 accumulation; the oracle evaluates the same sums in double from the
-same bfloat16 values.  Tolerance (derived in the design notes): FP32
-accumulation of the 128 products of each head (in an order the tensor core
-chooses) and of the 64 weighted heads errs by at most a few units of 2^-24
-per term, so |gpu - oracle| <= 2^-14 * M + 1e-30 with
-M = sum_j |w_tj| * sum_d |q_tjd * k_sd| leaves a wide margin.  The causal
-suffix (s >= row_lens[t]) must be exactly -inf.  The chained Top-K is exact
+same bfloat16 values.
+
+Tolerance.  Let M = sum_j |w_tj| * sum_d |q_tjd * k_sd| and u = 2^-24 (FP32
+unit roundoff).  Each product q_tjd * k_sd of two bfloat16 values (8
+significant bits each) is exact in FP32.  Recursive FP32 summation of the 128
+products of a head errs by at most 127 rounding errors, each no larger than
+the running sum of magnitudes: |fl(dot_j) - dot_j| <= 127 * e * sum_d |p_d|,
+with e = u for round-to-nearest and e = 2u for an accumulator that truncates
+(the tensor core's internal order and rounding are not IEEE round-to-nearest
+per step, so 2u is assumed).  ReLU adds no error and does not enlarge one;
+the product with w_tj adds one rounding (u) and the FP32 sum over 64 heads
+at most 63 more (u each), all relative to M at most.  First order:
+|gpu - exact| <= (127 * 2 + 1 + 63) * u * M = 318 * 2^-24 * M < 2^-15.68 * M.
+The test admits |gpu - oracle| <= 2^-14 * M + 1e-30: a margin of 3.2 over
+that worst case (5.4 if the tensor core rounded to nearest), and the oracle's
+own double-precision error is below 2^-45 * M.  The bound is a worst case;
+typical errors are far smaller.  The causal suffix (s >= row_lens[t]) must be
+exactly -inf.  The chained Top-K is exact
 on the scores the GPU produced: it must pass the oracle's set contract on
 those scores and equal the oracle's set wherever the boundary is untied.
 """

@@ -34,14 +34,18 @@ def ets():
 
 
 class _PtrAttr(ctypes.Structure):
+    """struct cudaPointerAttributes of the CUDA 13 runtime (driver_types.h),
+    reserved tail included: the call writes all of it."""
     _fields_ = [("type", ctypes.c_int), ("device", ctypes.c_int),
-                ("devicePointer", ctypes.c_void_p), ("hostPointer", ctypes.c_void_p)]
+                ("devicePointer", ctypes.c_void_p), ("hostPointer", ctypes.c_void_p),
+                ("reserved", ctypes.c_long * 8)]
 
 
 def _is_live_device_allocation(addr: int) -> bool:
     """cudaPointerGetAttributes: a live device allocation reports
     cudaMemoryTypeDevice (2); freed memory reports unregistered (0)."""
     rt = ctypes.CDLL("libcudart.so.13")
+    assert ctypes.sizeof(_PtrAttr) == 88
     rt.cudaPointerGetAttributes.argtypes = [ctypes.POINTER(_PtrAttr), ctypes.c_void_p]
     rt.cudaPointerGetAttributes.restype = ctypes.c_int
     a = _PtrAttr()
