@@ -362,7 +362,14 @@ def trace_leg(ets, dev, stream, tokens=430 * 1024, K=2048):
             lens_all[c.row0:c.row0 + c.rows], K,
             scores=buf[:c.rows * c.width].view(c.rows, c.width), out=outs[:c.rows])
 
-    for name, make, reps in (("topk", one_topk, (3, 20)), ("chain", one_chain, (2, 5))):
+    def one_fused(c):
+        return lambda: ets.topk_index_topk_fused(
+            q[c.row0:c.row0 + c.rows], k[:c.width], w[c.row0:c.row0 + c.rows],
+            lens_all[c.row0:c.row0 + c.rows], K,
+            scores=buf[:c.rows * c.width].view(c.rows, c.width), out=outs[:c.rows])
+
+    for name, make, reps in (("topk", one_topk, (3, 20)), ("chain", one_chain, (2, 5)),
+                             ("chain_fused", one_fused, (2, 5))):
         medians = []
         for c in calls:
             g = capture_graphs(stream, [make(c)])
@@ -410,6 +417,9 @@ def chain_leg(ets, dev, stream, reps, T=2048, S=262144, K=2048):
                                                    stream=stream))
     chain_ms = timed(lambda: ets.topk_index_topk(q, k, w, dl, K, scores=scores, out=out,
                                                  stream=stream))
+    out_f = torch.empty((T, K), dtype=torch.int32, device=dev)
+    fused_ms = timed(lambda: ets.topk_index_topk_fused(q, k, w, dl, K, scores=scores, out=out_f,
+                                                       stream=stream))
     status = ets.index_read_status(dev, stream)
     flops = 2.0 * T * S * 64 * 128
     peak, kind = measured_bf16_tflops()
@@ -418,6 +428,8 @@ def chain_leg(ets, dev, stream, reps, T=2048, S=262144, K=2048):
     rows = np.array([0, T // 3, T - 1])
     xr = scores[torch.as_tensor(rows, device=dev)].cpu().numpy()
     v = oracle.compare(xr, lens.numpy()[rows], K, out[torch.as_tensor(rows, device=dev)].cpu().numpy())
+    vf = oracle.compare(xr, lens.numpy()[rows], K,
+                        out_f[torch.as_tensor(rows, device=dev)].cpu().numpy())
     del scores, q, k
     torch.cuda.empty_cache()
     return {
@@ -432,6 +444,13 @@ def chain_leg(ets, dev, stream, reps, T=2048, S=262144, K=2048):
                      "flops_per_launch": flops, "kernel": "k_index_scores"},
         "spot_check": {"rows": int(rows.size), "contract_failures": int((v["check"] != 0).sum()),
                        "set_mismatches": int(v["set_mismatch"].sum())},
+        "fused": {"api": "topk_index_topk_fused (sample-key score pass, gated score pass, "
+                         "selection from the candidates)",
+                  "ms_per_call": fused_ms, "rows_per_s": T / (fused_ms / 1000.0),
+                  "selection_ms_beyond_scores": fused_ms - score_ms, "gpu_launches_per_call": 5,
+                  "spot_check": {"rows": int(rows.size),
+                                 "contract_failures": int((vf["check"] != 0).sum()),
+                                 "set_mismatches": int(vf["set_mismatch"].sum())}},
     }
 
 

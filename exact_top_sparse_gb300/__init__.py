@@ -72,7 +72,7 @@ EXPORTS = ("topk_ragged", "topk_ragged_diag", "topk_ragged_ws", "topk_workspace_
            "topk_ragged_bf16", "topk_ragged_bf16_diag", "topk_sort_rows", "topk_sort_rows_bf16",
            "topk_check_wait_timeout", "topk_ragged_k", "topk_ragged_k_bf16", "topk_ragged_k_diag",
            "topk_ragged_e4m3", "topk_ragged_e4m3_diag", "topk_ragged_k_e4m3", "topk_sort_rows_e4m3",
-           "topk_cached_workspace")
+           "topk_cached_workspace", "topk_index_topk_fused")
 NOALLOC_MAX_ROWS = 64
 
 _lib = None
@@ -109,6 +109,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.topk_ragged_bf16_diag.argtypes = [vp, vp, i64, i64, i32, vp, vp, vp]
     lib.topk_index_scores.argtypes = [vp, vp, vp, i64, i64, i32, i32, vp, vp, i64, vp]
     lib.topk_index_topk.argtypes = [vp, vp, vp, i64, i64, i32, i32, vp, vp, i64, i32, vp, vp]
+    lib.topk_index_topk_fused.argtypes = [vp, vp, vp, i64, i64, i32, i32, vp, vp, i64, i32, vp,
+                                          vp, vp]
     lib.topk_index_read_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     lib.topk_workspace_bytes.argtypes = [i64, i64, i32]
     lib.topk_workspace_bytes.restype = sz
@@ -132,7 +134,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                  "topk_ragged_k_diag", "topk_ragged_e4m3", "topk_ragged_e4m3_diag",
                  "topk_ragged_k_e4m3", "topk_sort_rows_e4m3", "topk_index_read_status",
                  "topk_plan", "topk_set_params", "topk_get_params", "topk_read_status",
-                 "topk_version", "topk_cached_workspace"):
+                 "topk_version", "topk_cached_workspace", "topk_index_topk_fused"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -443,6 +445,34 @@ def topk_index_topk(q, k, w, row_lens, K: int = 2048, scores=None, out=None, str
                                  row_lens.data_ptr(), scores.data_ptr(), scores.shape[1], K,
                                  out.data_ptr(), _stream_handle(q.device, stream))
     _check(rc, "topk_index_topk")
+    return scores, out
+
+
+def topk_index_topk_fused(q, k, w, row_lens, K: int = 2048, scores=None, out=None, diag=False,
+                          stream=None):
+    """Scores with the Top-K's threshold and candidate collection moved into
+    the score kernel (see topk_index_topk_fused in include/topk.h): returns
+    (scores, out_idx [T, K] int32) or, with diag=True, (scores, out_idx, diag
+    as a numpy structured array).  The result is the exact Top-K of the
+    scores written."""
+    lib = load_library()
+    if row_lens is None:
+        raise TypeError("row_lens is required")
+    T, S, H, D, scores = _index_inputs(q, k, w, row_lens, scores)
+    if out is None:
+        out = torch.empty((T, K), dtype=torch.int32, device=q.device)
+    elif not (out.device == q.device and out.dtype == torch.int32 and tuple(out.shape) == (T, K)
+              and out.is_contiguous()):
+        raise TypeError("out must be a contiguous int32 [T, K] tensor on q's device")
+    dg = torch.empty(T * DIAG_DTYPE.itemsize, dtype=torch.uint8, device=q.device) if diag else None
+    with torch.cuda.device(q.device):
+        rc = lib.topk_index_topk_fused(q.data_ptr(), k.data_ptr(), w.data_ptr(), T, S, H, D,
+                                       row_lens.data_ptr(), scores.data_ptr(), scores.shape[1], K,
+                                       out.data_ptr(), dg.data_ptr() if diag else None,
+                                       _stream_handle(q.device, stream))
+    _check(rc, "topk_index_topk_fused")
+    if diag:
+        return scores, out, dg.cpu().numpy().view(DIAG_DTYPE)
     return scores, out
 
 

@@ -25,6 +25,11 @@
 //                 sum over heads, masked causal suffix, coalesced stores.
 // Every wait is bounded; a timeout sets an abort flag that all roles honour,
 // and tensor memory is always released.
+//
+// Optionally the epilogue also gates every score against its query's
+// threshold tau1 and appends the admitted (key, order key) pairs to that
+// query's candidate area (the fused score -> select path; the thresholds come
+// from a first pass of this kernel over a fixed-stride sample of the keys).
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -34,6 +39,8 @@
 #include <mutex>
 
 #include "topk.h"
+#include "topk_device.cuh"
+#include "topk_launch.h"
 
 namespace tki {
 
@@ -151,6 +158,7 @@ struct Args {
   int32_t n_tiles;         // S / KT
   int32_t n_chunks;        // ceil(n_tiles / CHUNK_TILES)
   int32_t n_units;         // (T / QB) * n_chunks
+  uint8_t* rows;           // fused path: row states (tau1, candidate count and area); or nullptr
 };
 
 __device__ __forceinline__ void unit_coords(const Args& a, int32_t u, int32_t* qb, int32_t* t0,
@@ -329,8 +337,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         w_s[i] = a.w[(int64_t)qb * QB * HEADS + i];
       asm volatile("bar.sync 1, 128;" ::: "memory");
       int32_t lenq[QB];
+      float tau1q[QB];
 #pragma unroll
-      for (int q = 0; q < QB; ++q) lenq[q] = a.lens ? a.lens[qb * QB + q] : a.S;
+      for (int q = 0; q < QB; ++q) {
+        lenq[q] = a.lens ? a.lens[qb * QB + q] : a.S;
+        tau1q[q] = a.rows ? __ldcg(reinterpret_cast<const float*>(
+                                a.rows + (size_t)(qb * QB + q) * tk::kFusedRowBytes + tk::kKvTau1Off))
+                          : 0.0f;
+      }
       const int32_t te = unit_end(a, qb, t0, t1);
       // tiles past every query's valid length: -inf, no accumulator
       for (int32_t t = te; t < t1; ++t) {
@@ -390,6 +404,30 @@ __global__ void __launch_bounds__(THREADS, 1)
             a.out[tq * a.ld + key] = key < lenq[q] ? res[q] : -INFINITY;
           }
         }
+        if (a.rows) {
+          // the gate: scores >= tau1 of the query join its candidates (one
+          // atomic per warp and query for the warp's admitted keys)
+#pragma unroll
+          for (int q = 0; q < QB; ++q) {
+            const bool adm = key < a.S && key < lenq[q] && res[q] >= tau1q[q];
+            const uint32_t m = __ballot_sync(0xffffffffu, adm);
+            if (m) {
+              uint8_t* rs = a.rows + (size_t)(qb * QB + q) * tk::kFusedRowBytes;
+              const uint32_t leader = __ffs(m) - 1u;
+              uint32_t base = 0;
+              if (lane == leader)
+                base = atomicAdd(reinterpret_cast<uint32_t*>(rs + tk::kKvNcandOff),
+                                 (uint32_t)__popc(m));
+              base = __shfl_sync(0xffffffffu, base, leader);
+              if (adm) {
+                const uint32_t pos = base + (uint32_t)__popc(m & ((1u << lane) - 1u));
+                if (pos < tk::kKvCandCap)
+                  reinterpret_cast<uint2*>(rs + tk::kKvCandOff)[pos] =
+                      make_uint2((uint32_t)key, tk::fkey(res[q]));
+              }
+            }
+          }
+        }
       }
     }
   }
@@ -433,14 +471,43 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint32_t box_rows)
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace tki
+// Sample keys of the fused path and the samples' valid counts (one thread
+// per 16-byte piece of a key row; then one thread per query).
+__global__ void k_gather_sample_keys(const uint4* __restrict__ k, int64_t S, int32_t stride,
+                                     int64_t S_s, uint4* __restrict__ ks,
+                                     const int32_t* __restrict__ row_lens, int64_t T,
+                                     int32_t* __restrict__ lens_s) {
+  constexpr int PIECES = DIM * 2 / 16;  // 16 uint4 per key row
+  const int64_t n = S_s * PIECES;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n + T;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    if (i < n) {
+      const int64_t j = i / PIECES, p = i % PIECES, src = j * stride;
+      ks[i] = src < S ? k[src * PIECES + p] : make_uint4(0u, 0u, 0u, 0u);
+    } else {
+      const int64_t t = i - n;
+      int64_t l = row_lens[t];
+      l = l < 0 ? 0 : (l > S ? S : l);
+      lens_s[t] = (int32_t)((l + stride - 1) / stride);
+    }
+  }
+}
 
-extern "C" {
+cudaError_t launch_gather_sample_keys(const uint16_t* k, int64_t S, int32_t stride, int64_t S_s,
+                                      uint16_t* ks, const int32_t* row_lens, int64_t T,
+                                      int32_t* lens_s, cudaStream_t stream) {
+  const int64_t work = S_s * (DIM * 2 / 16) + T;
+  const int blocks = (int)((work + 255) / 256 < 1024 ? (work + 255) / 256 : 1024);
+  k_gather_sample_keys<<<blocks, 256, 0, stream>>>(reinterpret_cast<const uint4*>(k), S, stride,
+                                                   S_s, reinterpret_cast<uint4*>(ks), row_lens, T,
+                                                   lens_s);
+  return cudaGetLastError();
+}
 
-int topk_index_scores(const uint16_t* q, const uint16_t* k, const float* w, int64_t T, int64_t S,
-                      int32_t H, int32_t D, const int32_t* row_lens, float* scores,
-                      int64_t ld_scores, struct CUstream_st* stream) {
-  using namespace tki;
+// Argument checks of the score stage (shapes the kernel tiles, alignment).
+int check_index_args(const uint16_t* q, const uint16_t* k, const float* w, int64_t T, int64_t S,
+                     int32_t H, int32_t D, const int32_t* row_lens, const float* scores,
+                     int64_t ld_scores) {
   if (T < 0 || S < 0 || ld_scores < S) return TOPK_ERR_ARG;
   if (H != HEADS || D != DIM) return TOPK_ERR_UNSUPPORTED_SHAPE;
   if (T % QB != 0 || S % KT != 0) return TOPK_ERR_UNSUPPORTED_SHAPE;
@@ -451,6 +518,13 @@ int topk_index_scores(const uint16_t* q, const uint16_t* k, const float* w, int6
       (reinterpret_cast<uintptr_t>(w) & 15u) || (reinterpret_cast<uintptr_t>(scores) & 3u) ||
       (row_lens && (reinterpret_cast<uintptr_t>(row_lens) & 3u)))
     return TOPK_ERR_ALIGN;
+  return TOPK_OK;
+}
+
+int launch_index_scores(const uint16_t* q, const uint16_t* k, const float* w, int64_t T, int64_t S,
+                        const int32_t* row_lens, float* scores, int64_t ld_scores, uint8_t* rows,
+                        cudaStream_t stream) {
+  if (T == 0 || S == 0) return TOPK_OK;
   int dev = 0, sms = 0, major = 0, minor = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return TOPK_ERR_NO_DEVICE;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
@@ -473,6 +547,7 @@ int topk_index_scores(const uint16_t* q, const uint16_t* k, const float* w, int6
   const int64_t units = (T / QB) * (int64_t)a.n_chunks;
   if (units > INT32_MAX) return TOPK_ERR_ARG;
   a.n_units = (int32_t)units;
+  a.rows = rows;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
@@ -481,8 +556,21 @@ int topk_index_scores(const uint16_t* q, const uint16_t* k, const float* w, int6
   });
   if (attr_err != cudaSuccess) return TOPK_ERR_CUDA;
   const int grid = (int)(units < sms ? units : sms);
-  k_index_scores<<<grid, THREADS, SMEM_BYTES, reinterpret_cast<cudaStream_t>(stream)>>>(mk, mq, a);
+  k_index_scores<<<grid, THREADS, SMEM_BYTES, stream>>>(mk, mq, a);
   return cudaGetLastError() == cudaSuccess ? TOPK_OK : TOPK_ERR_CUDA;
+}
+
+}  // namespace tki
+
+extern "C" {
+
+int topk_index_scores(const uint16_t* q, const uint16_t* k, const float* w, int64_t T, int64_t S,
+                      int32_t H, int32_t D, const int32_t* row_lens, float* scores,
+                      int64_t ld_scores, struct CUstream_st* stream) {
+  const int rc = tki::check_index_args(q, k, w, T, S, H, D, row_lens, scores, ld_scores);
+  if (rc != TOPK_OK) return rc;
+  return tki::launch_index_scores(q, k, w, T, S, row_lens, scores, ld_scores, nullptr,
+                                  reinterpret_cast<cudaStream_t>(stream));
 }
 
 int topk_index_topk(const uint16_t* q, const uint16_t* k, const float* w, int64_t T, int64_t S,

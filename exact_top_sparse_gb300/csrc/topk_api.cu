@@ -122,6 +122,8 @@ struct Plan {
   size_t smem = 0;
 };
 
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
 int check_sizes(int64_t M, int64_t N, int32_t K) {
   if (M < 0 || N < 0 || N > INT32_MAX || M > INT32_MAX) return TOPK_ERR_ARG;
   if (K < 1) return TOPK_ERR_ARG;
@@ -443,6 +445,66 @@ size_t topk_workspace_bytes(int64_t M, int64_t N_alloc, int32_t K) {
   Plan pl;
   if (make_plan(M, N_alloc, K, params_snapshot(), d, &pl)) return 0;
   return pl.ws;
+}
+
+int topk_index_topk_fused(const uint16_t* q, const uint16_t* k, const float* w, int64_t T,
+                          int64_t S, int32_t H, int32_t D, const int32_t* row_lens, float* scores,
+                          int64_t ld_scores, int32_t K, int32_t* out_idx, topk_row_diag* diag,
+                          struct CUstream_st* stream) {
+  if (!row_lens || K < 1) return TOPK_ERR_ARG;
+  if (K > TOPK_K_MAX) return TOPK_ERR_UNSUPPORTED_K;
+  int rc = tki::check_index_args(q, k, w, T, S, H, D, row_lens, scores, ld_scores);
+  if (rc) return rc;
+  if (T == 0) return TOPK_OK;
+  if (!out_idx) return TOPK_ERR_ARG;
+  if (reinterpret_cast<uintptr_t>(out_idx) & 3u) return TOPK_ERR_ALIGN;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (S == 0) {  // every row is empty: K sentinels, through the selector
+    return topk_ragged(scores, row_lens, T, ld_scores, K, out_idx, stream);
+  }
+  DevInfo d;
+  int dev = 0;
+  rc = device_info(&d, &dev);
+  if (rc) return rc;
+  // one sampling tier for the whole call, the one rows of S keys would take
+  topk_params p = params_snapshot();
+  const bool lg = p.long_len > 0 && S >= p.long_len;
+  p.stride = lg ? p.long_stride : p.stride;
+  p.rho0 = lg ? p.long_rho0 : p.rho0;
+  p.rho1 = lg ? p.long_rho1 : p.rho1;
+  p.long_len = 0;
+  const int64_t s = p.stride;
+  const int64_t ns_max = (S + s - 1) / s;
+  const int64_t S_s = (ns_max + 127) / 128 * 128;  // the score kernel tiles 128 keys
+  // workspace: row states, sample keys, sample lengths, sample scores
+  const size_t rows_b = (size_t)T * tk::kFusedRowBytes;
+  const size_t ks_b = align256((size_t)S_s * 128 * 2);
+  const size_t ls_b = align256((size_t)T * 4);
+  const size_t ss_b = align256((size_t)T * S_s * 4);
+  const size_t need = kHdrBytes + rows_b + ks_b + ls_b + ss_b;
+  void* ws = nullptr;
+  rc = cached_workspace(dev, st, need, &ws);
+  if (rc) return rc;
+  uint8_t* rows = static_cast<uint8_t*>(ws) + kHdrBytes;
+  uint16_t* ks = reinterpret_cast<uint16_t*>(rows + rows_b);
+  int32_t* lens_s = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(ks) + ks_b);
+  float* ss = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(lens_s) + ls_b);
+  Plan pl;
+  pl.kind = TOPK_KIND_KVSPLIT;
+  pl.segments = 1;
+  tk::Params P = kernel_params(T, S, K, p, pl);
+  if (tki::launch_gather_sample_keys(k, S, (int32_t)s, S_s, ks, row_lens, T, lens_s, st) !=
+      cudaSuccess)
+    return TOPK_ERR_CUDA;
+  rc = tki::launch_index_scores(q, ks, w, T, S_s, lens_s, ss, S_s, nullptr, st);
+  if (rc) return rc;
+  if (tk::launch_fused_prepare(ss, S_s, row_lens, rows, P, st) != cudaSuccess) return TOPK_ERR_CUDA;
+  rc = tki::launch_index_scores(q, k, w, T, S, row_lens, scores, ld_scores, rows, st);
+  if (rc) return rc;
+  return tk::launch_fused_finish(scores, ld_scores, out_idx,
+                                 reinterpret_cast<tk::RowDiag*>(diag), rows, P, st) == cudaSuccess
+             ? TOPK_OK
+             : TOPK_ERR_CUDA;
 }
 
 int topk_cached_workspace(struct CUstream_st* stream, void** ptr, size_t* bytes) {

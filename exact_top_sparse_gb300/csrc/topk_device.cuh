@@ -135,7 +135,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // flag lives in memory that belongs to one launch and is reset by it (the
 // last CTA of a persistent launch, the prepare kernel of a KV-split launch),
 // so an abort never reaches another launch.
-__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, uint32_t* abort,
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, uint32_t* abort,
                                             uint64_t limit_ns = WAIT_LIMIT_NS) {
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
@@ -152,7 +152,7 @@ __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, uint
 
 // Polls until the phase completes or limit_ns passes, whatever the fail-fast
 // flag says (used to let copies in flight land before a CTA exits).
-__device__ __noinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+static __device__ __noinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = globaltimer();
   while (!mbar_try_wait(bar, parity))
     if (globaltimer() - t0 > limit_ns) return false;
@@ -1223,7 +1223,7 @@ __device__ uint32_t select_rank(const G& get, int64_t n, uint32_t r, uint32_t lo
 // they are gathered into `list` and ranked by counting, which yields both
 // answers at once.  Otherwise two general rank selections run.  Every thread
 // must call.
-__device__ void select_two_ranks(const uint32_t* keys, uint32_t n, uint32_t r0, uint32_t r1,
+static __device__ void select_two_ranks(const uint32_t* keys, uint32_t n, uint32_t r0, uint32_t r1,
                                  uint32_t kmin, uint32_t kmax, uint32_t* hist, uint32_t* list,
                                  Shared& S, uint32_t* key0, uint32_t* key1) {
   if (kmin == kmax) {
@@ -1271,18 +1271,14 @@ __device__ void select_two_ranks(const uint32_t* keys, uint32_t n, uint32_t r0, 
   *key0 = select_rank(g, n, r0, *key1, kmax, hist, S);
 }
 
-// Stage 1.  Samples at 0, s, 2s, ... < len; tau_j = r_j-th largest sample
-// with r_j = clamp(ceil(T_j * n_s / len), 1, n_s).  Leaves key0/key1 and the
-// sample key range in S.  Every thread must call.
+// The r0-th and r1-th largest (r0 <= r1, both in [1, ns]) of the ns values
+// row[0], row[stride], ... (read with an L2 evict-last hint); leaves key0/key1
+// and the range [kmin, kmax] of the values' keys in S.  Every thread must
+// call.
 template <class E>
-__device__ void sample_thresholds(const E* __restrict__ row, int64_t len, int32_t stride,
-                                  uint32_t T0, uint32_t T1, uint32_t* skeys, uint32_t* hist,
-                                  uint32_t* list, Shared& S) {
-  const int64_t ns = (len + stride - 1) / stride;
-  int64_t r0 = ((int64_t)T0 * ns + len - 1) / len;
-  int64_t r1 = ((int64_t)T1 * ns + len - 1) / len;
-  r0 = r0 < 1 ? 1 : (r0 > ns ? ns : r0);
-  r1 = r1 < 1 ? 1 : (r1 > ns ? ns : r1);
+__device__ void thresholds_at_ranks(const E* __restrict__ row, int64_t ns, int32_t stride,
+                                    uint32_t r0, uint32_t r1, uint32_t* skeys, uint32_t* hist,
+                                    uint32_t* list, Shared& S) {
   const uint64_t pol = l2_policy_evict_last();
   const bool on_chip = ns <= SAMPLE_SMEM;
   uint32_t mn = 0xffffffffu, mx = 0u;
@@ -1310,12 +1306,11 @@ __device__ void sample_thresholds(const E* __restrict__ row, int64_t len, int32_
   phase_mark(S, 8);
   uint32_t key1, key0;
   if (on_chip) {
-    select_two_ranks(skeys, (uint32_t)ns, (uint32_t)r0, (uint32_t)r1, kmin, kmax, hist, list, S,
-                     &key0, &key1);
+    select_two_ranks(skeys, (uint32_t)ns, r0, r1, kmin, kmax, hist, list, S, &key0, &key1);
   } else {
     const SampleGlobal<E> g{row, stride, pol};
-    key1 = select_rank(g, ns, (uint32_t)r1, kmin, kmax, hist, S);
-    key0 = select_rank(g, ns, (uint32_t)r0, key1, kmax, hist, S);
+    key1 = select_rank(g, ns, r1, kmin, kmax, hist, S);
+    key0 = select_rank(g, ns, r0, key1, kmax, hist, S);
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -1325,6 +1320,26 @@ __device__ void sample_thresholds(const E* __restrict__ row, int64_t len, int32_
     S.kmax = kmax;
   }
   __syncthreads();
+}
+
+// Sample rank of candidate target T for a row of len elements viewed through
+// ns samples: r = clamp(ceil(T * ns / len), 1, ns).
+__device__ __forceinline__ uint32_t sample_rank(uint32_t T, int64_t ns, int64_t len) {
+  int64_t r = ((int64_t)T * ns + len - 1) / len;
+  r = r < 1 ? 1 : (r > ns ? ns : r);
+  return (uint32_t)r;
+}
+
+// Stage 1.  Samples at 0, s, 2s, ... < len; tau_j = r_j-th largest sample
+// with r_j = clamp(ceil(T_j * n_s / len), 1, n_s).  Leaves key0/key1 and the
+// sample key range in S.  Every thread must call.
+template <class E>
+__device__ void sample_thresholds(const E* __restrict__ row, int64_t len, int32_t stride,
+                                  uint32_t T0, uint32_t T1, uint32_t* skeys, uint32_t* hist,
+                                  uint32_t* list, Shared& S) {
+  const int64_t ns = (len + stride - 1) / stride;
+  thresholds_at_ranks(row, ns, stride, sample_rank(T0, ns, len), sample_rank(T1, ns, len), skeys,
+                      hist, list, S);
 }
 
 // Seeded bins of the full-row pass: the candidates' keys start at key(tau1);

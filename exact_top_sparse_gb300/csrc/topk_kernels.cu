@@ -101,6 +101,10 @@ constexpr size_t CTA_AREA_BYTES = (size_t)SPILL * sizeof(uint2) + (size_t)TIE_CA
 static_assert(CTA_AREA_BYTES % 256 == 0, "CTA areas keep 256-byte alignment");
 static_assert(sizeof(KvHdr) <= KV_HIST_OFF, "KV row header too large");
 static_assert(KV_ROW_BYTES == kKvRowBytes, "kKvRowBytes must match the KV-split row layout");
+static_assert(offsetof(KvHdr, ncand) == kKvNcandOff && offsetof(KvHdr, tau1) == kKvTau1Off &&
+                  KV_CAND_OFF == kKvCandOff && (size_t)CAP_ALL == kKvCandCap &&
+                  align_up(KV_CAND_OFF + (size_t)CAP_ALL * sizeof(uint2), 256) == kFusedRowBytes,
+              "fused row state must follow the KV-split row layout");
 
 struct RowCarve {
   Shared* S;
@@ -754,6 +758,129 @@ __global__ void __launch_bounds__(THREADS, 2)
   ring_drain(R);
 }
 
+// ------------------------------------------------------ fused score -> select
+// The fused path applies the method one stage earlier: the sample view of a
+// row is the score kernel's own output at keys 0, s, 2s, ... < len (computed
+// first, from those keys alone), its thresholds follow the same rank rule,
+// and the full-row pass is the score kernel itself, whose epilogue admits
+// every score >= tau1 into the row's candidate area while it writes the row.
+// The selection then certifies C(tau0) >= K from the candidates and refines
+// them; a row the candidates cannot serve (C(tau1) < K, or more candidates
+// than the area holds) is served from the materialised row by the same
+// recovery and re-read paths as every other row.
+
+// One CTA per row: the row's mode and thresholds from its sample scores.
+__global__ void __launch_bounds__(THREADS, 1)
+    k_fused_prepare(const float* __restrict__ sscores, int64_t ld_s,
+                    const int32_t* __restrict__ row_lens, uint8_t* __restrict__ rows, Params P) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  Shared& S = *reinterpret_cast<Shared*>(smem);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem + SH_HDR);
+  uint32_t* list = hist + NB;
+  uint32_t* skeys = list + THREADS;
+  const int64_t r = blockIdx.x;
+  uint32_t lflags = 0;
+  const int64_t len = clamp_len(row_lens[r], P.N_alloc, lflags);
+  const int32_t Kr = row_k_of(P, r, lflags);
+  KvHdr* h = reinterpret_cast<KvHdr*>(rows + (size_t)r * kFusedRowBytes);
+  uint32_t mode = 2;
+  if (len <= Kr || Kr == 0) mode = 0;
+  else if (len < P.sample_min_len) mode = 1;
+  uint32_t key0 = 0, key1 = 0, kmin = 0, kmax = 0;
+  if (mode == 2) {
+    const SampleSpec sp = sample_spec(P, len, Kr);
+    const int64_t ns = (len + sp.stride - 1) / sp.stride;
+    thresholds_at_ranks(sscores + r * ld_s, ns, 1, sample_rank(sp.target0, ns, len),
+                        sample_rank(sp.target1, ns, len), skeys, hist, list, S);
+    key0 = S.key0;
+    key1 = S.key1;
+    kmin = S.kmin;
+    kmax = S.kmax;
+  }
+  if (threadIdx.x == 0) {
+    h->mode = mode;
+    h->len = (uint32_t)len;
+    h->key0 = key0;
+    h->key1 = key1;
+    h->kmin = kmin;
+    h->kmax = kmax;
+    h->c0 = 0;
+    h->ncand = 0;
+    h->neq = 0;
+    h->ticket = 0;
+    h->ovf = 0;
+    h->flags = lflags;
+    h->tau0 = key_to_float(key0);
+    h->tau1 = mode == 2 ? key_to_float(key1) : __int_as_float(0x7f800000);  // +inf: admit none
+    h->k = Kr;
+    h->abort = 0;
+  }
+}
+
+// One CTA per row: C(tau0) and the seeded histogram from the candidates the
+// score kernel appended, then the selection (refinement, or the recovery and
+// re-read paths over the materialised row).
+__global__ void __launch_bounds__(THREADS, 2)
+    k_fused_finish(const float* __restrict__ scores, int64_t ld, int32_t* __restrict__ out_idx,
+                   RowDiag* __restrict__ diag, uint8_t* __restrict__ rows, Params P) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const RowCarve c = carve(smem);
+  Shared& S = *c.S;
+  const int64_t r = blockIdx.x;
+  uint8_t* base = rows + (size_t)r * kFusedRowBytes;
+  KvHdr* h = reinterpret_cast<KvHdr*>(base);
+  uint2* gcand = reinterpret_cast<uint2*>(base + KV_CAND_OFF);
+  if (threadIdx.x == 0) {
+    S.flags = 0;
+    S.nout = 0;
+  }
+  Ring R;
+  ring_init(R, S, c.ring, &h->abort);
+  R.pf_ahead = P.pf_ahead;
+  const uint32_t mode = __ldcg(&h->mode);
+  const int64_t len = __ldcg(&h->len);
+  const uint32_t key0 = __ldcg(&h->key0), key1 = __ldcg(&h->key1), kmin = __ldcg(&h->kmin),
+                 kmax = __ldcg(&h->kmax);
+  const int32_t K = P.K;
+  const int32_t Kr = __ldcg(&h->k);
+  uint32_t lflags = __ldcg(&h->flags);
+  const float* row = scores + r * ld;
+  int32_t* out = out_idx + r * (int64_t)K;
+  const float qnan = __int_as_float(0x7fc00000);
+  if (mode == 0) {
+    write_sentinel_row(out, Kr, len);
+    if (threadIdx.x == 0) S.nout = (uint32_t)Kr;
+    finish_row(S, out, Kr, K, lflags, diag, r, PATH_SENTINEL, qnan, qnan, 0, 0);
+    ring_drain(R);
+    return;
+  }
+  if (mode == 1) {
+    if (fits_stage<float>(len)) exact_row_staged(row, len, out, Kr, c, lflags);
+    else exact_row_stream(row, len, out, Kr, R, c, lflags);
+    finish_row(S, out, Kr, K, lflags, diag, r, PATH_DIRECT, qnan, qnan, 0, 0);
+    ring_drain(R);
+    return;
+  }
+  const uint32_t Cgt = __ldcg(&h->ncand);
+  const bool overflow = Cgt > (uint32_t)CAP_ALL;
+  const uint32_t nkeep = min(Cgt, (uint32_t)CAP_ALL), nload = min(Cgt, (uint32_t)CAP);
+  for (uint32_t j = threadIdx.x; j < nload; j += THREADS) {
+    const uint2* p = gcand + j;
+    c.cand[j] = make_uint2(__ldcg(&p->x), __ldcg(&p->y));
+  }
+  const Bins sb = scan_bins(key1, kmax);
+  clear_hist(c.hist);
+  __syncthreads();
+  const uint32_t c0 = tally_candidates(c.cand, gcand + CAP, nkeep, key0, sb, c.hist);
+  uint32_t C0 = block_sum(c0, S);
+  const int32_t path =
+      select_after_scan(row, len, out, Kr, R, c, gcand + CAP, nullptr, sample_spec(P, len, Kr), C0,
+                        Cgt, 0u, overflow, key0, key1, kmin, sb, lflags);
+  finish_row(S, out, Kr, K, lflags, diag, r, path, key_to_float(key0), key_to_float(key1), C0,
+             Cgt);
+  ring_drain(R);
+}
+
 // ------------------------------------------------------------------ launchers
 size_t persistent_smem_bytes() { return SH_ROW_TOTAL; }
 size_t kv_segment_smem_bytes() { return SH_ROW_TOTAL; }
@@ -766,6 +893,7 @@ size_t direct_smem_bytes(int64_t n_alloc, int elem_bytes) {
          align_up((size_t)n_alloc * elem_bytes + 16, 16);
 }
 size_t kv_row_bytes() { return KV_ROW_BYTES; }
+size_t fused_prepare_smem_bytes() { return kv_prepare_smem_bytes(); }
 size_t persistent_spill_bytes() { return CTA_AREA_BYTES; }
 
 static cudaError_t set_smem(const void* fn, size_t bytes) {
@@ -790,6 +918,8 @@ cudaError_t prepare_device() {
                                 (const void*)k_kv_prepare<uint8_t>};
   for (const void* fn : prep_kernels)
     if ((e = set_smem(fn, kv_prepare_smem_bytes())) != cudaSuccess) return e;
+  if ((e = set_smem((const void*)k_fused_prepare, kv_prepare_smem_bytes())) != cudaSuccess) return e;
+  if ((e = set_smem((const void*)k_fused_finish, persistent_smem_bytes())) != cudaSuccess) return e;
   const void* direct_kernels[] = {(const void*)k_direct<float>, (const void*)k_direct<uint16_t>,
                                   (const void*)k_direct<uint8_t>};
   for (const void* fn : direct_kernels)
@@ -864,6 +994,20 @@ cudaError_t launch_kvsplit(const void* scores, const int32_t* row_lens, int32_t*
     return launch_kvsplit_t(static_cast<const uint8_t*>(scores), row_lens, out, diag, ws_rows, P,
                             st);
   return launch_kvsplit_t(static_cast<const float*>(scores), row_lens, out, diag, ws_rows, P, st);
+}
+
+cudaError_t launch_fused_prepare(const float* sscores, int64_t ld_s, const int32_t* row_lens,
+                                 uint8_t* rows, const Params& P, cudaStream_t st) {
+  k_fused_prepare<<<(unsigned)P.M, THREADS, kv_prepare_smem_bytes(), st>>>(sscores, ld_s, row_lens,
+                                                                          rows, P);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fused_finish(const float* scores, int64_t ld, int32_t* out, RowDiag* diag,
+                                uint8_t* rows, const Params& P, cudaStream_t st) {
+  k_fused_finish<<<(unsigned)P.M, THREADS, persistent_smem_bytes(), st>>>(scores, ld, out, diag,
+                                                                         rows, P);
+  return cudaGetLastError();
 }
 
 // Self-test of the bounded wait: one thread waits on a barrier that nothing

@@ -367,6 +367,32 @@ int topk_index_topk(const uint16_t* q, const uint16_t* k, const float* w, int64_
                     int32_t H, int32_t D, const int32_t* row_lens, float* scores,
                     int64_t ld_scores, int32_t K, int32_t* out_idx, struct CUstream_st* stream);
 
+/* Scores and exact Top-K with the selection's proposal and certification
+ * moved into the score stage (the fused score -> filter step of the xllm-io
+ * review of LiteTopK, sections "核心思想" and "详细方法": scores are gated
+ * against a threshold while they are produced, and survivors go to a
+ * candidate buffer).  The threshold is this method's own (PaperDaily section
+ * 问题二): the score kernel first scores a fixed-stride sample of the keys
+ * (k[0], k[s], k[2s], ...; s and the targets those of the sampling tier that
+ * rows of S keys take under topk_params), each row's tau0 and tau1 are its
+ * samples of rank ceil(T * n_s / len); then the full score pass writes
+ * `scores` as topk_index_scores() does and also appends every score >= tau1
+ * of a row to that row's candidate area, counting C(tau1).  The selection
+ * certifies C(tau0) >= K from the candidates and refines them exactly; a row
+ * whose candidates do not certify it (C(tau1) < K, or more than 16384
+ * candidates) is served from its materialised row in `scores` by the same
+ * recovery and re-read paths as topk_ragged(), so the result is always the
+ * exact Top-K of the scores written (same set contract).
+ * Arguments as topk_index_topk(); diag (device, [T] topk_row_diag) may be
+ * NULL.  Uses the library's workspace for the stream: about
+ * T * 140 KB + T * ceil(S / s) * 4 B (+ the sample keys); TOPK_ERR_CAPTURE_ALLOC
+ * if that must grow during stream capture.  Five launches on `stream`,
+ * capturable into one CUDA graph after a first uncaptured call. */
+int topk_index_topk_fused(const uint16_t* q, const uint16_t* k, const float* w, int64_t T,
+                          int64_t S, int32_t H, int32_t D, const int32_t* row_lens, float* scores,
+                          int64_t ld_scores, int32_t K, int32_t* out_idx, topk_row_diag* diag,
+                          struct CUstream_st* stream);
+
 /* Read and clear the score kernel's status word (TOPK_FLAG_TIMEOUT); syncs
  * the stream. */
 int topk_index_read_status(struct CUstream_st* stream, uint32_t* flags);
