@@ -521,7 +521,8 @@ def kernel_fingerprint(params, kind, grid, elem_bytes=4):
     score element size."""
     import hashlib
     h = hashlib.sha256()
-    for name in ("score_elem.cuh", "topk_device.cuh", "topk_kernels.cu", "topk_launch.h"):
+    for name in ("score_elem.cuh", "topk_device.cuh", "topk_kernels.cu", "topk_launch.h",
+                 "topk_api.cu"):
         with open(os.path.join(ROOT, "exact_top_sparse_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     launch = {"sampling": {k: params[k] for k in SAMPLING_KNOBS}, "kind": kind, "grid": grid,

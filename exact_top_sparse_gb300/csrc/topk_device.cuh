@@ -646,6 +646,8 @@ struct ScanCollect {
   uint32_t* ties;     // indices of scores equal to tau1, tie_cap of them
   uint32_t tie_cap;
   uint32_t* neq;      // scores equal to tau1 (counts past tie_cap)
+  uint32_t xeq;       // ties this thread counted in a register once it saw the tie list full
+  bool full;          // this thread saw the tie list full
 
   __device__ __forceinline__ bool admit(float x) const {
     if (POS) return (int32_t)__float_as_uint(x) >= (int32_t)t1;
@@ -665,8 +667,14 @@ struct ScanCollect {
   }
   // Counts the ties of mask q (element e of group a for bits 0-3, of group b
   // for bits 4-7) and keeps their indices while the tie list has room.
-  __device__ __forceinline__ void put_ties(uint32_t q, int64_t ia, int64_t ib) const {
-    uint32_t t = atomicAdd(neq, (uint32_t)__popc(q));
+  __device__ __forceinline__ void put_ties(uint32_t q, int64_t ia, int64_t ib) {
+    const uint32_t c = (uint32_t)__popc(q);
+    if (full) {  // the list has its first tie_cap indices: only count
+      xeq += c;
+      return;
+    }
+    uint32_t t = atomicAdd(neq, c);
+    if (t + c >= tie_cap) full = true;
     while (q && t < tie_cap) {
       const uint32_t e = (uint32_t)__ffs(q) - 1u;
       q &= q - 1u;
@@ -677,7 +685,7 @@ struct ScanCollect {
   // when ha, ib.. of vb when hb) with one shared-memory atomic, visiting only
   // the admitted elements.
   __device__ __forceinline__ void lane_put2(int64_t ia, const float4& va, bool ha, int64_t ib,
-                                            const float4& vb, bool hb) const {
+                                            const float4& vb, bool hb) {
     const uint32_t m = (ha ? admit_mask(va) : 0u) | ((hb ? admit_mask(vb) : 0u) << 4);
     if (!m) return;
     const uint32_t q =
@@ -687,7 +695,7 @@ struct ScanCollect {
   // Candidates of mask m and ties of mask q (bits 0-3: elements ia.. of va,
   // bits 4-7: elements ib.. of vb).
   __device__ __forceinline__ void put_masked(uint32_t m, uint32_t q, int64_t ia, const float4& va,
-                                             int64_t ib, const float4& vb) const {
+                                             int64_t ib, const float4& vb) {
     if (TIES && q) put_ties(q, ia, ib);
     if (!m) return;
     uint32_t pos = atomicAdd(ncand, (uint32_t)__popc(m));
@@ -705,26 +713,34 @@ struct ScanCollect {
   }
   // E4M3 unit of 16 raw bytes from index i0 on, tau1 > +0 with byte
   // pattern t (repeated in the four bytes of t4): bytes compare as signed
-  // integers in the order of the values, so the admission and the tie test
-  // are packed byte compares, and only the kept scores are widened.
-  __device__ __forceinline__ void put_e4m3_unit(int64_t i0, const uint4& u, uint32_t t4) const {
-    const uint32_t ge = byte_flags(__vcmpges4(u.x, t4)) | (byte_flags(__vcmpges4(u.y, t4)) << 4) |
-                        (byte_flags(__vcmpges4(u.z, t4)) << 8) |
-                        (byte_flags(__vcmpges4(u.w, t4)) << 12);
-    const uint32_t eq = byte_flags(__vcmpeq4(u.x, t4)) | (byte_flags(__vcmpeq4(u.y, t4)) << 4) |
-                        (byte_flags(__vcmpeq4(u.z, t4)) << 8) |
-                        (byte_flags(__vcmpeq4(u.w, t4)) << 12);
-    if (eq) {
-      uint32_t q = eq;
-      uint32_t t = atomicAdd(neq, (uint32_t)__popc(q));
-      while (q && t < tie_cap) {
-        const uint32_t e = (uint32_t)__ffs(q) - 1u;
-        q &= q - 1u;
-        ties[t++] = (uint32_t)(i0 + e);
+  // integers in the order of the values, so the tie and the candidate tests
+  // are packed byte compares, a unit's ties are counted from the compare
+  // words once the tie list is full, and only the candidates are widened.
+  __device__ __forceinline__ void put_e4m3_unit(int64_t i0, const uint4& u, uint32_t t4) {
+    const uint32_t e0 = __vcmpeq4(u.x, t4), e1 = __vcmpeq4(u.y, t4), e2 = __vcmpeq4(u.z, t4),
+                   e3 = __vcmpeq4(u.w, t4);
+    const uint32_t g0 = __vcmpgts4(u.x, t4), g1 = __vcmpgts4(u.y, t4), g2 = __vcmpgts4(u.z, t4),
+                   g3 = __vcmpgts4(u.w, t4);
+    if (e0 | e1 | e2 | e3) {
+      if (full) {
+        // every tie sets all 8 bits of its byte in the compare word
+        xeq += (uint32_t)(__popc(e0) + __popc(e1) + __popc(e2) + __popc(e3)) >> 3;
+      } else {
+        uint32_t q = byte_flags(e0) | (byte_flags(e1) << 4) | (byte_flags(e2) << 8) |
+                     (byte_flags(e3) << 12);
+        const uint32_t c = (uint32_t)__popc(q);
+        uint32_t t = atomicAdd(neq, c);
+        if (t + c >= tie_cap) full = true;
+        while (q && t < tie_cap) {
+          const uint32_t e = (uint32_t)__ffs(q) - 1u;
+          q &= q - 1u;
+          ties[t++] = (uint32_t)(i0 + e);
+        }
       }
     }
-    uint32_t m = ge & ~eq;
-    if (!m) return;
+    if (!(g0 | g1 | g2 | g3)) return;
+    uint32_t m = byte_flags(g0) | (byte_flags(g1) << 4) | (byte_flags(g2) << 8) |
+                 (byte_flags(g3) << 12);
     uint32_t pos = atomicAdd(ncand, (uint32_t)__popc(m));
     do {
       const uint32_t e = (uint32_t)__ffs(m) - 1u;
@@ -741,9 +757,34 @@ struct ScanCollect {
   __device__ static __forceinline__ uint32_t byte_flags(uint32_t c) {
     return ((c >> 7) & 1u) | ((c >> 14) & 2u) | ((c >> 21) & 4u) | ((c >> 28) & 8u);
   }
+  // bfloat16 unit of 8 raw patterns from index i0 on, tau1 > +0 with pattern
+  // t (in both halves of t2): patterns compare as signed 16-bit integers in
+  // the order of the values, so the admission is a packed compare and only
+  // the admitted scores are turned into keys (a positive bfloat16 widens to
+  // bits << 16, whose order key is those bits with the sign bit set).
+  __device__ __forceinline__ void put_bf16_unit(int64_t i0, const uint4& u, uint32_t t2) {
+    uint32_t m = half_flags(__vcmpges2(u.x, t2)) | (half_flags(__vcmpges2(u.y, t2)) << 2) |
+                 (half_flags(__vcmpges2(u.z, t2)) << 4) | (half_flags(__vcmpges2(u.w, t2)) << 6);
+    if (!m) return;
+    uint32_t pos = atomicAdd(ncand, (uint32_t)__popc(m));
+    do {
+      const uint32_t e = (uint32_t)__ffs(m) - 1u;
+      m &= m - 1u;
+      const uint32_t wd = e < 4u ? (e < 2u ? u.x : u.y) : (e < 6u ? u.z : u.w);
+      const uint32_t b = (wd >> (16u * (e & 1u))) & 0xFFFFu;
+      const uint2 ent = make_uint2((uint32_t)(i0 + e), (b << 16) | 0x80000000u);
+      if (pos < (uint32_t)CAP) cand[pos] = ent;
+      else if (pos < cap) spill[pos - (uint32_t)CAP] = ent;
+      ++pos;
+    } while (m);
+  }
+  // 2-bit mask of the halves that are 0xFFFF in a per-halfword compare result
+  __device__ static __forceinline__ uint32_t half_flags(uint32_t c) {
+    return ((c >> 15) & 1u) | ((c >> 30) & 2u);
+  }
   // Appends the admitted scores among the elements of v selected by vm
   // (element i0 + e is lane e).
-  __device__ __forceinline__ void lane_put(int64_t i0, const float4& v, uint32_t vm) const {
+  __device__ __forceinline__ void lane_put(int64_t i0, const float4& v, uint32_t vm) {
     const uint32_t m = admit_mask(v) & vm;
     if (!m) return;
     const uint32_t q = TIES ? (tie_mask(v) & vm) : 0u;
@@ -888,6 +929,11 @@ __device__ __forceinline__ void scan_pass(Ring& R, const E* __restrict__ row, in
         if constexpr (NG == 1) {
           f.lane_put2(off + (int64_t)P16 * j0, Elem<E>::group(u0, 0), h0, off + (int64_t)P16 * j1,
                       Elem<E>::group(u1, 0), h1);
+        } else if constexpr (NG == 2 && POS && !TIES) {
+          // bfloat16 above +0: packed 16-bit compares against tau1's pattern
+          const uint32_t t2 = ((uint32_t)thr & 0xFFFFu) * 0x10001u;
+          if (h0) f.put_bf16_unit(off + (int64_t)P16 * j0, u0, t2);
+          if (h1) f.put_bf16_unit(off + (int64_t)P16 * j1, u1, t2);
         } else if constexpr (NG == 2) {
           if (h0) f.lane_put2(off + (int64_t)P16 * j0, Elem<E>::group(u0, 0), true,
                               off + (int64_t)P16 * j0 + 4, Elem<E>::group(u0, 1), true);

@@ -264,15 +264,25 @@ __device__ uint32_t scan_collect(const E* row, int64_t s0, int64_t s1, Ring& R,
   const float tau1 = key_to_float(key1);
   const uint32_t cap = spill ? (uint32_t)CAP_ALL : (uint32_t)CAP;
   constexpr bool TIES = sizeof(E) == 1;  // a tie list for E4M3 rows only
+  uint32_t xeq = 0;
   if (tau1 > 0.0f) {
     ScanCollect<true, TIES> f{__float_as_uint(tau1), c.cand, spill, cap, &S.ncand,
-                              tl.idx, tl.cap, tl.n};
+                              tl.idx, tl.cap, tl.n, 0u, false};
     scan_pass(R, row, s0, s1, f, lflags, primed);
+    xeq = f.xeq;
   } else {
-    ScanCollect<false, TIES> f{key1, c.cand, spill, cap, &S.ncand, tl.idx, tl.cap, tl.n};
+    ScanCollect<false, TIES> f{key1, c.cand, spill, cap, &S.ncand, tl.idx, tl.cap, tl.n, 0u,
+                               false};
     scan_pass(R, row, s0, s1, f, lflags, primed);
+    xeq = f.xeq;
   }
   __syncthreads();
+  if constexpr (TIES) {
+    // the ties counted in registers once the list was full join the count
+    const uint32_t x = block_sum(xeq, S);
+    if (threadIdx.x == 0 && x) atomicAdd(tl.n, x);
+    __syncthreads();
+  }
   phase_mark(S, 2);
   const uint32_t c0 = tally_candidates(c.cand, spill, min(S.ncand, cap), key0, sb, c.hist);
   const uint32_t total = block_sum(c0, S);
