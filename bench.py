@@ -511,6 +511,11 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# Sources whose text decides a selector launch's DRAM traffic (the kernels and
+# the host defaults that reach them, such as the L2 prefetch distance).
+FINGERPRINT_SOURCES = ("score_elem.cuh", "topk_device.cuh", "topk_kernels.cu", "topk_launch.h",
+                       "topk_api.cu")
+
 SAMPLING_KNOBS = ("stride", "rho0", "rho1", "sample_min_len", "long_len", "long_stride",
                   "long_rho0", "long_rho1")
 
@@ -521,8 +526,7 @@ def kernel_fingerprint(params, kind, grid, elem_bytes=4):
     score element size."""
     import hashlib
     h = hashlib.sha256()
-    for name in ("score_elem.cuh", "topk_device.cuh", "topk_kernels.cu", "topk_launch.h",
-                 "topk_api.cu"):
+    for name in FINGERPRINT_SOURCES:
         with open(os.path.join(ROOT, "exact_top_sparse_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     launch = {"sampling": {k: params[k] for k in SAMPLING_KNOBS}, "kind": kind, "grid": grid,

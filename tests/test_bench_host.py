@@ -40,7 +40,7 @@ def _tree(tmp_path, fingerprint_of):
     src = SRC
     dst = tmp_path / "exact_top_sparse_gb300" / "csrc"
     dst.mkdir(parents=True)
-    for name in ("score_elem.cuh", "topk_device.cuh", "topk_kernels.cu", "topk_launch.h"):
+    for name in bench.FINGERPRINT_SOURCES:
         shutil.copy(os.path.join(src, name), dst / name)
     (tmp_path / "profiles").mkdir()
     rec = {"kernel_fingerprint": fingerprint_of, "dram_bytes_per_valid_byte": 1.25}
