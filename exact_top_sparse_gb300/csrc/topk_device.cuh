@@ -636,6 +636,27 @@ __device__ __forceinline__ uint2 cand_at(const uint2* cand, const uint2* spill, 
 // (TIES = false) ties are ordinary candidates, which keeps their scan loop
 // leaner (measured 13 % and 5 % faster), and a rare long tie run takes the
 // overflow path.
+// SWAR lane tests against a positive threshold t, exact per lane: the bytes
+// (E4M3) or 16-bit halves (bfloat16) of w read as signed integers.  A lane
+// >= t has its top bit clear, and then its low bits plus (top - t) reach the
+// top bit without a carry into the next lane (the sum stays below 2^8 or
+// 2^16).  k8 = (0x80 - t) * 0x01010101, g8 = (0x7F - t) * 0x01010101,
+// t4 = t * 0x01010101, k16 = (0x8000 - t) * 0x00010001.  The result has the
+// top bit of every passing lane set and nothing else.
+__device__ __forceinline__ uint32_t swar_ge8(uint32_t w, uint32_t k8) {
+  return ((w & 0x7F7F7F7Fu) + k8) & ~w & 0x80808080u;
+}
+__device__ __forceinline__ uint32_t swar_gt8(uint32_t w, uint32_t g8) {
+  return ((w & 0x7F7F7F7Fu) + g8) & ~w & 0x80808080u;
+}
+__device__ __forceinline__ uint32_t swar_eq8(uint32_t w, uint32_t t4) {
+  const uint32_t x = w ^ t4;  // a lane equal to t is zero here
+  return ~(((x & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | x) & 0x80808080u;
+}
+__device__ __forceinline__ uint32_t swar_ge16(uint32_t w, uint32_t k16) {
+  return ((w & 0x7FFF7FFFu) + k16) & ~w & 0x80008000u;
+}
+
 template <bool POS, bool TIES>
 struct ScanCollect {
   uint32_t t1;  // POS: bits of tau1; otherwise key(tau1)
@@ -714,17 +735,18 @@ struct ScanCollect {
   // E4M3 unit of 16 raw bytes from index i0 on, tau1 > +0 with byte
   // pattern t (repeated in the four bytes of t4): bytes compare as signed
   // integers in the order of the values, so the tie and the candidate tests
-  // are packed byte compares, a unit's ties are counted from the compare
-  // words once the tie list is full, and only the candidates are widened.
+  // are SWAR lane tests, a unit's ties are counted from the test words once
+  // the tie list is full, and only the candidates are widened.
   __device__ __forceinline__ void put_e4m3_unit(int64_t i0, const uint4& u, uint32_t t4) {
-    const uint32_t e0 = __vcmpeq4(u.x, t4), e1 = __vcmpeq4(u.y, t4), e2 = __vcmpeq4(u.z, t4),
-                   e3 = __vcmpeq4(u.w, t4);
-    const uint32_t g0 = __vcmpgts4(u.x, t4), g1 = __vcmpgts4(u.y, t4), g2 = __vcmpgts4(u.z, t4),
-                   g3 = __vcmpgts4(u.w, t4);
+    const uint32_t g8 = 0x7F7F7F7Fu - t4;  // (0x7F - t) in every byte
+    const uint32_t e0 = swar_eq8(u.x, t4), e1 = swar_eq8(u.y, t4), e2 = swar_eq8(u.z, t4),
+                   e3 = swar_eq8(u.w, t4);
+    const uint32_t g0 = swar_gt8(u.x, g8), g1 = swar_gt8(u.y, g8), g2 = swar_gt8(u.z, g8),
+                   g3 = swar_gt8(u.w, g8);
     if (e0 | e1 | e2 | e3) {
       if (full) {
-        // every tie sets all 8 bits of its byte in the compare word
-        xeq += (uint32_t)(__popc(e0) + __popc(e1) + __popc(e2) + __popc(e3)) >> 3;
+        // one bit per tie in the test words
+        xeq += (uint32_t)(__popc(e0) + __popc(e1) + __popc(e2) + __popc(e3));
       } else {
         uint32_t q = byte_flags(e0) | (byte_flags(e1) << 4) | (byte_flags(e2) << 8) |
                      (byte_flags(e3) << 12);
@@ -758,13 +780,14 @@ struct ScanCollect {
     return ((c >> 7) & 1u) | ((c >> 14) & 2u) | ((c >> 21) & 4u) | ((c >> 28) & 8u);
   }
   // bfloat16 unit of 8 raw patterns from index i0 on, tau1 > +0 with pattern
-  // t (in both halves of t2): patterns compare as signed 16-bit integers in
-  // the order of the values, so the admission is a packed compare and only
-  // the admitted scores are turned into keys (a positive bfloat16 widens to
-  // bits << 16, whose order key is those bits with the sign bit set).
-  __device__ __forceinline__ void put_bf16_unit(int64_t i0, const uint4& u, uint32_t t2) {
-    uint32_t m = half_flags(__vcmpges2(u.x, t2)) | (half_flags(__vcmpges2(u.y, t2)) << 2) |
-                 (half_flags(__vcmpges2(u.z, t2)) << 4) | (half_flags(__vcmpges2(u.w, t2)) << 6);
+  // t (k16 = (0x8000 - t) in both halves): patterns compare as signed 16-bit
+  // integers in the order of the values, so the admission is a SWAR lane
+  // test and only the admitted scores are turned into keys (a positive
+  // bfloat16 widens to bits << 16, whose order key is those bits with the
+  // sign bit set).
+  __device__ __forceinline__ void put_bf16_unit(int64_t i0, const uint4& u, uint32_t k16) {
+    uint32_t m = half_flags(swar_ge16(u.x, k16)) | (half_flags(swar_ge16(u.y, k16)) << 2) |
+                 (half_flags(swar_ge16(u.z, k16)) << 4) | (half_flags(swar_ge16(u.w, k16)) << 6);
     if (!m) return;
     uint32_t pos = atomicAdd(ncand, (uint32_t)__popc(m));
     do {
@@ -816,21 +839,6 @@ __device__ __forceinline__ int32_t max_operand(const float4& v) {
     return max(max(a, b), max(c, d));
   }
   return (int32_t)(max(max(fkey(v.x), fkey(v.y)), max(fkey(v.z), fkey(v.w))) ^ 0x80000000u);
-}
-
-// The largest of the eight bfloat16 patterns of a 16-byte unit, each read as
-// a signed 16-bit integer (for values above +0 this is their order).
-__device__ __forceinline__ int32_t max_bf16_pattern(const uint4& u) {
-  const uint32_t c = __vmaxs2(__vmaxs2(u.x, u.y), __vmaxs2(u.z, u.w));
-  return max((int32_t)(int16_t)(c & 0xFFFFu), (int32_t)(int16_t)(c >> 16));
-}
-
-// The largest of the sixteen E4M3 bytes of a 16-byte unit, each read as a
-// signed 8-bit integer (for values above +0 this is their order).
-__device__ __forceinline__ int32_t max_e4m3_pattern(const uint4& u) {
-  const uint32_t c = __vmaxs4(__vmaxs4(u.x, u.y), __vmaxs4(u.z, u.w));
-  return max(max((int32_t)(int8_t)(c & 0xFFu), (int32_t)(int8_t)((c >> 8) & 0xFFu)),
-             max((int32_t)(int8_t)((c >> 16) & 0xFFu), (int32_t)(int8_t)(c >> 24)));
 }
 
 // The certify+collect pass over [start, end) of `row`, whose first `primed`
@@ -889,6 +897,9 @@ __device__ __forceinline__ void scan_pass(Ring& R, const E* __restrict__ row, in
     else if constexpr (NG == 4 && POS)
       thr = Elem<uint8_t>::pattern_of_positive(__uint_as_float(f.t1));
     else thr = POS ? (int32_t)f.t1 : (int32_t)(f.t1 ^ 0x80000000u);
+    // SWAR constant of the narrow positive thresholds: (top - t) in every lane
+    const uint32_t kk = NG == 2 ? (0x8000u - (uint32_t)thr) * 0x00010001u
+                                : (0x80u - (uint32_t)thr) * 0x01010101u;
     for (uint32_t c = 0; c < nchunks; ++c) {
       const uint32_t q = R.seq + c, s = q % STAGES, use = q / STAGES;
       if (!mbar_wait(&R.full[s], use & 1u, R.abort)) lflags |= F_TIMEOUT;
@@ -903,13 +914,21 @@ __device__ __forceinline__ void scan_pass(Ring& R, const E* __restrict__ row, in
       int32_t m0, m1;
       if constexpr (NG == 2 && POS) {
         // bfloat16 with tau1 > +0: the raw 16-bit patterns compare as signed
-        // integers in the order of the values; two per instruction
-        m0 = max_bf16_pattern(u0);
-        m1 = max_bf16_pattern(u1);
+        // integers in the order of the values; two per SWAR lane test
+        const uint32_t a0 = swar_ge16(u0.x, kk) | swar_ge16(u0.y, kk) | swar_ge16(u0.z, kk) |
+                            swar_ge16(u0.w, kk);
+        const uint32_t a1 = swar_ge16(u1.x, kk) | swar_ge16(u1.y, kk) | swar_ge16(u1.z, kk) |
+                            swar_ge16(u1.w, kk);
+        m0 = a0 ? thr : INT32_MIN;
+        m1 = a1 ? thr : INT32_MIN;
       } else if constexpr (NG == 4 && POS) {
-        // E4M3 with tau1 > +0: the raw bytes, four per instruction
-        m0 = max_e4m3_pattern(u0);
-        m1 = max_e4m3_pattern(u1);
+        // E4M3 with tau1 > +0: the raw bytes, four per SWAR lane test
+        const uint32_t a0 = swar_ge8(u0.x, kk) | swar_ge8(u0.y, kk) | swar_ge8(u0.z, kk) |
+                            swar_ge8(u0.w, kk);
+        const uint32_t a1 = swar_ge8(u1.x, kk) | swar_ge8(u1.y, kk) | swar_ge8(u1.z, kk) |
+                            swar_ge8(u1.w, kk);
+        m0 = a0 ? thr : INT32_MIN;
+        m1 = a1 ? thr : INT32_MIN;
       } else {
         m0 = max_operand<POS>(Elem<E>::group(u0, 0));
         m1 = max_operand<POS>(Elem<E>::group(u1, 0));
@@ -931,9 +950,8 @@ __device__ __forceinline__ void scan_pass(Ring& R, const E* __restrict__ row, in
                       Elem<E>::group(u1, 0), h1);
         } else if constexpr (NG == 2 && POS && !TIES) {
           // bfloat16 above +0: packed 16-bit compares against tau1's pattern
-          const uint32_t t2 = ((uint32_t)thr & 0xFFFFu) * 0x10001u;
-          if (h0) f.put_bf16_unit(off + (int64_t)P16 * j0, u0, t2);
-          if (h1) f.put_bf16_unit(off + (int64_t)P16 * j1, u1, t2);
+          if (h0) f.put_bf16_unit(off + (int64_t)P16 * j0, u0, kk);
+          if (h1) f.put_bf16_unit(off + (int64_t)P16 * j1, u1, kk);
         } else if constexpr (NG == 2) {
           if (h0) f.lane_put2(off + (int64_t)P16 * j0, Elem<E>::group(u0, 0), true,
                               off + (int64_t)P16 * j0 + 4, Elem<E>::group(u0, 1), true);
