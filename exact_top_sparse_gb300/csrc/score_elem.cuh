@@ -25,6 +25,8 @@ struct Elem;
 template <>
 struct Elem<float> {
   static constexpr int kSize = 4, kPer16 = 4;
+  // low bits that are zero in the FP32 bits of every value (none)
+  static constexpr int kKeyQuantum = 0;
   __device__ static __forceinline__ float load(const float* p) { return *p; }
   __device__ static __forceinline__ float load_keep(const float* p, uint64_t pol) {
     return ld_keep(p, pol);
@@ -38,6 +40,9 @@ struct Elem<float> {
 template <>
 struct Elem<uint16_t> {
   static constexpr int kSize = 2, kPer16 = 8;
+  // a widened bfloat16 has 16 zero low bits: distinct values' order keys
+  // lie at least 2^16 apart (on each side of zero)
+  static constexpr int kKeyQuantum = 16;
   __device__ static __forceinline__ float widen(uint32_t b) { return __uint_as_float(b << 16); }
   __device__ static __forceinline__ float load(const uint16_t* p) { return widen(*p); }
   __device__ static __forceinline__ float load_keep(const uint16_t* p, uint64_t pol) {
@@ -59,6 +64,8 @@ struct Elem<uint16_t> {
 template <>
 struct Elem<uint8_t> {
   static constexpr int kSize = 1, kPer16 = 16;
+  // a widened E4M3 value has at most 3 significant bits: 20 zero low bits
+  static constexpr int kKeyQuantum = 20;
   __device__ static __forceinline__ float widen(uint32_t b) {
     const uint32_t e = (b >> 3) & 0xFu, m = b & 7u;
     const float mag = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : (float)m * 0x1p-9f;

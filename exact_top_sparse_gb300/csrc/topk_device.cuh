@@ -1154,7 +1154,10 @@ struct RowSrc {  // a row in global memory, streamed through the ring
 // Exact selection of Kp keys from the frontier of `src` (keys in
 // [bins.lo, bins.hi]), given `hist`, the complete histogram of that frontier
 // under `bins`.  Emits into out[] through S.nout.  Every thread must call.
-template <class Src>
+// QL: the source's scores have QL zero low bits in their FP32 patterns
+// (narrow types), so a boundary bin narrower than 2^QL keys on one side of
+// zero holds a single score value, and any Kr of its keys finish the row.
+template <int QL, class Src>
 __device__ void refine(const Src& src, Bins bins, uint32_t Kp, uint32_t* hist, uint2* cand,
                        int32_t* out, int32_t K, Shared& S, uint32_t& lflags) {
   for (int guard = 0; guard < 40; ++guard) {
@@ -1168,8 +1171,11 @@ __device__ void refine(const Src& src, Bins bins, uint32_t Kp, uint32_t* hist, u
     const uint32_t Kr = Kp - above;
     const uint32_t nlo = bins.bin_lo(b), nhi = bins.bin_hi(b);
     uint32_t mode;
+    const bool one_value =
+        nlo == nhi || (QL > 0 && nhi - nlo < (1u << QL) &&
+                       (nlo >= 0x80000000u || nhi < 0x80000000u));
     if (hb == Kr) mode = TAKE_ALL;
-    else if (nlo == nhi) mode = TAKE_SOME;
+    else if (one_value) mode = TAKE_SOME;
     else if (hb <= (uint32_t)SMALL) mode = SMALL_SORT;
     else if (Src::kRow && hb <= (uint32_t)CAP) mode = COLLECT;
     else mode = NEXT_HIST;
@@ -1206,7 +1212,7 @@ __device__ void refine(const Src& src, Bins bins, uint32_t Kp, uint32_t* hist, u
     if constexpr (Src::kRow) {
       if (mode == COLLECT) {
         const CandSrc cs{cand, nullptr, min(S.ncand, (uint32_t)CAP)};
-        refine(cs, nb, Kr, hist, cand, out, K, S, lflags);
+        refine<QL>(cs, nb, Kr, hist, cand, out, K, S, lflags);
         return;
       }
     }

@@ -185,7 +185,8 @@ __device__ void exact_row_stream(const E* row, int64_t len, int32_t* out, int32_
   HistF hf{bins, c.hist};
   ring_pass(R, row, 0, len, hf, lflags);
   __syncthreads();
-  refine(RowSrc<E>{&R, row, len}, bins, (uint32_t)K, c.hist, c.cand, out, K, S, lflags);
+  refine<Elem<E>::kKeyQuantum>(RowSrc<E>{&R, row, len}, bins, (uint32_t)K, c.hist, c.cand, out, K,
+                               S, lflags);
 }
 
 // Exact selection of a row staged in shared memory (element i at buf[i]):
@@ -209,7 +210,7 @@ __device__ void select_staged(const E* buf, int64_t len, int32_t* out, int32_t K
   HistF hf{bins, hist};
   src.for_each(hf, lflags);
   __syncthreads();
-  refine(src, bins, (uint32_t)K, hist, nullptr, out, K, S, lflags);
+  refine<Elem<E>::kKeyQuantum>(src, bins, (uint32_t)K, hist, nullptr, out, K, S, lflags);
 }
 
 // Rows an unsampled row can be staged for in the candidate buffer (which
@@ -329,7 +330,8 @@ __device__ int32_t select_after_scan(const E* row, int64_t len, int32_t* out, in
   if (C1 >= (uint32_t)K && !overflow) {
     if (!TIES || Cgt >= (uint32_t)K) {
       // the K-th largest score is above tau1: the ties cannot be selected
-      refine(CandSrc{c.cand, spill, Cgt}, sb, (uint32_t)K, c.hist, c.cand, out, K, S, lflags);
+      refine<Elem<E>::kKeyQuantum>(CandSrc{c.cand, spill, Cgt}, sb, (uint32_t)K, c.hist, c.cand,
+                                   out, K, S, lflags);
     } else {
       // the K-th largest score is tau1: every score above it, then any
       // K - Cgt of the ties (Cgt < K <= CAP: every candidate is on chip)
@@ -350,7 +352,8 @@ __device__ int32_t select_after_scan(const E* row, int64_t len, int32_t* out, in
     __syncthreads();
     C0 = block_sum(sf.c0, S);
     path = (C0 >= (uint32_t)K) ? PATH_TAU0 : PATH_TAU1;
-    refine(RowSrc<E>{&R, row, len}, sb, (uint32_t)K, c.hist, c.cand, out, K, S, lflags);
+    refine<Elem<E>::kKeyQuantum>(RowSrc<E>{&R, row, len}, sb, (uint32_t)K, c.hist, c.cand, out, K,
+                                 S, lflags);
   } else {
     // C(tau1) < K: every admitted score belongs to the answer; the remaining
     // K - C(tau1) come from the scores below tau1, selected exactly from the
@@ -385,7 +388,8 @@ __device__ int32_t select_after_scan(const E* row, int64_t len, int32_t* out, in
         clear_hist(c.hist);
         __syncthreads();
         hist_candidates(c.cand, spill, n2, bb, c.hist);
-        refine(CandSrc{c.cand, spill, n2}, bb, need, c.hist, c.cand, out, K, S, lflags);
+        refine<Elem<E>::kKeyQuantum>(CandSrc{c.cand, spill, n2}, bb, need, c.hist, c.cand, out, K,
+                                     S, lflags);
         return path;
       }
     }
@@ -396,7 +400,8 @@ __device__ int32_t select_after_scan(const E* row, int64_t len, int32_t* out, in
     HistF hf{rb, c.hist};
     ring_pass(R, row, 0, len, hf, lflags);
     __syncthreads();
-    refine(RowSrc<E>{&R, row, len}, rb, (uint32_t)K - C1, c.hist, c.cand, out, K, S, lflags);
+    refine<Elem<E>::kKeyQuantum>(RowSrc<E>{&R, row, len}, rb, (uint32_t)K - C1, c.hist, c.cand,
+                                 out, K, S, lflags);
   }
   return path;
 }
