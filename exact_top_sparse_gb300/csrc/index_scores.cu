@@ -66,7 +66,13 @@ constexpr uint32_t OFF_W = OFF_A + STAGES * A_BYTES;       // QB * HEADS floats
 constexpr uint32_t OFF_BAR = OFF_W + QB * HEADS * 4;
 constexpr uint32_t NBAR = 2 * STAGES + 2 + 4 + 1;
 constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;      // + alignment slack
+// Gated scores of the fused path are staged in shared memory, per query of
+// the unit and per epilogue warp (no atomics while scoring), and flushed to
+// the query's candidate area once per unit.
+constexpr uint32_t STG_W = 256;                             // entries per query, warp and unit
+constexpr uint32_t OFF_STG = OFF_MISC + 128;
+constexpr uint32_t SMEM_BYTES = OFF_STG + QB * 4 * STG_W * 8 + 1024;  // + alignment slack
+static_assert(SMEM_BYTES <= 232448, "shared memory plan exceeds the opt-in limit");
 
 __device__ uint32_t g_idx_status;  // OR of error bits since the last read
 
@@ -124,6 +130,24 @@ __device__ __forceinline__ void bar_drain(uint32_t bar, uint32_t parity) {
         : "memory");
     if (ok || gtime() - t0 > 100000000ull) return;
   }
+}
+
+// Two-lane FP32 fused multiply-add (fma.rn.f32x2, sm_100 family): lanes are
+// the low and high halves of each 64-bit operand.
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ float sum2(uint64_t x) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(x));
+  return lo + hi;
 }
 
 __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
@@ -201,6 +225,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   const uint32_t drain = bars + 8u * (2 * STAGES + 6);
   uint32_t* misc = reinterpret_cast<uint32_t*>(sm + OFF_MISC);
   volatile uint32_t* abort_flag = misc + 1;
+  uint32_t* stg_n = misc + 2;      // [QB][4] scores each epilogue warp admitted in this unit
+  uint32_t* stg_base = misc + 18;  // [QB] where the unit's go in the query's candidate area
+  uint2* stg = reinterpret_cast<uint2*>(sm + OFF_STG);  // [QB][4][STG_W]
   const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31u;
 
   if (tid == 0) {
@@ -336,14 +363,16 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (uint32_t i = etid; i < (uint32_t)(QB * HEADS); i += 128u)
         w_s[i] = a.w[(int64_t)qb * QB * HEADS + i];
       asm volatile("bar.sync 1, 128;" ::: "memory");
+      uint32_t cnt[QB];  // this warp's admitted scores per query in the unit (warp-uniform)
+#pragma unroll
+      for (int q = 0; q < QB; ++q) cnt[q] = 0u;
       int32_t lenq[QB];
       float tau1q[QB];
 #pragma unroll
       for (int q = 0; q < QB; ++q) {
         lenq[q] = a.lens ? a.lens[qb * QB + q] : a.S;
-        tau1q[q] = a.rows ? __ldcg(reinterpret_cast<const float*>(
-                                a.rows + (size_t)(qb * QB + q) * tk::kFusedRowBytes + tk::kKvTau1Off))
-                          : 0.0f;
+        const uint8_t* rs = a.rows + (size_t)(qb * QB + q) * tk::kFusedRowBytes;
+        tau1q[q] = a.rows ? __ldcg(reinterpret_cast<const float*>(rs + tk::kKvTau1Off)) : 0.0f;
       }
       const int32_t te = unit_end(a, qb, t0, t1);
       // tiles past every query's valid length: -inf, no accumulator
@@ -365,7 +394,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int q = 0; q < QB; ++q) {
           uint32_t v[32];
-          float acc = 0.0f;
+          uint64_t acc = 0ull;  // partial sums of the even and of the odd heads
 #pragma unroll
           for (int h0 = 0; h0 < HEADS; h0 += 32) {
             const uint32_t taddr = tmem + ((quarter * 32u) << 16) + buf * NCOL + q * HEADS + h0;
@@ -381,17 +410,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                   "=r"(v[30]), "=r"(v[31])
                 : "r"(taddr));
             asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-            const float4* w4 = reinterpret_cast<const float4*>(w_s + q * HEADS + h0);
+            // the weights of heads h0+j, h0+j+1 as one 64-bit pair
+            const uint64_t* w2 = reinterpret_cast<const uint64_t*>(w_s + q * HEADS + h0);
 #pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-              const float4 ww = w4[j >> 2];
-              acc = fmaf(fmaxf(__uint_as_float(v[j]), 0.0f), ww.x, acc);
-              acc = fmaf(fmaxf(__uint_as_float(v[j + 1]), 0.0f), ww.y, acc);
-              acc = fmaf(fmaxf(__uint_as_float(v[j + 2]), 0.0f), ww.z, acc);
-              acc = fmaf(fmaxf(__uint_as_float(v[j + 3]), 0.0f), ww.w, acc);
+            for (int j = 0; j < 32; j += 2) {
+              const uint64_t r2 = pack2(fmaxf(__uint_as_float(v[j]), 0.0f),
+                                        fmaxf(__uint_as_float(v[j + 1]), 0.0f));
+              acc = ffma2(r2, w2[j >> 1], acc);
             }
           }
-          res[q] = acc;
+          res[q] = sum2(acc);
         }
         // the accumulator is in registers: hand the buffer back to the MMA
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -405,27 +433,53 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
         if (a.rows) {
-          // the gate: scores >= tau1 of the query join its candidates (one
-          // atomic per warp and query for the warp's admitted keys)
+          // the gate: scores >= tau1 of the query are staged in this warp's
+          // region (positions from the ballot, no atomics)
 #pragma unroll
           for (int q = 0; q < QB; ++q) {
             const bool adm = key < a.S && key < lenq[q] && res[q] >= tau1q[q];
             const uint32_t m = __ballot_sync(0xffffffffu, adm);
-            if (m) {
-              uint8_t* rs = a.rows + (size_t)(qb * QB + q) * tk::kFusedRowBytes;
-              const uint32_t leader = __ffs(m) - 1u;
-              uint32_t base = 0;
-              if (lane == leader)
-                base = atomicAdd(reinterpret_cast<uint32_t*>(rs + tk::kKvNcandOff),
-                                 (uint32_t)__popc(m));
-              base = __shfl_sync(0xffffffffu, base, leader);
-              if (adm) {
-                const uint32_t pos = base + (uint32_t)__popc(m & ((1u << lane) - 1u));
-                if (pos < tk::kKvCandCap)
-                  reinterpret_cast<uint2*>(rs + tk::kKvCandOff)[pos] =
-                      make_uint2((uint32_t)key, tk::fkey(res[q]));
-              }
-            }
+            const uint32_t pos = cnt[q] + (uint32_t)__popc(m & ((1u << lane) - 1u));
+            if (adm && pos < STG_W)
+              stg[(q * 4 + quarter) * STG_W + pos] = make_uint2((uint32_t)key, tk::fkey(res[q]));
+            cnt[q] += (uint32_t)__popc(m);
+          }
+        }
+      }
+      if (a.rows) {
+        // flush the unit's staged candidates: one global atomic per query
+        // reserves their place (and counts C(tau1) exactly, kept or not); a
+        // query whose staging overflowed is marked, and its row is then
+        // served from the written scores
+        if (lane == 0)
+#pragma unroll
+          for (int q = 0; q < QB; ++q) stg_n[q * 4 + quarter] = cnt[q];
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (etid < (uint32_t)QB) {
+          uint8_t* rs = a.rows + (size_t)(qb * QB + etid) * tk::kFusedRowBytes;
+          uint32_t n = 0u;
+          bool lost = false;
+#pragma unroll
+          for (int wq = 0; wq < 4; ++wq) {
+            n += stg_n[etid * 4 + wq];
+            lost = lost || stg_n[etid * 4 + wq] > STG_W;
+          }
+          if (lost) atomicOr(reinterpret_cast<uint32_t*>(rs + tk::kKvOvfOff), 1u);
+          uint32_t* count = reinterpret_cast<uint32_t*>(rs + tk::kKvNcandOff);
+          stg_base[etid] = n ? atomicAdd(count, n) : 0u;
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+#pragma unroll
+        for (int q = 0; q < QB; ++q) {
+          uint2* dst = reinterpret_cast<uint2*>(a.rows + (size_t)(qb * QB + q) * tk::kFusedRowBytes +
+                                                tk::kKvCandOff);
+          uint32_t g = stg_base[q];
+#pragma unroll
+          for (int wq = 0; wq < 4; ++wq) {
+            const uint32_t n = min(stg_n[q * 4 + wq], STG_W);
+            for (uint32_t j = etid; j < n; j += 128u)
+              if (g + j < tk::kKvCandCap) dst[g + j] = stg[(q * 4 + wq) * STG_W + j];
+            g += n;
           }
         }
       }

@@ -102,6 +102,7 @@ static_assert(CTA_AREA_BYTES % 256 == 0, "CTA areas keep 256-byte alignment");
 static_assert(sizeof(KvHdr) <= KV_HIST_OFF, "KV row header too large");
 static_assert(KV_ROW_BYTES == kKvRowBytes, "kKvRowBytes must match the KV-split row layout");
 static_assert(offsetof(KvHdr, ncand) == kKvNcandOff && offsetof(KvHdr, tau1) == kKvTau1Off &&
+                  offsetof(KvHdr, ovf) == kKvOvfOff &&
                   KV_CAND_OFF == kKvCandOff && (size_t)CAP_ALL == kKvCandCap &&
                   align_up(KV_CAND_OFF + (size_t)CAP_ALL * sizeof(uint2), 256) == kFusedRowBytes,
               "fused row state must follow the KV-split row layout");
@@ -877,7 +878,20 @@ __global__ void __launch_bounds__(THREADS, 2)
     return;
   }
   const uint32_t Cgt = __ldcg(&h->ncand);
-  const bool overflow = Cgt > (uint32_t)CAP_ALL;
+  // some admitted scores were not kept (the score kernel's staging of a unit
+  // overflowed): the count C(tau1) is still exact, the candidates are not
+  const bool lost = __ldcg(&h->ovf) != 0u;
+  if (lost && Cgt < (uint32_t)Kr) {
+    // fewer than K admitted, and not all of them at hand: the exact
+    // selection over the whole written row
+    lflags |= F_OVERFLOW | F_RECOVERY;
+    exact_row_stream(row, len, out, Kr, R, c, lflags);
+    finish_row(S, out, Kr, K, lflags, diag, r, PATH_RECOVERY, key_to_float(key0),
+               key_to_float(key1), 0, Cgt);
+    ring_drain(R);
+    return;
+  }
+  const bool overflow = lost || Cgt > (uint32_t)CAP_ALL;
   const uint32_t nkeep = min(Cgt, (uint32_t)CAP_ALL), nload = min(Cgt, (uint32_t)CAP);
   for (uint32_t j = threadIdx.x; j < nload; j += THREADS) {
     const uint2* p = gcand + j;

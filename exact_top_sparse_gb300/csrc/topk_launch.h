@@ -57,6 +57,7 @@ constexpr size_t kKvRowBytes = 155904;
 // Offsets inside a row state (checked against the KV-split layout where it
 // is defined):
 constexpr size_t kKvNcandOff = 28;      // uint32: admitted scores (counts past the capacity)
+constexpr size_t kKvOvfOff = 36;        // uint32: nonzero when admitted scores were not kept
 constexpr size_t kKvTau1Off = 48;       // float: tau1 (+inf: the row admits nothing)
 constexpr size_t kKvCandOff = 8448;     // uint2 (index, order key) entries
 constexpr uint32_t kKvCandCap = 16384;  // entries kept
