@@ -39,7 +39,11 @@ SM_MHZ = 2070.0  # clock the cycle counts are converted with (GB300 maximum SM c
 
 
 def build_phase_library() -> str:
-    """Compile every translation unit with -DTOPK_PHASE_TIMING and link them."""
+    """Compile every translation unit with -DTOPK_PHASE_TIMING and link them
+    (skipped while the library is newer than every source)."""
+    if os.path.exists(PHASE_LIB) and all(os.path.getmtime(p) <= os.path.getmtime(PHASE_LIB)
+                                         for p in B._inputs()):
+        return PHASE_LIB
     objdir = os.path.join(B.HERE, "_build_phases")
     os.makedirs(objdir, exist_ok=True)
     os.makedirs(B.LIBDIR, exist_ok=True)
