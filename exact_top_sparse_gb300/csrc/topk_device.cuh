@@ -256,6 +256,16 @@ __device__ __forceinline__ void phase_mark(Shared& S, int i) {
 #endif
 }
 
+// Phase timing builds only: counts an event (slot i then holds a count).
+__device__ __forceinline__ void phase_count(Shared& S, int i) {
+#ifdef TOPK_PHASE_TIMING
+  if (threadIdx.x == 0) S.ph[i] += 1;
+#else
+  (void)S;
+  (void)i;
+#endif
+}
+
 // Exclusive prefix sum over all THREADS threads (every thread must call).
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, Shared& S, uint32_t* total) {
   const uint32_t lane = lane_id(), warp = threadIdx.x >> 5;
@@ -1162,6 +1172,7 @@ __device__ void refine(const Src& src, Bins bins, uint32_t Kp, uint32_t* hist, u
                        int32_t* out, int32_t K, Shared& S, uint32_t& lflags) {
   for (int guard = 0; guard < 40; ++guard) {
     __syncthreads();
+    phase_count(S, 9);  // refinement rounds
     find_boundary(hist, Kp, S);
     if (!S.ok) {
       lflags |= F_INTERNAL;
