@@ -85,6 +85,40 @@ def max_over_ranks(value: float, ws: int, device) -> float:
     return float(t.item())
 
 
+def copy_only_rate(h, K, steps=3, chunk_bytes=1 << 30):
+    """Rows per second that the host-buffer call's copies alone allow: the
+    pinned host rows h [M, N] go to the device in chunks of about 1 GiB,
+    alternating between two streams as topk_ragged_host does, and K indices
+    per row come back; no selection runs.  Returns (rows/s, H2D GB/s)."""
+    M, N = h.shape
+    rows = max(1, min(M, chunk_bytes // max(1, N * 4)))
+    dev = torch.device("cuda", torch.cuda.current_device())
+    bufs = [torch.empty((rows, N), dtype=torch.float32, device=dev) for _ in range(2)]
+    outs = [torch.zeros((rows, K), dtype=torch.int32, device=dev) for _ in range(2)]
+    ho = torch.empty((M, K), dtype=torch.int32, pin_memory=True)
+    sts = [torch.cuda.Stream(device=dev) for _ in range(2)]
+
+    def one():
+        for c, r0 in enumerate(range(0, M, rows)):
+            n = min(rows, M - r0)
+            with torch.cuda.stream(sts[c & 1]):
+                bufs[c & 1][:n].copy_(h[r0:r0 + n], non_blocking=True)
+                ho[r0:r0 + n].copy_(outs[c & 1][:n], non_blocking=True)
+        for s in sts:
+            s.synchronize()
+
+    one()
+    ts = []
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        one()
+        ts.append(time.perf_counter() - t0)
+    t = sum(ts) / len(ts)
+    del bufs, outs
+    torch.cuda.empty_cache()
+    return M / t, M * N * 4 / t / 1e9
+
+
 def job_rows_per_s(ws: int, M: int, steps: int, total_ms: float) -> float:
     """Whole-job throughput: every rank selects its own M-row batch per step
     (weak scaling, no data-path collective), timed by the slowest rank."""
@@ -840,10 +874,15 @@ def run_gb300(args):
                 ets.topk_ragged_host(hn, hl, K, out=ho)
                 ts.append(time.perf_counter() - t0)
             e2e_rate = M * len(ts) / sum(ts)
+            copy_rate, h2d_gbs = copy_only_rate(h, K, steps=args.e2e_steps)
             result["e2e"] = {"value": e2e_rate, "unit": UNIT,
                              "h2d_bytes_per_step": M * N * 4 + M * 4,
                              "d2h_bytes_per_step": M * K * 4,
-                             "steps": len(ts), "api": "topk_ragged_host (pinned host buffers)"}
+                             "steps": len(ts), "api": "topk_ragged_host (pinned host buffers)",
+                             "copy_only": {"value": copy_rate, "unit": UNIT, "h2d_gbs": h2d_gbs,
+                                           "what": "the same host->device and device->host "
+                                                   "bytes in the same 1 GiB chunks on two "
+                                                   "streams, no selection"}}
             del h
         except RuntimeError as e:
             result["e2e"] = {"value": None, "unit": UNIT, "error": str(e)[:200]}
