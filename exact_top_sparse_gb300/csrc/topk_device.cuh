@@ -674,8 +674,8 @@ struct ScanCollect {
   uint2* spill; // entries CAP.. in global memory (nullptr: none)
   uint32_t cap; // CAP_ALL with a spill area, else CAP
   uint32_t* ncand;    // scores above tau1 (counts past the capacity)
-  uint32_t* ties;     // indices of scores equal to tau1, tie_cap of them
-  uint32_t tie_cap;
+  uint32_t* ties;     // indices of scores equal to tau1, at most tie_cap of them
+  uint32_t tie_cap;   // the row's K (at most the list's capacity)
   uint32_t* neq;      // scores equal to tau1 (counts past tie_cap)
   uint32_t xeq;       // ties this thread counted in a register once it saw the tie list full
   bool full;          // this thread saw the tie list full
@@ -696,6 +696,18 @@ struct ScanCollect {
     return (tie(v.x) ? 1u : 0u) | (tie(v.y) ? 2u : 0u) | (tie(v.z) ? 4u : 0u) |
            (tie(v.w) ? 8u : 0u);
   }
+  // Candidates appended so far (a lower bound of the final count while the
+  // pass runs).
+  __device__ __forceinline__ uint32_t cands_so_far() const {
+    return *reinterpret_cast<const volatile uint32_t*>(ncand);
+  }
+  // A thread stops listing ties (and only counts them) once the list holds
+  // tie_cap - (candidates so far) of them.  The answer takes ties only when
+  // the K-th largest score is tau1, and then K - C(>tau1) of them; C(>tau1)
+  // only grows, so the list already covers it, while a row whose admitted
+  // scores number fewer than K (recovery: every tie is needed) never reaches
+  // the limit.  With tie_cap = K most ties are counted in registers instead of
+  // taking an atomic and a global store.
   // Counts the ties of mask q (element e of group a for bits 0-3, of group b
   // for bits 4-7) and keeps their indices while the tie list has room.
   __device__ __forceinline__ void put_ties(uint32_t q, int64_t ia, int64_t ib) {
@@ -705,7 +717,7 @@ struct ScanCollect {
       return;
     }
     uint32_t t = atomicAdd(neq, c);
-    if (t + c >= tie_cap) full = true;
+    if (t + c + cands_so_far() >= tie_cap) full = true;
     while (q && t < tie_cap) {
       const uint32_t e = (uint32_t)__ffs(q) - 1u;
       q &= q - 1u;
@@ -762,7 +774,7 @@ struct ScanCollect {
                      (byte_flags(e3) << 12);
         const uint32_t c = (uint32_t)__popc(q);
         uint32_t t = atomicAdd(neq, c);
-        if (t + c >= tie_cap) full = true;
+        if (t + c + cands_so_far() >= tie_cap) full = true;
         while (q && t < tie_cap) {
           const uint32_t e = (uint32_t)__ffs(q) - 1u;
           q &= q - 1u;

@@ -493,7 +493,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       S.neq = 0;
     }
     __syncthreads();
-    uint32_t C0 = scan_collect(row, 0, len, R, c, spill, TieList{ties, (uint32_t)TIE_CAP, &S.neq},
+    uint32_t C0 = scan_collect(row, 0, len, R, c, spill, TieList{ties, (uint32_t)min(K0, (int32_t)TIE_CAP), &S.neq},
                                key0, key1, sb, lflags, primed);
     // claim the next row now and warm L2 with its sample points while this
     // one is refined
