@@ -801,31 +801,40 @@ struct ScanCollect {
   __device__ static __forceinline__ uint32_t byte_flags(uint32_t c) {
     return ((c >> 7) & 1u) | ((c >> 14) & 2u) | ((c >> 21) & 4u) | ((c >> 28) & 8u);
   }
-  // bfloat16 unit of 8 raw patterns from index i0 on, tau1 > +0 with pattern
-  // t (k16 = (0x8000 - t) in both halves): patterns compare as signed 16-bit
-  // integers in the order of the values, so the admission is a SWAR lane
-  // test and only the admitted scores are turned into keys (a positive
-  // bfloat16 widens to bits << 16, whose order key is those bits with the
-  // sign bit set).
-  __device__ __forceinline__ void put_bf16_unit(int64_t i0, const uint4& u, uint32_t k16) {
-    uint32_t m = half_flags(swar_ge16(u.x, k16)) | (half_flags(swar_ge16(u.y, k16)) << 2) |
-                 (half_flags(swar_ge16(u.z, k16)) << 4) | (half_flags(swar_ge16(u.w, k16)) << 6);
-    if (!m) return;
+  // Two bfloat16 units, u0 from index i0 on and u1 from i1 on, tau1 > +0,
+  // with the SWAR test words w[0..7] of their 32-bit words (the top bit of a
+  // 16-bit half set where that pattern is admitted; see swar_ge16): patterns
+  // compare as signed 16-bit integers in the order of the values, so only
+  // the admitted ones become keys (a positive bfloat16 widens to bits << 16,
+  // whose order key is those bits with the sign bit set), and both units take
+  // one shared-memory atomic.
+  __device__ __forceinline__ void put_bf16_words(uint32_t i0, const uint4& u0, uint32_t i1,
+                                                 const uint4& u1, const uint32_t (&w)[8]) {
+    // bit e of m: element e (0-7 of u0, 8-15 of u1); the flags sit in bytes 1
+    // and 3 of each word, which byte_perm gathers four at a time
+    uint32_t m = flags4(__byte_perm(w[0], w[1], 0x7531u)) |
+                 (flags4(__byte_perm(w[2], w[3], 0x7531u)) << 4) |
+                 (flags4(__byte_perm(w[4], w[5], 0x7531u)) << 8) |
+                 (flags4(__byte_perm(w[6], w[7], 0x7531u)) << 12);
     uint32_t pos = atomicAdd(ncand, (uint32_t)__popc(m));
     do {
       const uint32_t e = (uint32_t)__ffs(m) - 1u;
       m &= m - 1u;
-      const uint32_t wd = e < 4u ? (e < 2u ? u.x : u.y) : (e < 6u ? u.z : u.w);
-      const uint32_t b = (wd >> (16u * (e & 1u))) & 0xFFFFu;
-      const uint2 ent = make_uint2((uint32_t)(i0 + e), (b << 16) | 0x80000000u);
+      const uint4 u = e < 8u ? u0 : u1;
+      const uint32_t k = e & 7u;
+      const uint32_t wd = k < 4u ? (k < 2u ? u.x : u.y) : (k < 6u ? u.z : u.w);
+      const uint32_t b = (wd >> (16u * (k & 1u))) & 0xFFFFu;
+      const uint2 ent = make_uint2((e < 8u ? i0 : i1) + k, (b << 16) | 0x80000000u);
       if (pos < (uint32_t)CAP) cand[pos] = ent;
       else if (pos < cap) spill[pos - (uint32_t)CAP] = ent;
       ++pos;
     } while (m);
   }
-  // 2-bit mask of the halves that are 0xFFFF in a per-halfword compare result
-  __device__ static __forceinline__ uint32_t half_flags(uint32_t c) {
-    return ((c >> 15) & 1u) | ((c >> 30) & 2u);
+  // 4-bit mask of the bytes of p whose top bit is set (the only bits p may
+  // hold): one multiply moves bit 7 of byte j to bit 24 + j, and no two
+  // partial products share a bit below 32, so nothing carries
+  __device__ static __forceinline__ uint32_t flags4(uint32_t p) {
+    return (((p >> 7) & 0x01010101u) * 0x01020408u) >> 24;
   }
   // Appends the admitted scores among the elements of v selected by vm
   // (element i0 + e is lane e).
@@ -922,81 +931,101 @@ __device__ __forceinline__ void scan_pass(Ring& R, const E* __restrict__ row, in
     // SWAR constant of the narrow positive thresholds: (top - t) in every lane
     const uint32_t kk = NG == 2 ? (0x8000u - (uint32_t)thr) * 0x00010001u
                                 : (0x80u - (uint32_t)thr) * 0x01010101u;
+    // stage and phase of the pass's first chunk, advanced per chunk; only the
+    // last chunk can be short, so the others load without bounds tests.
+    // Indices fit in 32 bits (N_alloc <= INT32_MAX).
+    uint32_t s = R.seq % STAGES, ph = (R.seq / STAGES) & 1u;
+    const uint32_t nfull = (uint32_t)((a1 - a0) / CE);
+    const uint4* const sm0 = reinterpret_cast<const uint4*>(R.buf) + ct;
+    uint32_t off = (uint32_t)a0;
     for (uint32_t c = 0; c < nchunks; ++c) {
-      const uint32_t q = R.seq + c, s = q % STAGES, use = q / STAGES;
-      if (!mbar_wait(&R.full[s], use & 1u, R.abort)) lflags |= F_TIMEOUT;
-      const int64_t off = a0 + (int64_t)c * CE;
-      const int64_t n = (a1 - off) < CE ? (a1 - off) : CE;
-      const int nu = (int)(n / P16);
-      const uint4* sm = reinterpret_cast<const uint4*>(R.buf + (size_t)s * CHUNK_FLOATS);
-      const int j0 = (int)ct, j1 = (int)ct + CONSUMERS;
-      const bool ok0 = j0 < nu, ok1 = j1 < nu;
-      const uint4 u0 = ok0 ? sm[j0] : make_uint4(0u, 0u, 0u, 0u);
-      const uint4 u1 = ok1 ? sm[j1] : make_uint4(0u, 0u, 0u, 0u);
-      int32_t m0, m1;
-      if constexpr (NG == 2 && POS) {
-        // bfloat16 with tau1 > +0: the raw 16-bit patterns compare as signed
-        // integers in the order of the values; two per SWAR lane test
-        const uint32_t a0 = swar_ge16(u0.x, kk) | swar_ge16(u0.y, kk) | swar_ge16(u0.z, kk) |
-                            swar_ge16(u0.w, kk);
-        const uint32_t a1 = swar_ge16(u1.x, kk) | swar_ge16(u1.y, kk) | swar_ge16(u1.z, kk) |
-                            swar_ge16(u1.w, kk);
-        m0 = a0 ? thr : INT32_MIN;
-        m1 = a1 ? thr : INT32_MIN;
-      } else if constexpr (NG == 4 && POS) {
-        // E4M3 with tau1 > +0: the raw bytes, four per SWAR lane test
-        const uint32_t a0 = swar_ge8(u0.x, kk) | swar_ge8(u0.y, kk) | swar_ge8(u0.z, kk) |
-                            swar_ge8(u0.w, kk);
-        const uint32_t a1 = swar_ge8(u1.x, kk) | swar_ge8(u1.y, kk) | swar_ge8(u1.z, kk) |
-                            swar_ge8(u1.w, kk);
-        m0 = a0 ? thr : INT32_MIN;
-        m1 = a1 ? thr : INT32_MIN;
+      if (!mbar_wait(&R.full[s], ph, R.abort)) lflags |= F_TIMEOUT;
+      const uint4* sm = sm0 + s * (uint32_t)(CHUNK_BYTES / 16);
+      uint4 u0, u1;
+      bool ok0 = true, ok1 = true;
+      if (c < nfull) {
+        u0 = sm[0];
+        u1 = sm[CONSUMERS];
       } else {
-        m0 = max_operand<POS>(Elem<E>::group(u0, 0));
-        m1 = max_operand<POS>(Elem<E>::group(u1, 0));
-#pragma unroll
-        for (int k = 1; k < NG; ++k) {
-          m0 = max(m0, max_operand<POS>(Elem<E>::group(u0, k)));
-          m1 = max(m1, max_operand<POS>(Elem<E>::group(u1, k)));
-        }
+        const int nu = (int)(((uint32_t)a1 - off) / (uint32_t)P16);
+        ok0 = (int)ct < nu;
+        ok1 = (int)ct + CONSUMERS < nu;
+        u0 = ok0 ? sm[0] : make_uint4(0u, 0u, 0u, 0u);
+        u1 = ok1 ? sm[CONSUMERS] : make_uint4(0u, 0u, 0u, 0u);
       }
-      if (!ok0) m0 = INT32_MIN;
-      if (!ok1) m1 = INT32_MIN;
-      // both loads have fed m0/m1: hand the stage back before any appends
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&R.empty[s]);
-      const bool h0 = ok0 && m0 >= thr, h1 = ok1 && m1 >= thr;
-      if (h0 || h1) {
-        if constexpr (NG == 1) {
-          f.lane_put2(off + (int64_t)P16 * j0, Elem<E>::group(u0, 0), h0, off + (int64_t)P16 * j1,
-                      Elem<E>::group(u1, 0), h1);
-        } else if constexpr (NG == 2 && POS && !TIES) {
-          // bfloat16 above +0: packed 16-bit compares against tau1's pattern
-          if (h0) f.put_bf16_unit(off + (int64_t)P16 * j0, u0, kk);
-          if (h1) f.put_bf16_unit(off + (int64_t)P16 * j1, u1, kk);
-        } else if constexpr (NG == 2) {
-          if (h0) f.lane_put2(off + (int64_t)P16 * j0, Elem<E>::group(u0, 0), true,
-                              off + (int64_t)P16 * j0 + 4, Elem<E>::group(u0, 1), true);
-          if (h1) f.lane_put2(off + (int64_t)P16 * j1, Elem<E>::group(u1, 0), true,
-                              off + (int64_t)P16 * j1 + 4, Elem<E>::group(u1, 1), true);
-        } else if constexpr (TIES && POS) {
-          // E4M3 above +0: packed byte compares against tau1's byte
-          const uint32_t t4 = (uint32_t)thr * 0x01010101u;
-          if (h0) f.put_e4m3_unit(off + (int64_t)P16 * j0, u0, t4);
-          if (h1) f.put_e4m3_unit(off + (int64_t)P16 * j1, u1, t4);
+      const uint32_t i0 = off + (uint32_t)P16 * ct, i1 = i0 + (uint32_t)(P16 * CONSUMERS);
+      if constexpr (NG == 1) {
+        // FP32: the admission mask of all eight scores, kept for the append
+        uint32_t m = f.admit_mask(Elem<E>::group(u0, 0)) | (f.admit_mask(Elem<E>::group(u1, 0)) << 4);
+        if (!ok0) m &= 0xF0u;
+        if (!ok1) m &= 0x0Fu;
+        // the loads have fed the mask: hand the stage back before any appends
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&R.empty[s]);
+        if (m) f.put_masked(m, 0u, i0, Elem<E>::group(u0, 0), i1, Elem<E>::group(u1, 0));
+      } else if constexpr (NG == 2 && POS && !TIES) {
+        // bfloat16 with tau1 > +0: the raw 16-bit patterns compare as signed
+        // integers in the order of the values; two per SWAR lane test, and
+        // the test words are kept for the append
+        uint32_t w[8] = {swar_ge16(u0.x, kk), swar_ge16(u0.y, kk), swar_ge16(u0.z, kk),
+                         swar_ge16(u0.w, kk), swar_ge16(u1.x, kk), swar_ge16(u1.y, kk),
+                         swar_ge16(u1.z, kk), swar_ge16(u1.w, kk)};
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&R.empty[s]);
+        // a short chunk's missing units were loaded as zero, which no
+        // positive threshold admits
+        if ((w[0] | w[1] | w[2] | w[3] | w[4] | w[5] | w[6] | w[7]) != 0u)
+          f.put_bf16_words(i0, u0, i1, u1, w);
+      } else {
+        int32_t m0, m1;
+        if constexpr (NG == 4 && POS) {
+          // E4M3 with tau1 > +0: the raw bytes, four per SWAR lane test
+          const uint32_t a0 = swar_ge8(u0.x, kk) | swar_ge8(u0.y, kk) | swar_ge8(u0.z, kk) |
+                              swar_ge8(u0.w, kk);
+          const uint32_t a1 = swar_ge8(u1.x, kk) | swar_ge8(u1.y, kk) | swar_ge8(u1.z, kk) |
+                              swar_ge8(u1.w, kk);
+          m0 = a0 ? thr : INT32_MIN;
+          m1 = a1 ? thr : INT32_MIN;
         } else {
-          // one unit and a pair of groups (eight scores) at a time: a single
-          // inlined append keeps few values live
+          m0 = max_operand<POS>(Elem<E>::group(u0, 0));
+          m1 = max_operand<POS>(Elem<E>::group(u1, 0));
+#pragma unroll
+          for (int k = 1; k < NG; ++k) {
+            m0 = max(m0, max_operand<POS>(Elem<E>::group(u0, k)));
+            m1 = max(m1, max_operand<POS>(Elem<E>::group(u1, k)));
+          }
+        }
+        if (!ok0) m0 = INT32_MIN;
+        if (!ok1) m1 = INT32_MIN;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&R.empty[s]);
+        const bool h0 = m0 >= thr, h1 = m1 >= thr;
+        if (h0 || h1) {
+          if constexpr (NG == 2) {
+            if (h0) f.lane_put2(i0, Elem<E>::group(u0, 0), true, i0 + 4, Elem<E>::group(u0, 1), true);
+            if (h1) f.lane_put2(i1, Elem<E>::group(u1, 0), true, i1 + 4, Elem<E>::group(u1, 1), true);
+          } else if constexpr (TIES && POS) {
+            // E4M3 above +0: packed byte compares against tau1's byte
+            const uint32_t t4 = (uint32_t)thr * 0x01010101u;
+            if (h0) f.put_e4m3_unit(i0, u0, t4);
+            if (h1) f.put_e4m3_unit(i1, u1, t4);
+          } else {
+            // one unit and a pair of groups (eight scores) at a time: a single
+            // inlined append keeps few values live
 #pragma unroll 1
-          for (int t = 0; t < NG; ++t) {
-            const int v = t / (NG / 2), k = 2 * (t % (NG / 2));
-            if (!(v ? h1 : h0)) continue;
-            const uint4& u = v ? u1 : u0;
-            const int64_t i0 = off + (int64_t)P16 * (v ? j1 : j0) + 4 * k;
-            f.lane_put2(i0, Elem<E>::group(u, k), true, i0 + 4, Elem<E>::group(u, k + 1), true);
+            for (int t = 0; t < NG; ++t) {
+              const int v = t / (NG / 2), k = 2 * (t % (NG / 2));
+              if (!(v ? h1 : h0)) continue;
+              const uint4& u = v ? u1 : u0;
+              const uint32_t ib = (v ? i1 : i0) + 4u * (uint32_t)k;
+              f.lane_put2(ib, Elem<E>::group(u, k), true, ib + 4, Elem<E>::group(u, k + 1), true);
+            }
           }
         }
       }
+      s = (s + 1u == (uint32_t)STAGES) ? 0u : s + 1u;
+      ph ^= (s == 0u) ? 1u : 0u;
+      off += (uint32_t)CE;
     }
   }
   R.seq += nchunks;
