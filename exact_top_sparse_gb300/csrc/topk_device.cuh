@@ -642,7 +642,7 @@ __device__ __forceinline__ uint2 cand_at(const uint2* cand, const uint2* spill, 
 // contract lets boundary ties go either way), so the first K ties suffice.
 // E4M3 rows (8 values per octave) put long runs of ties at tau1, which would
 // otherwise overflow the candidate buffers (with tau1 > +0 their units are
-// tested byte-wise, put_e4m3_unit); for FP32 and bfloat16 rows
+// tested byte-wise, put_e4m3_words); for FP32 and bfloat16 rows
 // (TIES = false) ties are ordinary candidates, which keeps their scan loop
 // leaner (measured 13 % and 5 % faster), and a rare long tie run takes the
 // overflow path.
@@ -658,10 +658,6 @@ __device__ __forceinline__ uint32_t swar_ge8(uint32_t w, uint32_t k8) {
 }
 __device__ __forceinline__ uint32_t swar_gt8(uint32_t w, uint32_t g8) {
   return ((w & 0x7F7F7F7Fu) + g8) & ~w & 0x80808080u;
-}
-__device__ __forceinline__ uint32_t swar_eq8(uint32_t w, uint32_t t4) {
-  const uint32_t x = w ^ t4;  // a lane equal to t is zero here
-  return ~(((x & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | x) & 0x80808080u;
 }
 __device__ __forceinline__ uint32_t swar_ge16(uint32_t w, uint32_t k16) {
   return ((w & 0x7FFF7FFFu) + k16) & ~w & 0x80008000u;
@@ -754,52 +750,64 @@ struct ScanCollect {
       ++pos;
     } while (m);
   }
-  // E4M3 unit of 16 raw bytes from index i0 on, tau1 > +0 with byte
-  // pattern t (repeated in the four bytes of t4): bytes compare as signed
-  // integers in the order of the values, so the tie and the candidate tests
-  // are SWAR lane tests, a unit's ties are counted from the test words once
-  // the tie list is full, and only the candidates are widened.
-  __device__ __forceinline__ void put_e4m3_unit(int64_t i0, const uint4& u, uint32_t t4) {
+  // Two E4M3 units, u0 from index i0 on and u1 from i1 on, tau1 > +0 with
+  // byte pattern t (repeated in the four bytes of t4), and the SWAR test
+  // words ge[0..7] of their 32-bit words (bit 7 of a byte set where that
+  // score is >= tau1; see swar_ge8).  The strict test of the same words
+  // splits them: a byte >= tau1 but not > tau1 is a tie.  Ties are counted
+  // with one popc per word (and listed while the list has room), scores above
+  // tau1 are appended with one atomic for both units, and only those are
+  // widened.
+  __device__ __forceinline__ void put_e4m3_words(uint32_t i0, const uint4& u0, uint32_t i1,
+                                                 const uint4& u1, const uint32_t (&ge)[8],
+                                                 uint32_t t4) {
     const uint32_t g8 = 0x7F7F7F7Fu - t4;  // (0x7F - t) in every byte
-    const uint32_t e0 = swar_eq8(u.x, t4), e1 = swar_eq8(u.y, t4), e2 = swar_eq8(u.z, t4),
-                   e3 = swar_eq8(u.w, t4);
-    const uint32_t g0 = swar_gt8(u.x, g8), g1 = swar_gt8(u.y, g8), g2 = swar_gt8(u.z, g8),
-                   g3 = swar_gt8(u.w, g8);
-    if (e0 | e1 | e2 | e3) {
+    const uint32_t uw[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+    uint32_t gt[8], eq[8];
+    uint32_t anygt = 0, c = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      gt[k] = swar_gt8(uw[k], g8);
+      eq[k] = ge[k] & ~gt[k];
+      anygt |= gt[k];
+      c += (uint32_t)__popc(eq[k]);
+    }
+    if (c) {
       if (full) {
-        // one bit per tie in the test words
-        xeq += (uint32_t)(__popc(e0) + __popc(e1) + __popc(e2) + __popc(e3));
+        xeq += c;  // the list holds enough: only count
       } else {
-        uint32_t q = byte_flags(e0) | (byte_flags(e1) << 4) | (byte_flags(e2) << 8) |
-                     (byte_flags(e3) << 12);
-        const uint32_t c = (uint32_t)__popc(q);
         uint32_t t = atomicAdd(neq, c);
         if (t + c + cands_so_far() >= tie_cap) full = true;
-        while (q && t < tie_cap) {
-          const uint32_t e = (uint32_t)__ffs(q) - 1u;
-          q &= q - 1u;
-          ties[t++] = (uint32_t)(i0 + e);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          uint32_t q = eq[k];
+          while (q && t < tie_cap) {
+            const uint32_t b = (uint32_t)__ffs(q) - 1u;  // bit 7 of byte b >> 3
+            q &= q - 1u;
+            ties[t++] = (k < 4 ? i0 : i1) + 4u * (uint32_t)(k & 3) + (b >> 3);
+          }
         }
       }
     }
-    if (!(g0 | g1 | g2 | g3)) return;
-    uint32_t m = byte_flags(g0) | (byte_flags(g1) << 4) | (byte_flags(g2) << 8) |
-                 (byte_flags(g3) << 12);
-    uint32_t pos = atomicAdd(ncand, (uint32_t)__popc(m));
-    do {
-      const uint32_t e = (uint32_t)__ffs(m) - 1u;
-      m &= m - 1u;
-      const uint32_t wd = e < 8u ? (e < 4u ? u.x : u.y) : (e < 12u ? u.z : u.w);
-      const uint32_t b = (wd >> (8u * (e & 3u))) & 0xFFu;
-      const uint2 ent = make_uint2((uint32_t)(i0 + e), fkey(Elem<uint8_t>::widen(b)));
-      if (pos < (uint32_t)CAP) cand[pos] = ent;
-      else if (pos < cap) spill[pos - (uint32_t)CAP] = ent;
-      ++pos;
-    } while (m);
-  }
-  // 4-bit mask of the bytes that are 0xFF in a per-byte compare result
-  __device__ static __forceinline__ uint32_t byte_flags(uint32_t c) {
-    return ((c >> 7) & 1u) | ((c >> 14) & 2u) | ((c >> 21) & 4u) | ((c >> 28) & 8u);
+    if (!anygt) return;
+    uint32_t n = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) n += (uint32_t)__popc(gt[k]);
+    uint32_t pos = atomicAdd(ncand, n);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      uint32_t q = gt[k];
+      while (q) {
+        const uint32_t b = (uint32_t)__ffs(q) - 1u;
+        q &= q - 1u;
+        const uint32_t byte = (uw[k] >> (b - 7u)) & 0xFFu;
+        const uint2 ent = make_uint2((k < 4 ? i0 : i1) + 4u * (uint32_t)(k & 3) + (b >> 3),
+                                     fkey(Elem<uint8_t>::widen(byte)));
+        if (pos < (uint32_t)CAP) cand[pos] = ent;
+        else if (pos < cap) spill[pos - (uint32_t)CAP] = ent;
+        ++pos;
+      }
+    }
   }
   // Two bfloat16 units, u0 from index i0 on and u1 from i1 on, tau1 > +0,
   // with the SWAR test words w[0..7] of their 32-bit words (the top bit of a
@@ -976,24 +984,25 @@ __device__ __forceinline__ void scan_pass(Ring& R, const E* __restrict__ row, in
         // positive threshold admits
         if ((w[0] | w[1] | w[2] | w[3] | w[4] | w[5] | w[6] | w[7]) != 0u)
           f.put_bf16_words(i0, u0, i1, u1, w);
+      } else if constexpr (NG == 4 && POS) {
+        // E4M3 with tau1 > +0: the raw bytes compare as signed integers in the
+        // order of the values, four per SWAR lane test; the test words are
+        // kept for the tie and candidate split
+        uint32_t w[8] = {swar_ge8(u0.x, kk), swar_ge8(u0.y, kk), swar_ge8(u0.z, kk),
+                         swar_ge8(u0.w, kk), swar_ge8(u1.x, kk), swar_ge8(u1.y, kk),
+                         swar_ge8(u1.z, kk), swar_ge8(u1.w, kk)};
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&R.empty[s]);
+        // missing units of a short chunk were loaded as zero: never admitted
+        if ((w[0] | w[1] | w[2] | w[3] | w[4] | w[5] | w[6] | w[7]) != 0u)
+          f.put_e4m3_words(i0, u0, i1, u1, w, (uint32_t)thr * 0x01010101u);
       } else {
-        int32_t m0, m1;
-        if constexpr (NG == 4 && POS) {
-          // E4M3 with tau1 > +0: the raw bytes, four per SWAR lane test
-          const uint32_t a0 = swar_ge8(u0.x, kk) | swar_ge8(u0.y, kk) | swar_ge8(u0.z, kk) |
-                              swar_ge8(u0.w, kk);
-          const uint32_t a1 = swar_ge8(u1.x, kk) | swar_ge8(u1.y, kk) | swar_ge8(u1.z, kk) |
-                              swar_ge8(u1.w, kk);
-          m0 = a0 ? thr : INT32_MIN;
-          m1 = a1 ? thr : INT32_MIN;
-        } else {
-          m0 = max_operand<POS>(Elem<E>::group(u0, 0));
-          m1 = max_operand<POS>(Elem<E>::group(u1, 0));
+        int32_t m0 = max_operand<POS>(Elem<E>::group(u0, 0));
+        int32_t m1 = max_operand<POS>(Elem<E>::group(u1, 0));
 #pragma unroll
-          for (int k = 1; k < NG; ++k) {
-            m0 = max(m0, max_operand<POS>(Elem<E>::group(u0, k)));
-            m1 = max(m1, max_operand<POS>(Elem<E>::group(u1, k)));
-          }
+        for (int k = 1; k < NG; ++k) {
+          m0 = max(m0, max_operand<POS>(Elem<E>::group(u0, k)));
+          m1 = max(m1, max_operand<POS>(Elem<E>::group(u1, k)));
         }
         if (!ok0) m0 = INT32_MIN;
         if (!ok1) m1 = INT32_MIN;
@@ -1004,11 +1013,6 @@ __device__ __forceinline__ void scan_pass(Ring& R, const E* __restrict__ row, in
           if constexpr (NG == 2) {
             if (h0) f.lane_put2(i0, Elem<E>::group(u0, 0), true, i0 + 4, Elem<E>::group(u0, 1), true);
             if (h1) f.lane_put2(i1, Elem<E>::group(u1, 0), true, i1 + 4, Elem<E>::group(u1, 1), true);
-          } else if constexpr (TIES && POS) {
-            // E4M3 above +0: packed byte compares against tau1's byte
-            const uint32_t t4 = (uint32_t)thr * 0x01010101u;
-            if (h0) f.put_e4m3_unit(i0, u0, t4);
-            if (h1) f.put_e4m3_unit(i1, u1, t4);
           } else {
             // one unit and a pair of groups (eight scores) at a time: a single
             // inlined append keeps few values live
