@@ -45,6 +45,22 @@ bool g_params_init = false;
 // nothing on any width.
 uint32_t g_knob_pf_ahead = 4;
 uint32_t g_knob_pf_next_bytes = 0;
+// The persistent kernel's sampler warp (see tk::Params::sampler_warp): -1
+// chooses by row width and element size, 0 and 1 force it (tuning builds).
+int g_knob_sampler = -1;
+
+// Whether a persistent launch over rows of N_alloc elements of elem_bytes
+// each gives its last warp to sampling the next row.  The certify pass is
+// bound by its consumer warps' instructions, so one warp fewer streams about
+// 1/15 slower, while the next row's stage 1 (about 6 us per row on the whole
+// CTA) leaves the critical path.  Measured (8192 causal rows, ms per call,
+// without / with): FP32 128K 1.029 / 0.936, 256K 1.566 / 1.496, 512K 2.737 /
+// 2.750, 1M 5.073 / 5.125; bfloat16 1M 3.197 / 3.047; E4M3 1M 2.600 / 2.524.
+// FP32 rows of 512K elements and more stream without it.
+bool use_sampler_warp(int64_t N, int elem_bytes) {
+  if (g_knob_sampler >= 0) return g_knob_sampler != 0;
+  return elem_bytes < 4 || N < ((int64_t)1 << 19);
+}
 
 struct DevInfo {
   bool ready = false;
@@ -222,6 +238,7 @@ tk::Params kernel_params(int64_t M, int64_t N, int32_t K, const topk_params& p, 
   P.long_rho1 = p.long_rho1;
   P.pf_ahead = g_knob_pf_ahead;
   P.pf_next_bytes = g_knob_pf_next_bytes;
+  P.sampler_warp = use_sampler_warp(N, elem_bytes) ? 1u : 0u;
   return P;
 }
 
@@ -713,6 +730,12 @@ int topk_version(void) { return kVersion; }
 int topk_debug_set_prefetch(uint32_t ahead_chunks, uint32_t next_bytes) {
   g_knob_pf_ahead = ahead_chunks;
   g_knob_pf_next_bytes = next_bytes & ~15u;
+  return TOPK_OK;
+}
+// Forces the persistent kernel's sampler warp on (1) or off (0), or leaves
+// the choice to the width rule (-1).
+int topk_debug_set_sampler(int mode) {
+  g_knob_sampler = mode < 0 ? -1 : (mode ? 1 : 0);
   return TOPK_OK;
 }
 #endif

@@ -42,15 +42,16 @@ namespace tk {
 // ----------------------------------------------------------------- constants
 constexpr int THREADS = 512;                // threads per CTA for every kernel
 constexpr int NWARPS = THREADS / 32;
-constexpr int CONSUMER_WARPS = NWARPS - 1;  // warp 0 issues the bulk copies
-constexpr int CONSUMERS = CONSUMER_WARPS * 32;
+constexpr int CONSUMER_WARPS = NWARPS - 1;  // warp 0 issues the bulk copies; at most
+                                            // the others consume (see Ring::cw)
 constexpr int NB_BITS = 11;
 constexpr int NB = 1 << NB_BITS;            // bins per radix round
 static_assert(NB == 4 * THREADS, "boundary search maps 4 bins to each thread");
 constexpr int STAGES = 3;                   // ring stages
-constexpr int CHUNK_BYTES = 8 * CONSUMERS * 4;  // bytes per bulk copy / ring stage (15 KB):
-                                                // two float4 per consumer thread
-constexpr int CHUNK_FLOATS = CHUNK_BYTES / 4;
+constexpr int UNIT_CHUNK_BYTES = 32 * 32;    // chunk bytes per consumer warp: two 16-byte
+                                            // units per consumer thread
+constexpr int STAGE_BYTES = UNIT_CHUNK_BYTES * CONSUMER_WARPS;  // ring stage (15 KB)
+constexpr int STAGE_FLOATS = STAGE_BYTES / 4;
 constexpr int CAP = 6144;                   // on-chip candidate capacity (entries of 8 B)
 constexpr int SPILL = 10240;                // further candidates kept in global memory
 constexpr int CAP_ALL = CAP + SPILL;        // candidates one full-row pass can keep
@@ -233,6 +234,8 @@ struct __align__(16) Shared {
   uint32_t key0, key1;
   uint32_t last;
   uint32_t next, next_ok;        // a row claimed ahead of time (persistent kernel)
+  uint32_t nx_row, nx_ok;        // the claimed row, and whether nx_key holds its stage 1
+  uint32_t nx_key[4];            // key(tau0), key(tau1), smallest and largest sample key
   uint32_t neq;                  // scores equal to tau1 (counts past the tie list)
 #ifdef TOPK_PHASE_TIMING
   unsigned long long ph[12];     // cycles per phase of the persistent kernel (thread 0's clock)
@@ -452,7 +455,9 @@ __device__ __forceinline__ void warp_emit(int32_t* out, int32_t K, uint32_t idx,
 
 // ------------------------------------------------------------- the TMA ring
 // A 3-stage ring of 15 KB shared-memory stages filled by 1-D bulk copies.
-// Warp 0, lane 0 produces; warps 1..15 consume.  Every thread keeps the same
+// Warp 0, lane 0 produces; warps 1..cw consume, and a chunk is 1 KB per
+// consumer warp.  With cw = 14 the last warp, instead of consuming, samples
+// the next row during a certify pass (and sits the other passes out).  Every thread keeps the same
 // chunk sequence number, so passes can follow one another without resetting
 // the barriers.
 struct Ring {
@@ -463,9 +468,12 @@ struct Ring {
   uint64_t policy;
   uint32_t* abort;  // fail-fast flag of the launch's work (see mbar_wait_slow)
   uint32_t pf_ahead;  // chunks ahead of the ring a certify pass prefetches into L2
+  uint32_t cw;        // consumer warps (warps 1..cw)
+  uint32_t chunk;     // bytes per chunk: UNIT_CHUNK_BYTES * cw
 };
 
-__device__ __forceinline__ void ring_init(Ring& R, Shared& S, float* buf, uint32_t* abort) {
+__device__ __forceinline__ void ring_init(Ring& R, Shared& S, float* buf, uint32_t* abort,
+                                          uint32_t cw = (uint32_t)CONSUMER_WARPS) {
   R.buf = buf;
   R.full = S.full;
   R.empty = S.empty;
@@ -473,10 +481,12 @@ __device__ __forceinline__ void ring_init(Ring& R, Shared& S, float* buf, uint32
   R.policy = l2_policy_evict_first();
   R.abort = abort;
   R.pf_ahead = 0;
+  R.cw = cw;
+  R.chunk = (uint32_t)UNIT_CHUNK_BYTES * cw;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&S.full[s], 1);
-      mbar_init(&S.empty[s], CONSUMER_WARPS);
+      mbar_init(&S.empty[s], cw);
     }
     fence_mbar_init();
   }
@@ -487,8 +497,9 @@ __device__ __forceinline__ void ring_init(Ring& R, Shared& S, float* buf, uint32
 // start the bulk copy of chunk c of the 16-byte aligned body [a0, a1).
 template <class E>
 __device__ __forceinline__ void ring_issue(Ring& R, const E* __restrict__ row, int64_t a0,
-                                           int64_t a1, uint32_t c, uint32_t& lflags) {
-  constexpr int64_t CE = CHUNK_BYTES / Elem<E>::kSize;
+                                           int64_t a1, uint32_t c, uint32_t& lflags,
+                                           uint32_t chunk) {
+  const int64_t CE = chunk / Elem<E>::kSize;
   const uint32_t q = R.seq + c, s = q % STAGES, use = q / STAGES;
   if (!mbar_wait(&R.empty[s], (use & 1u) ^ 1u, R.abort)) lflags |= F_TIMEOUT;
   const int64_t off = a0 + (int64_t)c * CE;
@@ -496,32 +507,33 @@ __device__ __forceinline__ void ring_issue(Ring& R, const E* __restrict__ row, i
   const uint32_t bytes = (uint32_t)(n * Elem<E>::kSize);
   fence_proxy_async();
   mbar_arrive_expect_tx(&R.full[s], bytes);
-  bulk_load(R.buf + (size_t)s * CHUNK_FLOATS, row + off, bytes, &R.full[s], R.policy);
+  bulk_load(R.buf + (size_t)s * STAGE_FLOATS, row + off, bytes, &R.full[s], R.policy);
 }
 
 // The 16-byte aligned body [a0, a1) of [start, end) and its chunk count.
 template <class E>
 __device__ __forceinline__ uint32_t ring_span(const E* row, int64_t start, int64_t end,
-                                              int64_t* a0, int64_t* a1);
+                                              uint32_t chunk, int64_t* a0, int64_t* a1);
 
 // L2 prefetch of the first max_bytes of the 16-byte aligned body of row
 // [0, len) (one bulk prefetch; nothing past len is touched).
 template <class E>
 __device__ __forceinline__ void prefetch_row_head(const E* row, int64_t len, uint32_t max_bytes) {
   int64_t a0, a1;
-  ring_span(row, 0, len, &a0, &a1);
+  ring_span(row, 0, len, (uint32_t)STAGE_BYTES, &a0, &a1);
   int64_t n = a1 - a0;
   if (n > (int64_t)(max_bytes / Elem<E>::kSize)) n = (int64_t)(max_bytes / Elem<E>::kSize);
   const uint32_t bytes = (uint32_t)(n * Elem<E>::kSize) & ~15u;
   if (bytes) bulk_prefetch_l2(row + a0, bytes);
 }
 
-// The 16-byte aligned body [a0, a1) of [start, end) and its chunk count.
+// The 16-byte aligned body [a0, a1) of [start, end) and its count of chunks
+// of `chunk` bytes.
 template <class E>
 __device__ __forceinline__ uint32_t ring_span(const E* row, int64_t start, int64_t end,
-                                              int64_t* a0, int64_t* a1) {
+                                              uint32_t chunk, int64_t* a0, int64_t* a1) {
   constexpr int P16 = Elem<E>::kPer16;
-  constexpr int64_t CE = CHUNK_BYTES / Elem<E>::kSize;
+  const int64_t CE = chunk / Elem<E>::kSize;
   const uintptr_t addr = reinterpret_cast<uintptr_t>(row + start);
   int64_t b0 = start + (int64_t)(((16u - (uint32_t)(addr & 15u)) & 15u) / Elem<E>::kSize);
   if (b0 > end) b0 = end;
@@ -539,13 +551,13 @@ __device__ __forceinline__ uint32_t ring_prime(Ring& R, const E* __restrict__ ro
                                                int64_t start, int64_t end, uint32_t& lflags) {
   if (end <= start) return 0;
   int64_t a0, a1;
-  const uint32_t nchunks = ring_span(row, start, end, &a0, &a1);
+  const uint32_t nchunks = ring_span(row, start, end, R.chunk, &a0, &a1);
   const uint32_t n = nchunks < (uint32_t)STAGES ? nchunks : (uint32_t)STAGES;
   if (threadIdx.x == 0) {
-    for (uint32_t c = 0; c < n; ++c) ring_issue(R, row, a0, a1, c, lflags);
+    for (uint32_t c = 0; c < n; ++c) ring_issue(R, row, a0, a1, c, lflags, R.chunk);
     // and the next pf_ahead chunks into L2, which the pass would ask for
     // first (scan_pass then starts its own prefetches past them)
-    constexpr int64_t CE = CHUNK_BYTES / Elem<E>::kSize;
+    const int64_t CE = R.chunk / Elem<E>::kSize;
     if (R.pf_ahead > 0 && n < nchunks) {
       const int64_t p0 = a0 + (int64_t)n * CE;
       const int64_t p1 = min(a1, a0 + (int64_t)(n + R.pf_ahead) * CE);
@@ -581,11 +593,11 @@ __device__ __forceinline__ void ring_pass(Ring& R, const E* __restrict__ row, in
   const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31u;
   if (end <= start) return;
   int64_t a0, a1;
-  const uint32_t nchunks = ring_span(row, start, end, &a0, &a1);
+  const uint32_t nchunks = ring_span(row, start, end, R.chunk, &a0, &a1);
   if (warp == 0) {
     if (lane == 0)
-      for (uint32_t c = 0; c < nchunks; ++c) ring_issue(R, row, a0, a1, c, lflags);
-  } else {
+      for (uint32_t c = 0; c < nchunks; ++c) ring_issue(R, row, a0, a1, c, lflags, R.chunk);
+  } else if (warp <= R.cw) {
     if (warp == 1) {
       // head [start, a0) on lanes 0.., tail [a1, end) on lanes 16..
       const int64_t nh = a0 - start, nt = end - a1;
@@ -596,17 +608,18 @@ __device__ __forceinline__ void ring_pass(Ring& R, const E* __restrict__ row, in
       f.quad(i >= 0 ? i : 0, make_float4(v, 0.f, 0.f, 0.f), i >= 0 ? 1u : 0u);
     }
     const uint32_t ct = tid - 32;
-    constexpr int64_t CE = CHUNK_BYTES / Elem<E>::kSize;
+    const int C = 32 * (int)R.cw;  // consumer threads
+    const int64_t CE = R.chunk / Elem<E>::kSize;
     for (uint32_t c = 0; c < nchunks; ++c) {
       const uint32_t q = R.seq + c, s = q % STAGES, use = q / STAGES;
       if (!mbar_wait(&R.full[s], use & 1u, R.abort)) lflags |= F_TIMEOUT;
       const int64_t off = a0 + (int64_t)c * CE;
       const int64_t n = (a1 - off) < CE ? (a1 - off) : CE;
       const int nu = (int)(n / P16);
-      const uint4* sm = reinterpret_cast<const uint4*>(R.buf + (size_t)s * CHUNK_FLOATS);
-      const int iters = (nu + CONSUMERS - 1) / CONSUMERS;
+      const uint4* sm = reinterpret_cast<const uint4*>(R.buf + (size_t)s * STAGE_FLOATS);
+      const int iters = (nu + C - 1) / C;
       for (int it = 0; it < iters; ++it) {
-        const int j = (int)ct + it * CONSUMERS;
+        const int j = (int)ct + it * C;
         const bool ok = j < nu;
         const uint4 u = ok ? sm[j] : make_uint4(0u, 0u, 0u, 0u);
         // one group of four widened scores at a time (the functor's work is
@@ -887,17 +900,22 @@ __device__ __forceinline__ int32_t max_operand(const float4& v) {
 // bfloat16 or 32 E4M3) are tested with one integer max, the stage is handed back as
 // soon as the loads have fed that test, and only lanes holding an admitted
 // score (rare) append.
-template <class E, bool POS, bool TIES>
+// The sampler warp runs `job` meanwhile (the next row's claim and stage 1 in
+// the persistent kernel; nothing elsewhere).
+// CW: the ring's consumer warps (R.cw), fixed at compile time here so that
+// the chunk geometry folds into the loop.
+template <class E, bool POS, bool TIES, int CW, class J>
 __device__ __forceinline__ void scan_pass(Ring& R, const E* __restrict__ row, int64_t start,
                                           int64_t end, ScanCollect<POS, TIES>& f,
-                                          uint32_t& lflags, uint32_t primed) {
-  static_assert(CHUNK_BYTES == 32 * CONSUMERS, "a full chunk is two 16-byte units per consumer");
+                                          uint32_t& lflags, uint32_t primed, const J& job) {
   constexpr int P16 = Elem<E>::kPer16, NG = P16 / 4;
-  constexpr int64_t CE = CHUNK_BYTES / Elem<E>::kSize;
+  constexpr uint32_t CHUNK = (uint32_t)UNIT_CHUNK_BYTES * CW;  // two units per consumer thread
+  constexpr int64_t CE = CHUNK / Elem<E>::kSize;
+  constexpr uint32_t C = 32u * CW;  // consumer threads
   const uint32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31u;
   if (end <= start) return;
   int64_t a0, a1;
-  const uint32_t nchunks = ring_span(row, start, end, &a0, &a1);
+  const uint32_t nchunks = ring_span(row, start, end, CHUNK, &a0, &a1);
   if (warp == 0) {
     if (lane == 0) {
       // chunks [primed, primed + D) in one L2 prefetch, then chunk c + D as
@@ -914,10 +932,10 @@ __device__ __forceinline__ void scan_pass(Ring& R, const E* __restrict__ row, in
           const int64_t p1 = min(a1, p0 + CE);
           bulk_prefetch_l2(row + p0, (uint32_t)((p1 - p0) * Elem<E>::kSize));
         }
-        ring_issue(R, row, a0, a1, c, lflags);
+        ring_issue(R, row, a0, a1, c, lflags, CHUNK);
       }
     }
-  } else {
+  } else if (warp <= (uint32_t)CW) {
     if (warp == 1) {
       // head [start, a0) on lanes 0.., tail [a1, end) on lanes 16..
       const int64_t nh = a0 - start, nt = end - a1;
@@ -948,20 +966,20 @@ __device__ __forceinline__ void scan_pass(Ring& R, const E* __restrict__ row, in
     uint32_t off = (uint32_t)a0;
     for (uint32_t c = 0; c < nchunks; ++c) {
       if (!mbar_wait(&R.full[s], ph, R.abort)) lflags |= F_TIMEOUT;
-      const uint4* sm = sm0 + s * (uint32_t)(CHUNK_BYTES / 16);
+      const uint4* sm = sm0 + s * (uint32_t)(STAGE_BYTES / 16);
       uint4 u0, u1;
       bool ok0 = true, ok1 = true;
       if (c < nfull) {
         u0 = sm[0];
-        u1 = sm[CONSUMERS];
+        u1 = sm[C];
       } else {
         const int nu = (int)(((uint32_t)a1 - off) / (uint32_t)P16);
         ok0 = (int)ct < nu;
-        ok1 = (int)ct + CONSUMERS < nu;
+        ok1 = (int)(ct + C) < nu;
         u0 = ok0 ? sm[0] : make_uint4(0u, 0u, 0u, 0u);
-        u1 = ok1 ? sm[CONSUMERS] : make_uint4(0u, 0u, 0u, 0u);
+        u1 = ok1 ? sm[C] : make_uint4(0u, 0u, 0u, 0u);
       }
-      const uint32_t i0 = off + (uint32_t)P16 * ct, i1 = i0 + (uint32_t)(P16 * CONSUMERS);
+      const uint32_t i0 = off + (uint32_t)P16 * ct, i1 = i0 + (uint32_t)P16 * C;
       if constexpr (NG == 1) {
         // FP32: the admission mask of all eight scores, kept for the append
         uint32_t m = f.admit_mask(Elem<E>::group(u0, 0)) | (f.admit_mask(Elem<E>::group(u1, 0)) << 4);
@@ -1031,9 +1049,16 @@ __device__ __forceinline__ void scan_pass(Ring& R, const E* __restrict__ row, in
       ph ^= (s == 0u) ? 1u : 0u;
       off += (uint32_t)CE;
     }
+  } else {
+    job();
   }
   R.seq += nchunks;
 }
+
+// The job of a sampler warp with nothing to sample.
+struct NoJob {
+  __device__ __forceinline__ void operator()() const {}
+};
 
 // ------------------------------------------------ frontier refinement engine
 enum PassMode : uint32_t { TAKE_ALL = 0, TAKE_SOME = 1, SMALL_SORT = 2, COLLECT = 3, NEXT_HIST = 4 };
@@ -1466,6 +1491,73 @@ __device__ void sample_thresholds(const E* __restrict__ row, int64_t len, int32_
   const int64_t ns = (len + stride - 1) / stride;
   thresholds_at_ranks(row, ns, stride, sample_rank(T0, ns, len), sample_rank(T1, ns, len), skeys,
                       hist, list, S);
+}
+
+// ------------------------------------------ stage 1 on one warp, ahead of time
+// The same thresholds as sample_thresholds, taken by a single warp with no
+// block barrier and no shared memory, so that the sampler warp can prepare
+// the next row while the consumer warps stream the current one.  The ranks
+// r0 <= r1 are small in every sampling tier (about rho * K / s: 12 to 18 with
+// the default tiers), so the warp keeps the r1 largest sample keys seen so
+// far, sorted across lanes 0..r1-1, and inserts each later key that beats the
+// smallest of them; the r-th largest is then lane r-1's key.  With samples in
+// no particular order a key enters with probability about r1 / (keys seen),
+// so a row of n_s samples costs about r1 * (1 + ln(n_s / r1)) insertions.
+constexpr uint32_t WARP_RANK_MAX = 32;  // ranks the sampler warp can take
+
+// Returns false (nothing computed) when r1 > WARP_RANK_MAX; the row is then
+// sampled at its own start.  Otherwise out = {key(tau0), key(tau1), smallest
+// and largest sample key}, exactly as sample_thresholds leaves them.  Every
+// lane of the warp must call.
+template <class E>
+__device__ __noinline__ bool warp_sample_thresholds(const E* __restrict__ row, int64_t len,
+                                                   int32_t stride, uint32_t T0, uint32_t T1,
+                                                   uint32_t* out) {
+  const uint32_t lane = lane_id();
+  const int64_t ns = (len + stride - 1) / stride;
+  const uint32_t r0 = sample_rank(T0, ns, len), r1 = sample_rank(T1, ns, len);
+  if (r1 > WARP_RANK_MAX || r0 > r1) return false;
+  const uint64_t pol = l2_policy_evict_last();
+  const uint32_t live = (r1 == 32u) ? FULL_MASK : ((1u << r1) - 1u);  // lanes of the list
+  // the list: key 0 marks an empty place (only a NaN pattern has key 0, and
+  // NaN is not a supported score; every valid sample has a larger key)
+  uint32_t top = 0u, floor = 0u;  // floor: the list's smallest key (lane r1 - 1)
+  uint32_t mn = 0xffffffffu, mx = 0u;
+  constexpr int U = 8;  // 256 samples per round trip
+  for (int64_t i0 = 0; i0 < ns; i0 += 32 * U) {
+    uint32_t k[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t i = i0 + 32 * u + lane;
+      k[u] = (i < ns) ? fkey(Elem<E>::load_keep(row + i * stride, pol)) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t i = i0 + 32 * u + lane;
+      if (i < ns) {
+        mn = min(mn, k[u]);
+        mx = max(mx, k[u]);
+      }
+      uint32_t m = __ballot_sync(FULL_MASK, k[u] > floor);
+      while (m) {
+        const uint32_t src = (uint32_t)__ffs(m) - 1u;
+        m &= m - 1u;
+        const uint32_t x = __shfl_sync(FULL_MASK, k[u], src);
+        if (x <= floor) continue;  // the list moved past it
+        // x goes after every listed key >= x; the keys below it move down
+        const uint32_t pos = (uint32_t)__popc(__ballot_sync(FULL_MASK, top >= x) & live);
+        const uint32_t up = __shfl_up_sync(FULL_MASK, top, 1);
+        if (lane > pos) top = up;
+        else if (lane == pos) top = x;
+        floor = __shfl_sync(FULL_MASK, top, r1 - 1u);
+      }
+    }
+  }
+  out[0] = __shfl_sync(FULL_MASK, top, r0 - 1u);
+  out[1] = floor;
+  out[2] = __reduce_min_sync(FULL_MASK, mn);
+  out[3] = __reduce_max_sync(FULL_MASK, mx);
+  return true;
 }
 
 // Seeded bins of the full-row pass: the candidates' keys start at key(tau1);

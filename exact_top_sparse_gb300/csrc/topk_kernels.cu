@@ -76,7 +76,7 @@ __device__ __forceinline__ int32_t row_k_of(const Params& P, int64_t r, uint32_t
 constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 constexpr size_t SH_HDR = align_up(sizeof(Shared), 128);
 constexpr size_t SH_RING = SH_HDR;
-constexpr size_t SH_CAND = SH_RING + (size_t)STAGES * CHUNK_BYTES;
+constexpr size_t SH_CAND = SH_RING + (size_t)STAGES * STAGE_BYTES;
 constexpr size_t SH_HIST = SH_CAND + (size_t)CAP * sizeof(uint2);
 constexpr size_t SH_LIST = SH_HIST + (size_t)NB * sizeof(uint32_t);
 constexpr size_t SH_ROW_TOTAL = SH_LIST + (size_t)THREADS * sizeof(uint32_t);
@@ -257,11 +257,11 @@ struct TieList {
 // stays 0), the seeded histogram of the kept candidates in c.hist.  Returns
 // C(tau0) over the kept candidates (without the ties, which the caller adds
 // when tau0 == tau1); exact unless the candidates overflowed.
-template <class E>
+template <int CW, class E, class J>
 __device__ uint32_t scan_collect(const E* row, int64_t s0, int64_t s1, Ring& R,
                                  const RowCarve& c, uint2* spill, const TieList& tl,
                                  uint32_t key0, uint32_t key1, const Bins& sb, uint32_t& lflags,
-                                 uint32_t primed) {
+                                 uint32_t primed, const J& job) {
   Shared& S = *c.S;
   const float tau1 = key_to_float(key1);
   const uint32_t cap = spill ? (uint32_t)CAP_ALL : (uint32_t)CAP;
@@ -270,12 +270,12 @@ __device__ uint32_t scan_collect(const E* row, int64_t s0, int64_t s1, Ring& R,
   if (tau1 > 0.0f) {
     ScanCollect<true, TIES> f{__float_as_uint(tau1), c.cand, spill, cap, &S.ncand,
                               tl.idx, tl.cap, tl.n, 0u, false};
-    scan_pass(R, row, s0, s1, f, lflags, primed);
+    scan_pass<E, true, TIES, CW>(R, row, s0, s1, f, lflags, primed, job);
     xeq = f.xeq;
   } else {
     ScanCollect<false, TIES> f{key1, c.cand, spill, cap, &S.ncand, tl.idx, tl.cap, tl.n, 0u,
                                false};
-    scan_pass(R, row, s0, s1, f, lflags, primed);
+    scan_pass<E, false, TIES, CW>(R, row, s0, s1, f, lflags, primed, job);
     xeq = f.xeq;
   }
   __syncthreads();
@@ -407,12 +407,52 @@ __device__ int32_t select_after_scan(const E* row, int64_t len, int32_t* out, in
   return path;
 }
 
+// The sampler warp's job while a persistent CTA streams a sampled row:
+// claim the next row and, when that row is sampled, take its stage 1
+// (warp_sample_thresholds, the same thresholds sample_thresholds gives), so
+// that the row starts its full-row pass as soon as this one is done.  The
+// results reach the other warps through S after the block barrier that ends
+// the pass.
+template <class E>
+struct NextRowJob {
+  const E* scores;
+  const int32_t* row_lens;
+  const Params* P;
+  uint32_t* queue;
+  Shared* S;
+  __device__ __forceinline__ void operator()() const {
+    const uint32_t lane = lane_id();
+    uint32_t rn = 0;
+    if (lane == 0) rn = atomicAdd(queue, 1u);
+    rn = __shfl_sync(FULL_MASK, rn, 0);
+    uint32_t key[4] = {0u, 0u, 0u, 0u};
+    bool sampled = false;
+    if ((int64_t)rn < P->M) {
+      uint32_t fl = 0;
+      const int64_t ln = clamp_len(row_lens[rn], P->N_alloc, fl);
+      const int32_t kn = row_k_of(*P, rn, fl);
+      if (ln > kn && kn > 0 && ln >= P->sample_min_len) {
+        const E* row = scores + (int64_t)rn * P->N_alloc;
+        if (lane == 0 && P->pf_next_bytes) prefetch_row_head(row, ln, P->pf_next_bytes);
+        const SampleSpec sp = sample_spec(*P, ln, kn);
+        sampled = warp_sample_thresholds(row, ln, sp.stride, sp.target0, sp.target1, key);
+      }
+    }
+    if (lane == 0) {
+      S->next = rn;
+      S->next_ok = 1u;
+      S->nx_row = rn;
+      S->nx_ok = sampled ? 1u : 0u;
+      for (int j = 0; j < 4; ++j) S->nx_key[j] = key[j];
+    }
+  }
+};
+
 // Warms L2 with the sample points of a row the CTA takes next (evict-last,
 // as the sampler's own loads), so that its sampling, latency-bound DRAM
 // loads otherwise, reads L2 instead.  Issued while the current row is
-// refined.  Every address lies inside the row's valid prefix.  Every thread
-// may call.  (Prefetching the row's first ring chunks as well measured no
-// faster.)
+// refined (persistent kernel without a sampler warp).  Every address lies
+// inside the row's valid prefix.  Every thread may call.
 template <class E>
 __device__ void warm_samples(const E* row, int64_t len, int32_t stride) {
   const int64_t ns = (len + stride - 1) / stride;
@@ -420,11 +460,13 @@ __device__ void warm_samples(const E* row, int64_t len, int32_t stride) {
 }
 
 // ------------------------------------------------------------ persistent path
-template <class E>
+// CW: consumer warps, CONSUMER_WARPS, or one fewer with the last warp as
+// the sampler warp (Params::sampler_warp says which instance is launched).
+template <class E, int CW>
 __global__ void __launch_bounds__(THREADS, 2)
     k_persistent(const E* __restrict__ scores, const int32_t* __restrict__ row_lens,
                  int32_t* __restrict__ out_idx, RowDiag* __restrict__ diag, uint32_t* hdr,
-                 uint2* __restrict__ spill_all, Params P) {
+                 uint2* __restrict__ spill_all, const __grid_constant__ Params P) {
   extern __shared__ __align__(128) uint8_t smem[];
   const RowCarve c = carve(smem);
   // this CTA's global area: candidate spill, then the tie list
@@ -435,13 +477,15 @@ __global__ void __launch_bounds__(THREADS, 2)
   if (threadIdx.x == 0) {
     S.flags = 0;
     S.next_ok = 0;
+    S.nx_ok = 0;
 #ifdef TOPK_PHASE_TIMING
     for (int i = 0; i < NPHASE; ++i) S.ph[i] = 0;
     S.ph_t = clock64();
 #endif
   }
   Ring R;
-  ring_init(R, S, c.ring, hdr + 2);  // hdr[2]: this launch's fail-fast flag
+  // hdr[2]: this launch's fail-fast flag; with CW = 14, warp 15 samples
+  ring_init(R, S, c.ring, hdr + 2, (uint32_t)CW);
   R.pf_ahead = P.pf_ahead;
   const int32_t K = P.K;
   for (;;) {
@@ -451,6 +495,9 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
     __syncthreads();
     const int64_t r = S.row;
+    // stage 1 of this row, when the sampler warp took it during the last pass
+    const bool pre = CW < CONSUMER_WARPS && S.nx_ok != 0u && (int64_t)S.nx_row == r;
+    const uint32_t pk0 = S.nx_key[0], pk1 = S.nx_key[1], pk2 = S.nx_key[2], pk3 = S.nx_key[3];
     __syncthreads();
     phase_mark(S, 0);
     if (r >= P.M) break;
@@ -458,7 +505,10 @@ __global__ void __launch_bounds__(THREADS, 2)
     const int64_t len = clamp_len(row_lens[r], P.N_alloc, lflags);
     const E* row = scores + r * P.N_alloc;
     int32_t* out = out_idx + r * (int64_t)K;
-    if (threadIdx.x == 0) S.nout = 0;
+    if (threadIdx.x == 0) {
+      S.nout = 0;
+      S.nx_ok = 0;
+    }
     __syncthreads();
     const float qnan = __int_as_float(0x7fc00000);
     const int32_t K0 = row_k_of(P, r, lflags);
@@ -478,13 +528,17 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
     // the ring is idle: start the row's first chunks before sampling it
     const uint32_t primed = ring_prime(R, row, 0, len, lflags);
-    {
+    uint32_t key0 = pk0, key1 = pk1, kmin = pk2, kmax = pk3;
+    if (!pre) {
       const SampleSpec sp = sample_spec(P, len, K0);
       sample_thresholds(row, len, sp.stride, sp.target0, sp.target1,
                         reinterpret_cast<uint32_t*>(c.cand), c.hist, c.list, S);
+      key0 = S.key0;
+      key1 = S.key1;
+      kmin = S.kmin;
+      kmax = S.kmax;
     }
     phase_mark(S, 1);
-    const uint32_t key0 = S.key0, key1 = S.key1, kmin = S.kmin, kmax = S.kmax;
     const Bins sb = scan_bins(key1, kmax);
     __syncthreads();
     clear_hist(c.hist);
@@ -493,18 +547,24 @@ __global__ void __launch_bounds__(THREADS, 2)
       S.neq = 0;
     }
     __syncthreads();
-    uint32_t C0 = scan_collect(row, 0, len, R, c, spill, TieList{ties, (uint32_t)min(K0, (int32_t)TIE_CAP), &S.neq},
-                               key0, key1, sb, lflags, primed);
-    // claim the next row now and warm L2 with its sample points while this
-    // one is refined
-    if (threadIdx.x == 0) {
-      S.next = atomicAdd(&hdr[0], 1u);
-      S.next_ok = 1u;
-    }
+    // a sampler warp claims the next row and takes its stage 1 meanwhile
+    const TieList tl{ties, (uint32_t)min(K0, (int32_t)TIE_CAP), &S.neq};
+    uint32_t C0;
+    if constexpr (CW == CONSUMER_WARPS)
+      C0 = scan_collect<CW>(row, 0, len, R, c, spill, tl, key0, key1, sb, lflags, primed, NoJob{});
+    else
+      C0 = scan_collect<CW>(row, 0, len, R, c, spill, tl, key0, key1, sb, lflags, primed,
+                            NextRowJob<E>{scores, row_lens, &P, hdr, &S});
     const uint32_t Cgt = S.ncand, Ceq = S.neq;
     if (key0 == key1) C0 += Ceq;
-    __syncthreads();
-    {
+    if (CW == CONSUMER_WARPS) {
+      // claim the next row now and warm L2 with its sample points while
+      // this one is refined
+      if (threadIdx.x == 0) {
+        S.next = atomicAdd(&hdr[0], 1u);
+        S.next_ok = 1u;
+      }
+      __syncthreads();
       const int64_t rn = S.next;
       if (rn < P.M) {
         uint32_t fl = 0;
@@ -705,9 +765,9 @@ __global__ void __launch_bounds__(THREADS, 2)
     clear_hist(c.hist);
     if (threadIdx.x == 0) S.ncand = 0;
     __syncthreads();
-    const uint32_t C0 = scan_collect(row, s0, s1, R, c, nullptr,
+    const uint32_t C0 = scan_collect<CONSUMER_WARPS>(row, s0, s1, R, c, nullptr,
                                      TieList{gties, (uint32_t)TIE_CAP, &h->neq}, key0, key1, sb,
-                                     lflags, 0u);
+                                     lflags, 0u, NoJob{});
     const uint32_t nloc = S.ncand;
     if (threadIdx.x == 0) {
       atomicAdd(&h->c0, C0);
@@ -937,8 +997,12 @@ cudaError_t prepare_device() {
       cudaSuccess)
     return e;
   const void* row_kernels[] = {
-      (const void*)k_persistent<float>, (const void*)k_persistent<uint16_t>,
-      (const void*)k_persistent<uint8_t>, (const void*)k_kv_segment<float>,
+      (const void*)k_persistent<float, CONSUMER_WARPS>,
+      (const void*)k_persistent<uint16_t, CONSUMER_WARPS>,
+      (const void*)k_persistent<uint8_t, CONSUMER_WARPS>,
+      (const void*)k_persistent<float, CONSUMER_WARPS - 1>,
+      (const void*)k_persistent<uint16_t, CONSUMER_WARPS - 1>,
+      (const void*)k_persistent<uint8_t, CONSUMER_WARPS - 1>, (const void*)k_kv_segment<float>,
       (const void*)k_kv_segment<uint16_t>, (const void*)k_kv_segment<uint8_t>};
   for (const void* fn : row_kernels)
     if ((e = set_smem(fn, persistent_smem_bytes())) != cudaSuccess) return e;
@@ -957,7 +1021,7 @@ cudaError_t prepare_device() {
 }
 
 cudaError_t persistent_occupancy(int* blocks_per_sm) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k_persistent<float>, THREADS,
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k_persistent<float, CONSUMER_WARPS>, THREADS,
                                                        persistent_smem_bytes());
 }
 
@@ -973,7 +1037,11 @@ template <class E>
 static cudaError_t launch_persistent_t(const E* scores, const int32_t* row_lens, int32_t* out,
                                        RowDiag* diag, uint32_t* hdr, void* spill, int grid,
                                        const Params& P, cudaStream_t st) {
-  k_persistent<E><<<grid, THREADS, persistent_smem_bytes(), st>>>(
+  if (P.sampler_warp)
+    k_persistent<E, CONSUMER_WARPS - 1><<<grid, THREADS, persistent_smem_bytes(), st>>>(
+      scores, row_lens, out, diag, hdr, static_cast<uint2*>(spill), P);
+  else
+    k_persistent<E, CONSUMER_WARPS><<<grid, THREADS, persistent_smem_bytes(), st>>>(
       scores, row_lens, out, diag, hdr, static_cast<uint2*>(spill), P);
   return cudaGetLastError();
 }

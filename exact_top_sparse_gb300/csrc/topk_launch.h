@@ -34,6 +34,11 @@ struct Params {
   // row it takes next as soon as its current row's pass ends (0: none).
   uint32_t pf_ahead;
   uint32_t pf_next_bytes;
+  // Persistent kernel: 1 when its last warp, instead of consuming chunks,
+  // claims the next row and takes its stage 1 during each certify pass (14
+  // consumer warps, 14 KB chunks); 0 for 15 consumer warps, the next row then
+  // claimed after the pass and sampled at its own start.
+  uint32_t sampler_warp;
 };
 
 // Same layout as topk_row_diag in the public header.
