@@ -8,10 +8,13 @@ microseconds one CTA spends per row in each phase:
 
   claim        taking the row from the queue
   first_load   the first ring copies, the sample loads and their range
-  sample_rank  the two sample ranks that give tau0 and tau1
+  sample_rank  the two sample ranks that give tau0 and tau1 (with a sampler
+               warp, which took them during the previous row's pass: the
+               first ring copies only)
   scan         the certify + collect pass over the whole row
   tally        C(tau0) and the seeded histogram from the candidates
-  next         claiming the next row and warming L2 with its sample points
+  next         without a sampler warp: claiming the next row and warming L2
+               with its sample points
   select       refinement (and, on rare rows, recovery or a re-read)
   finish       closing the row (padding, flags, diagnostics)
   unsampled    rows served without sampling (sentinel or exact path)
