@@ -719,7 +719,7 @@ struct ScanCollect {
   // taking an atomic and a global store.
   // Counts the ties of mask q (element e of group a for bits 0-3, of group b
   // for bits 4-7) and keeps their indices while the tie list has room.
-  __device__ __forceinline__ void put_ties(uint32_t q, int64_t ia, int64_t ib) {
+  __device__ __forceinline__ void put_ties(uint32_t q, uint32_t ia, uint32_t ib) {
     const uint32_t c = (uint32_t)__popc(q);
     if (full) {  // the list has its first tie_cap indices: only count
       xeq += c;
@@ -736,7 +736,7 @@ struct ScanCollect {
   // Appends the admitted scores of two groups of four (elements ia.. of va
   // when ha, ib.. of vb when hb) with one shared-memory atomic, visiting only
   // the admitted elements.
-  __device__ __forceinline__ void lane_put2(int64_t ia, const float4& va, bool ha, int64_t ib,
+  __device__ __forceinline__ void lane_put2(uint32_t ia, const float4& va, bool ha, uint32_t ib,
                                             const float4& vb, bool hb) {
     const uint32_t m = (ha ? admit_mask(va) : 0u) | ((hb ? admit_mask(vb) : 0u) << 4);
     if (!m) return;
@@ -746,8 +746,8 @@ struct ScanCollect {
   }
   // Candidates of mask m and ties of mask q (bits 0-3: elements ia.. of va,
   // bits 4-7: elements ib.. of vb).
-  __device__ __forceinline__ void put_masked(uint32_t m, uint32_t q, int64_t ia, const float4& va,
-                                             int64_t ib, const float4& vb) {
+  __device__ __forceinline__ void put_masked(uint32_t m, uint32_t q, uint32_t ia, const float4& va,
+                                             uint32_t ib, const float4& vb) {
     if (TIES && q) put_ties(q, ia, ib);
     if (!m) return;
     uint32_t pos = atomicAdd(ncand, (uint32_t)__popc(m));
@@ -757,7 +757,10 @@ struct ScanCollect {
       const float4 v = e < 4u ? va : vb;
       const uint32_t k = e & 3u;
       const float x = k == 0u ? v.x : (k == 1u ? v.y : (k == 2u ? v.z : v.w));
-      const uint2 ent = make_uint2((uint32_t)((e < 4u ? ia : ib) + k), fkey(x));
+      // an admitted score above a positive tau1 is positive: its key is its
+      // bits with the sign bit set
+      const uint2 ent = make_uint2((e < 4u ? ia : ib) + k,
+                                   POS ? (__float_as_uint(x) | 0x80000000u) : fkey(x));
       if (pos < (uint32_t)CAP) cand[pos] = ent;
       else if (pos < cap) spill[pos - (uint32_t)CAP] = ent;
       ++pos;
@@ -859,7 +862,7 @@ struct ScanCollect {
   }
   // Appends the admitted scores among the elements of v selected by vm
   // (element i0 + e is lane e).
-  __device__ __forceinline__ void lane_put(int64_t i0, const float4& v, uint32_t vm) {
+  __device__ __forceinline__ void lane_put(uint32_t i0, const float4& v, uint32_t vm) {
     const uint32_t m = admit_mask(v) & vm;
     if (!m) return;
     const uint32_t q = TIES ? (tie_mask(v) & vm) : 0u;

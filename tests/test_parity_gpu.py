@@ -459,3 +459,31 @@ def test_plan_kinds(ets):
     assert ets.plan(512, 131072, K)["kind"] == "persistent"   # short rows: split only when tiny
     assert ets.plan(sms // 4, 131072, K)["kind"] == "kvsplit"
     assert ets.plan(4 * sms, 1048576, K)["kind"] == "persistent"
+
+
+# ------------------------------------------------------------ sampler warp
+@pytest.mark.parametrize("order", ["rising", "falling", "ties"])
+def test_sampler_warp_thresholds_on_ordered_rows(ets, order):
+    """Rows narrower than 512K FP32 elements run the sampler-warp kernel: one
+    warp ranks the next row's samples while the others stream the current
+    row, keeping the r1 largest sample keys in a list sorted across its
+    lanes.  Rows whose scores rise along the row make every sample enter that
+    list, falling rows make none after the first, and rows of a few values
+    make most samples tie with the list's smallest key; tau0, tau1, the
+    counts and the path must still equal the oracle's on every sampled row
+    (more rows than CTAs, so most rows are prepared by a sampler warp)."""
+    assert ets.plan(1024, 65536, K)["kind"] == "persistent"
+    N, M = 65536, 1024
+    lens = torch.full((M,), N, dtype=torch.int32) - torch.arange(M, dtype=torch.int32) * 16
+    g = torch.Generator().manual_seed(71)
+    base = torch.arange(N, dtype=torch.float32) / N
+    if order == "rising":
+        x = base.repeat(M, 1) + torch.rand((M, N), generator=g) * 1e-3
+    elif order == "falling":
+        x = base.flip(0).repeat(M, 1) + torch.rand((M, N), generator=g) * 1e-3
+    else:
+        x = torch.randint(0, 6, (M, N), generator=g).to(torch.float32)
+    x = x.to(DEV)
+    out, dg = run(ets, x, lens, diag=True)
+    verify(x, lens, K, out)
+    verify_diag(ets, x, lens, K, dg)
