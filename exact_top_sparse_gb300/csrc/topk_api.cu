@@ -26,12 +26,14 @@ constexpr size_t kHdrBytes = 256;
 constexpr int64_t kMinSegment = 32768;  // floats per KV-split segment, at least
 // Planner crossovers, measured on GB300 over 128K-1M columns and M = 64-2048:
 // with at least two rows per resident CTA the persistent queue balances
-// well; below that, rows of 384K+ elements leave a long tail on the
+// well; below that, rows of 768K+ elements leave a long tail on the
 // persistent path and are split, and shorter rows are split only when they
-// would leave half the CTAs idle.  KV-split cuts rows into segments of
-// about 256K floats, and into more when that gives fewer CTAs than resident.
+// would leave half the CTAs idle (512K x 256 / x 512: persistent 0.121 /
+// 0.224 ms, split 0.134 / 0.231; 768K x 512: 0.320 against 0.307; 1M x 512:
+// 0.397 against 0.381).  KV-split cuts rows into segments of about 256K
+// floats, and into more when that gives fewer CTAs than resident.
 constexpr int kPersistentRowsPerCta = 2;
-constexpr int64_t kKvLongRow = 393216;
+constexpr int64_t kKvLongRow = 786432;
 constexpr int64_t kKvSegmentTarget = 262144;
 
 std::mutex g_mu;

@@ -457,6 +457,8 @@ def test_plan_kinds(ets):
     assert p["kind"] == "kvsplit" and p["segments"] > 1
     sms = p["sm_count"]
     assert ets.plan(512, 131072, K)["kind"] == "persistent"   # short rows: split only when tiny
+    assert ets.plan(512, 524288, K)["kind"] == "persistent"
+    assert ets.plan(512, 786432, K)["kind"] == "kvsplit"
     assert ets.plan(sms // 4, 131072, K)["kind"] == "kvsplit"
     assert ets.plan(4 * sms, 1048576, K)["kind"] == "persistent"
 
