@@ -85,11 +85,12 @@ def max_over_ranks(value: float, ws: int, device) -> float:
     return float(t.item())
 
 
-def copy_only_rate(h, K, steps=3, chunk_bytes=1 << 30):
-    """Rows per second that the host-buffer call's copies alone allow: the
-    pinned host rows h [M, N] go to the device in chunks of about 1 GiB,
+def copy_only_step(h, K, chunk_bytes=1 << 30):
+    """One step of the copies the host-buffer call makes, without selection:
+    the pinned host rows h [M, N] go to the device in chunks of about 1 GiB,
     alternating between two streams as topk_ragged_host does, and K indices
-    per row come back; no selection runs.  Returns (rows/s, H2D GB/s)."""
+    per row come back.  Returns (step, release): step() runs and waits for
+    one step; release() frees its buffers."""
     M, N = h.shape
     rows = max(1, min(M, chunk_bytes // max(1, N * 4)))
     dev = torch.device("cuda", torch.cuda.current_device())
@@ -98,25 +99,21 @@ def copy_only_rate(h, K, steps=3, chunk_bytes=1 << 30):
     ho = torch.empty((M, K), dtype=torch.int32, pin_memory=True)
     sts = [torch.cuda.Stream(device=dev) for _ in range(2)]
 
-    def one():
+    def step():
         for c, r0 in enumerate(range(0, M, rows)):
             n = min(rows, M - r0)
             with torch.cuda.stream(sts[c & 1]):
                 bufs[c & 1][:n].copy_(h[r0:r0 + n], non_blocking=True)
                 ho[r0:r0 + n].copy_(outs[c & 1][:n], non_blocking=True)
-        for s in sts:
-            s.synchronize()
+        for st in sts:
+            st.synchronize()
 
-    one()
-    ts = []
-    for _ in range(steps):
-        t0 = time.perf_counter()
-        one()
-        ts.append(time.perf_counter() - t0)
-    t = sum(ts) / len(ts)
-    del bufs, outs
-    torch.cuda.empty_cache()
-    return M / t, M * N * 4 / t / 1e9
+    def release():
+        bufs.clear()
+        outs.clear()
+        torch.cuda.empty_cache()
+
+    return step, release
 
 
 def job_rows_per_s(ws: int, M: int, steps: int, total_ms: float) -> float:
@@ -867,14 +864,23 @@ def run_gb300(args):
             hl = lens.numpy().copy()
             ho = np.empty((M, K), dtype=np.int32)
             hn = h.numpy()
+            copy_step, copy_release = copy_only_step(h, K)
             ets.topk_ragged_host(hn, hl, K, out=ho)
-            ts = []
+            copy_step()
+            # the call and its copy-only bound alternate step by step, so a
+            # host link whose speed drifts over seconds affects both alike
+            ts, tc = [], []
             for _ in range(args.e2e_steps):
                 t0 = time.perf_counter()
                 ets.topk_ragged_host(hn, hl, K, out=ho)
                 ts.append(time.perf_counter() - t0)
+                t0 = time.perf_counter()
+                copy_step()
+                tc.append(time.perf_counter() - t0)
+            copy_release()
             e2e_rate = M * len(ts) / sum(ts)
-            copy_rate, h2d_gbs = copy_only_rate(h, K, steps=args.e2e_steps)
+            copy_rate = M * len(tc) / sum(tc)
+            h2d_gbs = M * N * 4 * len(tc) / sum(tc) / 1e9
             result["e2e"] = {"value": e2e_rate, "unit": UNIT,
                              "h2d_bytes_per_step": M * N * 4 + M * 4,
                              "d2h_bytes_per_step": M * K * 4,
@@ -882,7 +888,8 @@ def run_gb300(args):
                              "copy_only": {"value": copy_rate, "unit": UNIT, "h2d_gbs": h2d_gbs,
                                            "what": "the same host->device and device->host "
                                                    "bytes in the same 1 GiB chunks on two "
-                                                   "streams, no selection"}}
+                                                   "streams, no selection, timed in steps "
+                                                   "alternating with the call's"}}
             del h
         except RuntimeError as e:
             result["e2e"] = {"value": None, "unit": UNIT, "error": str(e)[:200]}

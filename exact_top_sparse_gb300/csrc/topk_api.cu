@@ -616,7 +616,7 @@ int topk_ragged_host(const float* h_scores, const int32_t* h_lens, int64_t M, in
   // Calls from several host threads on one device take turns on its buffers
   // and streams.
   std::lock_guard<std::mutex> pipe_lock(hp->mu);
-  const size_t need_s = (size_t)rows * row_bytes, need_l = (size_t)rows * 4,
+  const size_t need_s = (size_t)rows * row_bytes, need_l = (size_t)M * 4,
                need_o = (size_t)rows * K * 4;
   for (int i = 0; i < 2; ++i) {
     if (!hp->st[i] && cudaStreamCreateWithFlags(&hp->st[i], cudaStreamNonBlocking) != cudaSuccess)
@@ -645,6 +645,17 @@ int topk_ragged_host(const float* h_scores, const int32_t* h_lens, int64_t M, in
     hp->lens_bytes = need_l;
     hp->out_bytes = need_o;
   }
+  // Every row length in one copy (a few KB; the caller's array may be
+  // pageable, which would make a copy per chunk hold the host thread).
+  if (cudaMemcpy(hp->lens[0], h_lens, (size_t)M * 4, cudaMemcpyHostToDevice) != cudaSuccess)
+    return TOPK_ERR_CUDA;
+  // Chunk c's result is read back only after chunk c + 1's copy and
+  // selection are queued: a read into pageable memory holds the host thread
+  // until it is done, and the copy engine then still has chunk c + 1's rows
+  // to move.  Each buffer pair is reused two chunks later on the same stream,
+  // after its result was read.
+  int64_t prev_r0 = -1, prev_n = 0;
+  int prev_s = 0;
   for (int64_t r0 = 0, c = 0; r0 < M; r0 += rows, ++c) {
     const int64_t n = (M - r0) < rows ? (M - r0) : rows;
     const int s = (int)(c & 1);
@@ -653,15 +664,20 @@ int topk_ragged_host(const float* h_scores, const int32_t* h_lens, int64_t M, in
         cudaMemcpyAsync(hp->scores[s], h_scores + r0 * N_alloc, (size_t)n * row_bytes,
                         cudaMemcpyHostToDevice, st) != cudaSuccess)
       return TOPK_ERR_CUDA;
-    if (cudaMemcpyAsync(hp->lens[s], h_lens + r0, (size_t)n * 4, cudaMemcpyHostToDevice, st) !=
-        cudaSuccess)
-      return TOPK_ERR_CUDA;
-    rc = topk_ragged(hp->scores[s], hp->lens[s], n, N_alloc, K, hp->out[s], st);
+    rc = topk_ragged(hp->scores[s], hp->lens[0] + r0, n, N_alloc, K, hp->out[s], st);
     if (rc) return rc;
-    if (cudaMemcpyAsync(h_out + r0 * K, hp->out[s], (size_t)n * K * 4, cudaMemcpyDeviceToHost,
-                        st) != cudaSuccess)
+    if (prev_r0 >= 0 &&
+        cudaMemcpyAsync(h_out + prev_r0 * K, hp->out[prev_s], (size_t)prev_n * K * 4,
+                        cudaMemcpyDeviceToHost, hp->st[prev_s]) != cudaSuccess)
       return TOPK_ERR_CUDA;
+    prev_r0 = r0;
+    prev_n = n;
+    prev_s = s;
   }
+  if (prev_r0 >= 0 &&
+      cudaMemcpyAsync(h_out + prev_r0 * K, hp->out[prev_s], (size_t)prev_n * K * 4,
+                      cudaMemcpyDeviceToHost, hp->st[prev_s]) != cudaSuccess)
+    return TOPK_ERR_CUDA;
   for (int i = 0; i < 2; ++i)
     if (cudaStreamSynchronize(hp->st[i]) != cudaSuccess) return TOPK_ERR_CUDA;
   return TOPK_OK;
