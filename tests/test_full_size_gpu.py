@@ -14,6 +14,7 @@ Workloads (synthetic indexer-like rows, see exact_top_sparse_gb300.synth):
   * the width sweep 16K..64K x M in {64 .. 4096} (section "采样不是处处都该开");
   * the stride sweep s in {16, 64, 128, 256} at 32K and 256K columns;
   * decode-style calls of one and two full-length rows at 128K and 1M;
+  * bfloat16 and FP8 E4M3 rows of the 8192-row window at 128K and 1M;
   * every Top-K call of the 245K-token prefill trace (section "框架轨迹").
 """
 import numpy as np
@@ -84,6 +85,30 @@ def test_operator_matrix_every_row(ets, N, M_other, group_other):
     got, dg = run(ets, xs, ls, diag=True)
     verify_every_row(ets, xs, ls, K, got, dg)
     _release(x, xs, got)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+@pytest.mark.parametrize("N", [131072, 1048576])
+def test_narrow_rows_every_row(ets, dtype, N):
+    """bfloat16 and FP8 E4M3 rows of the 8192-row causal window (the
+    sampler-warp kernel serves every narrow row), every row against the
+    oracle run on PyTorch's own widening of the same values, with thresholds,
+    counts and paths."""
+    M = 8192
+    lens = synth.causal_lens(N, M, 0)
+    x = synth.indexer_rows(lens, N, seed=13, device=DEV)
+    x = x.to(torch.bfloat16) if dtype == "bf16" else (x * 4.0).clamp(max=448.0).to(
+        torch.float8_e4m3fn)
+    got, dg = run(ets, x, lens, diag=True)
+    assert not np.any(dg["flags"] & (ets.FLAG_INTERNAL | ets.FLAG_TIMEOUT))
+    step = max(1, CHUNK_BYTES // (N * 4))
+    for r0 in range(0, M, step):
+        r1 = min(M, r0 + step)
+        xf = x[r0:r1].float()
+        verify(xf, lens[r0:r1], K, got[r0:r1])
+        verify_diag(ets, xf, lens[r0:r1], K, dg[r0:r1])
+        del xf
+    _release(x, got)
 
 
 @pytest.mark.parametrize("N", [16384, 24576, 32768, 40960, 49152, 57344, 65536])
