@@ -860,6 +860,25 @@ struct ScanCollect {
   __device__ static __forceinline__ uint32_t flags4(uint32_t p) {
     return (((p >> 7) & 0x01010101u) * 0x01020408u) >> 24;
   }
+  // Candidates of a 16-bit mask over four groups of four scores (bits 4j..4j+3:
+  // elements ij.. of vj), scores without ties (FP32 rows), one atomic.
+  __device__ __forceinline__ void put_masked16(uint32_t m, uint32_t ia, const float4& va,
+                                               uint32_t ib, const float4& vb, uint32_t ic,
+                                               const float4& vc, uint32_t id, const float4& vd) {
+    uint32_t pos = atomicAdd(ncand, (uint32_t)__popc(m));
+    do {
+      const uint32_t e = (uint32_t)__ffs(m) - 1u;
+      m &= m - 1u;
+      const uint32_t j = e >> 2, k = e & 3u;
+      const float4 v = j < 2u ? (j == 0u ? va : vb) : (j == 2u ? vc : vd);
+      const uint32_t i = j < 2u ? (j == 0u ? ia : ib) : (j == 2u ? ic : id);
+      const float x = k == 0u ? v.x : (k == 1u ? v.y : (k == 2u ? v.z : v.w));
+      const uint2 ent = make_uint2(i + k, POS ? (__float_as_uint(x) | 0x80000000u) : fkey(x));
+      if (pos < (uint32_t)CAP) cand[pos] = ent;
+      else if (pos < cap) spill[pos - (uint32_t)CAP] = ent;
+      ++pos;
+    } while (m);
+  }
   // Appends the admitted scores among the elements of v selected by vm
   // (element i0 + e is lane e).
   __device__ __forceinline__ void lane_put(uint32_t i0, const float4& v, uint32_t vm) {
@@ -967,7 +986,42 @@ __device__ __forceinline__ void scan_pass(Ring& R, const E* __restrict__ row, in
     const uint32_t nfull = (uint32_t)((a1 - a0) / CE);
     const uint4* const sm0 = reinterpret_cast<const uint4*>(R.buf) + ct;
     uint32_t off = (uint32_t)a0;
-    for (uint32_t c = 0; c < nchunks; ++c) {
+    uint32_t c = 0;
+    if constexpr (NG == 1 && CW < CONSUMER_WARPS) {
+      // FP32 rows on the sampler-warp kernel (rows narrower than 512K
+      // elements, a few percent of their scores admitted): full chunks are
+      // taken in pairs, so that one 16-score mask, one atomic and one append
+      // loop serve two chunks (a warp's append loop runs as long as its
+      // busiest lane, which matters less over more scores).
+      for (; c + 1u < nfull; c += 2u) {
+        const uint32_t s1 = (s + 1u == (uint32_t)STAGES) ? 0u : s + 1u;
+        const uint32_t ph1 = ph ^ ((s1 == 0u) ? 1u : 0u);
+        if (!mbar_wait(&R.full[s], ph, R.abort)) lflags |= F_TIMEOUT;
+        if (!mbar_wait(&R.full[s1], ph1, R.abort)) lflags |= F_TIMEOUT;
+        const uint4* sa = sm0 + s * (uint32_t)(STAGE_BYTES / 16);
+        const uint4* sb = sm0 + s1 * (uint32_t)(STAGE_BYTES / 16);
+        const uint4 u0 = sa[0], u1 = sa[C], u2 = sb[0], u3 = sb[C];
+        const uint32_t m = f.admit_mask(Elem<E>::group(u0, 0)) |
+                           (f.admit_mask(Elem<E>::group(u1, 0)) << 4) |
+                           (f.admit_mask(Elem<E>::group(u2, 0)) << 8) |
+                           (f.admit_mask(Elem<E>::group(u3, 0)) << 12);
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&R.empty[s]);
+          mbar_arrive(&R.empty[s1]);
+        }
+        if (m) {
+          const uint32_t i0 = off + (uint32_t)P16 * ct, i2 = i0 + (uint32_t)CE;
+          f.put_masked16(m, i0, Elem<E>::group(u0, 0), i0 + (uint32_t)P16 * C,
+                         Elem<E>::group(u1, 0), i2, Elem<E>::group(u2, 0),
+                         i2 + (uint32_t)P16 * C, Elem<E>::group(u3, 0));
+        }
+        s = (s1 + 1u == (uint32_t)STAGES) ? 0u : s1 + 1u;
+        ph = ph1 ^ ((s == 0u) ? 1u : 0u);
+        off += 2u * (uint32_t)CE;
+      }
+    }
+    for (; c < nchunks; ++c) {
       if (!mbar_wait(&R.full[s], ph, R.abort)) lflags |= F_TIMEOUT;
       const uint4* sm = sm0 + s * (uint32_t)(STAGE_BYTES / 16);
       uint4 u0, u1;
