@@ -987,29 +987,29 @@ __device__ __forceinline__ void scan_pass(Ring& R, const E* __restrict__ row, in
     const uint4* const sm0 = reinterpret_cast<const uint4*>(R.buf) + ct;
     uint32_t off = (uint32_t)a0;
     uint32_t c = 0;
-    if constexpr (NG == 1 && CW < CONSUMER_WARPS) {
-      // FP32 rows on the sampler-warp kernel (rows narrower than 512K
-      // elements, a few percent of their scores admitted): full chunks are
-      // taken in pairs, so that one 16-score mask, one atomic and one append
-      // loop serve two chunks (a warp's append loop runs as long as its
-      // busiest lane, which matters less over more scores).
+    if constexpr (NG == 1) {
+      // FP32 rows: full chunks are taken in pairs, so that one 16-score mask,
+      // one atomic and one append loop serve two chunks (a warp's append
+      // loop runs as long as its busiest lane, which matters less over more
+      // scores); each stage is handed back as soon as its mask is formed, so
+      // the ring keeps its depth.
       for (; c + 1u < nfull; c += 2u) {
         const uint32_t s1 = (s + 1u == (uint32_t)STAGES) ? 0u : s + 1u;
         const uint32_t ph1 = ph ^ ((s1 == 0u) ? 1u : 0u);
         if (!mbar_wait(&R.full[s], ph, R.abort)) lflags |= F_TIMEOUT;
-        if (!mbar_wait(&R.full[s1], ph1, R.abort)) lflags |= F_TIMEOUT;
         const uint4* sa = sm0 + s * (uint32_t)(STAGE_BYTES / 16);
-        const uint4* sb = sm0 + s1 * (uint32_t)(STAGE_BYTES / 16);
-        const uint4 u0 = sa[0], u1 = sa[C], u2 = sb[0], u3 = sb[C];
-        const uint32_t m = f.admit_mask(Elem<E>::group(u0, 0)) |
-                           (f.admit_mask(Elem<E>::group(u1, 0)) << 4) |
-                           (f.admit_mask(Elem<E>::group(u2, 0)) << 8) |
-                           (f.admit_mask(Elem<E>::group(u3, 0)) << 12);
+        const uint4 u0 = sa[0], u1 = sa[C];
+        uint32_t m = f.admit_mask(Elem<E>::group(u0, 0)) |
+                     (f.admit_mask(Elem<E>::group(u1, 0)) << 4);
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&R.empty[s]);
-          mbar_arrive(&R.empty[s1]);
-        }
+        if (lane == 0) mbar_arrive(&R.empty[s]);
+        if (!mbar_wait(&R.full[s1], ph1, R.abort)) lflags |= F_TIMEOUT;
+        const uint4* sb = sm0 + s1 * (uint32_t)(STAGE_BYTES / 16);
+        const uint4 u2 = sb[0], u3 = sb[C];
+        m |= (f.admit_mask(Elem<E>::group(u2, 0)) << 8) |
+             (f.admit_mask(Elem<E>::group(u3, 0)) << 12);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&R.empty[s1]);
         if (m) {
           const uint32_t i0 = off + (uint32_t)P16 * ct, i2 = i0 + (uint32_t)CE;
           f.put_masked16(m, i0, Elem<E>::group(u0, 0), i0 + (uint32_t)P16 * C,
