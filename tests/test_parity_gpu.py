@@ -489,3 +489,37 @@ def test_sampler_warp_thresholds_on_ordered_rows(ets, order):
     out, dg = run(ets, x, lens, diag=True)
     verify(x, lens, K, out)
     verify_diag(ets, x, lens, K, dg)
+
+
+# ------------------------------------------------------ infinities in the rows
+@pytest.mark.parametrize("kind", ["auto", "persistent", "kvsplit"])
+def test_infinities_inside_the_valid_prefix(params, kind):
+    """+inf and -inf are ordinary scores inside a row's valid prefix (the key
+    transform keeps the IEEE order): some rows carry a few +inf and many -inf,
+    one row is all -inf (every score ties), one is all +inf, one has exactly K
+    +inf (they are the answer), one has -inf everywhere but K - 1 finite
+    scores.  Every row must pass the checker and equal the oracle's set
+    where untied; sampled rows reproduce the oracle's thresholds."""
+    ets = params
+    kinds = {"auto": ets.KIND_AUTO, "persistent": ets.KIND_PERSISTENT,
+             "kvsplit": ets.KIND_KVSPLIT}
+    ets.set_params(force_kind=kinds[kind], kv_segments=3 if kind == "kvsplit" else 0)
+    N, M = 65536, 640 if kind != "kvsplit" else 48
+    lens = synth.causal_lens(N, M, 0, window=M * (8192 // M))
+    x = synth.indexer_rows(lens, N, seed=91, device=DEV)
+    g = torch.Generator(device=DEV).manual_seed(92)
+    r = torch.rand(x.shape, generator=g, device=DEV)
+    x = torch.where(r < 0.001, torch.full_like(x, float("inf")), x)
+    x = torch.where((r > 0.5) & (r < 0.51), torch.full_like(x, float("-inf")), x)
+    L0 = int(lens[0])
+    x[0, :L0] = float("-inf")
+    x[1, :int(lens[1])] = float("inf")
+    x[2, : 3 * K : 3] = float("inf")
+    x[3, :int(lens[3])] = float("-inf")
+    x[3, 100:100 + K - 1] = 1.0
+    # the causal suffix stays -inf
+    for i in range(4):
+        x[i, int(lens[i]):] = float("-inf")
+    out, dg = run(ets, x, lens, diag=True)
+    verify(x, lens, K, out)
+    verify_diag(ets, x, lens, K, dg)
