@@ -492,10 +492,11 @@ def test_sampler_warp_thresholds_on_ordered_rows(ets, order):
 
 
 # ------------------------------------------------------ infinities in the rows
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("kind", ["auto", "persistent", "kvsplit"])
-def test_infinities_inside_the_valid_prefix(params, kind):
+def test_infinities_inside_the_valid_prefix(params, kind, dtype):
     """+inf and -inf are ordinary scores inside a row's valid prefix (the key
-    transform keeps the IEEE order): some rows carry a few +inf and many -inf,
+    transform keeps the IEEE order), in FP32 and bfloat16 rows: some rows carry a few +inf and many -inf,
     one row is all -inf (every score ties), one is all +inf, one has exactly K
     +inf (they are the answer), one has -inf everywhere but K - 1 finite
     scores.  Every row must pass the checker and equal the oracle's set
@@ -520,6 +521,9 @@ def test_infinities_inside_the_valid_prefix(params, kind):
     # the causal suffix stays -inf
     for i in range(4):
         x[i, int(lens[i]):] = float("-inf")
+    if dtype == "bf16":
+        x = x.to(torch.bfloat16)  # +-inf are bfloat16 values too
     out, dg = run(ets, x, lens, diag=True)
-    verify(x, lens, K, out)
-    verify_diag(ets, x, lens, K, dg)
+    xf = x.float()
+    verify(xf, lens, K, out)
+    verify_diag(ets, xf, lens, K, dg)
