@@ -36,6 +36,39 @@ constexpr int NPHASE = 12;
 __device__ unsigned long long g_phase[NPHASE];
 #endif
 
+// Per-CTA timeline of a k_persistent launch (a build with -DTOPK_PHASE_TIMING
+// only; global timer, ns): slot 0 the CTA's start, 1 its exit, then for each
+// of its first TL_ROWS rows five slots: row + 1, the claim, the start and the
+// end of the full-row pass (0 for a row served without sampling) and the
+// row's close.
+constexpr int TL_CTAS = 1024, TL_ROWS = 4, TL_SLOTS = 2 + 5 * TL_ROWS;
+#ifdef TOPK_PHASE_TIMING
+__device__ unsigned long long g_timeline[TL_CTAS * TL_SLOTS];
+#endif
+__device__ __forceinline__ unsigned long long tl_now() {
+#ifdef TOPK_PHASE_TIMING
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+#else
+  return 0;
+#endif
+}
+// Thread 0 writes slot `slot` of its CTA's record (no-op without the flag).
+__device__ __forceinline__ void tl_put(int slot, unsigned long long v) {
+#ifdef TOPK_PHASE_TIMING
+  if (threadIdx.x == 0 && blockIdx.x < (unsigned)TL_CTAS && slot < TL_SLOTS)
+    g_timeline[(size_t)blockIdx.x * TL_SLOTS + slot] = v;
+#else
+  (void)slot;
+  (void)v;
+#endif
+}
+// Field f (0..4) of the CTA's n-th row.
+__device__ __forceinline__ void tl_row(int n, int f, unsigned long long v) {
+  if (n < TL_ROWS) tl_put(2 + 5 * n + f, v);
+}
+
 // Sampling stride and targets of a row of `len` elements.
 struct SampleSpec {
   int32_t stride;
@@ -474,6 +507,8 @@ __global__ void __launch_bounds__(THREADS, 2)
   uint2* spill = reinterpret_cast<uint2*>(area);
   uint32_t* ties = reinterpret_cast<uint32_t*>(area + (size_t)SPILL * sizeof(uint2));
   Shared& S = *c.S;
+  tl_put(0, tl_now());
+  int nrow = 0;  // rows this CTA has taken (timeline only)
   if (threadIdx.x == 0) {
     S.flags = 0;
     S.next_ok = 0;
@@ -501,6 +536,8 @@ __global__ void __launch_bounds__(THREADS, 2)
     __syncthreads();
     phase_mark(S, 0);
     if (r >= P.M) break;
+    tl_row(nrow, 0, (unsigned long long)r + 1u);
+    tl_row(nrow, 1, tl_now());
     uint32_t lflags = 0;
     const int64_t len = clamp_len(row_lens[r], P.N_alloc, lflags);
     const E* row = scores + r * P.N_alloc;
@@ -517,6 +554,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       if (threadIdx.x == 0) S.nout = (uint32_t)K0;
       finish_row(S, out, K0, K, lflags, diag, r, PATH_SENTINEL, qnan, qnan, 0, 0);
       phase_mark(S, 7);
+      tl_row(nrow++, 4, tl_now());
       continue;
     }
     if (len < P.sample_min_len) {
@@ -524,6 +562,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       else exact_row_stream(row, len, out, K0, R, c, lflags);
       finish_row(S, out, K0, K, lflags, diag, r, PATH_DIRECT, qnan, qnan, 0, 0);
       phase_mark(S, 7);
+      tl_row(nrow++, 4, tl_now());
       continue;
     }
     // the ring is idle: start the row's first chunks before sampling it
@@ -539,6 +578,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       kmax = S.kmax;
     }
     phase_mark(S, 1);
+    tl_row(nrow, 2, tl_now());
     const Bins sb = scan_bins(key1, kmax);
     __syncthreads();
     clear_hist(c.hist);
@@ -556,6 +596,7 @@ __global__ void __launch_bounds__(THREADS, 2)
       C0 = scan_collect<CW>(row, 0, len, R, c, spill, tl, key0, key1, sb, lflags, primed,
                             NextRowJob<E>{scores, row_lens, &P, hdr, &S});
     const uint32_t Cgt = S.ncand, Ceq = S.neq;
+    tl_row(nrow, 3, tl_now());
     if (key0 == key1) C0 += Ceq;
     if (CW == CONSUMER_WARPS) {
       // claim the next row now and warm L2 with its sample points while
@@ -588,7 +629,9 @@ __global__ void __launch_bounds__(THREADS, 2)
     finish_row(S, out, Kr, K, lflags, diag, r, path, key_to_float(key0), key_to_float(key1), C0,
                Cgt + Ceq);
     phase_mark(S, 6);
+    tl_row(nrow++, 4, tl_now());
   }
+  tl_put(1, tl_now());
 #ifdef TOPK_PHASE_TIMING
   if (threadIdx.x == 0)
     for (int i = 0; i < NPHASE; ++i) atomicAdd(&g_phase[i], S.ph[i]);
@@ -1153,5 +1196,25 @@ extern "C" int topk_debug_phase_cycles(unsigned long long* out, int reset) {
     if (cudaMemcpyToSymbol(tk::g_phase, zero, sizeof(zero)) != cudaSuccess) return -4;
   }
   return 0;
+}
+
+// Copies the timeline records of CTAs [0, ctas) of the last k_persistent
+// launches into out (ctas * slots values; with reset != 0 clears them first
+// instead) and returns the slots per CTA (negative on a CUDA error).
+// Exported only by a build with -DTOPK_PHASE_TIMING.
+extern "C" int topk_debug_timeline(unsigned long long* out, int ctas, int reset) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return -4;
+  if (reset) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, tk::g_timeline) != cudaSuccess) return -4;
+    if (cudaMemset(p, 0, sizeof(tk::g_timeline)) != cudaSuccess) return -4;
+    if (cudaDeviceSynchronize() != cudaSuccess) return -4;
+  } else if (out && ctas > 0) {
+    const int n = ctas < tk::TL_CTAS ? ctas : tk::TL_CTAS;
+    if (cudaMemcpyFromSymbol(out, tk::g_timeline,
+                             (size_t)n * tk::TL_SLOTS * sizeof(unsigned long long)) != cudaSuccess)
+      return -4;
+  }
+  return tk::TL_SLOTS;
 }
 #endif

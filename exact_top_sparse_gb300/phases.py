@@ -19,10 +19,14 @@ microseconds one CTA spends per row in each phase:
   finish       closing the row (padding, flags, diagnostics)
   unsampled    rows served without sampling (sentinel or exact path)
 
-and the refinement rounds per row.  The library used by everything else is
-not touched.  Needs a GPU.
+and the refinement rounds per row.  With --timeline it also records, for
+one more call, every CTA's global-timer stamps (start, exit, and for each of
+its first four rows the claim, the start and end of the full-row pass and
+the close) and prints their spread over the CTAs in microseconds from the
+first CTA's start: where a call of few rows per CTA spends its time.  The
+library used by everything else is not touched.  Needs a GPU.
 
-    python -m exact_top_sparse_gb300.phases [--dtype f32|bf16|e4m3] NxM ...
+    python -m exact_top_sparse_gb300.phases [--dtype f32|bf16|e4m3] [--timeline] NxM ...
 """
 import argparse
 import ctypes
@@ -69,6 +73,42 @@ def build_phase_library() -> str:
     return PHASE_LIB
 
 
+def _spread(v):
+    """min / median / 90th percentile / max of v, rounded to 0.1."""
+    v = sorted(v)
+    if not v:
+        return []
+    return [round(v[min(len(v) - 1, int(q * (len(v) - 1) + 0.5))], 1) for q in (0, 0.5, 0.9, 1)]
+
+
+def timeline_summary(shape, tl, grid, slots):
+    """Spread over the CTAs of one launch's timeline stamps (microseconds from
+    the first CTA's start)."""
+    recs = [tl[i * slots:(i + 1) * slots] for i in range(grid)]
+    recs = [r for r in recs if r[0] > 0]
+    t0 = min(r[0] for r in recs)
+    us = lambda t: (t - t0) / 1000.0  # noqa: E731
+    nrows = [sum(1 for j in range((slots - 2) // 5) if r[2 + 5 * j] > 0) for r in recs]
+    out = {"shape": shape, "timeline_ctas": len(recs),
+           "ctas_by_rows": {str(n): nrows.count(n) for n in sorted(set(nrows))},
+           "start_us": _spread([us(r[0]) for r in recs]),
+           "exit_us": _spread([us(r[1]) for r in recs])}
+    for j in range((slots - 2) // 5):
+        rows = [r[2 + 5 * j:7 + 5 * j] for r in recs if r[2 + 5 * j] > 0]
+        sampled = [f for f in rows if f[2] > 0 and f[3] > 0]
+        if not rows:
+            break
+        out["row%d" % j] = {
+            "ctas": len(rows),
+            "claim_us": _spread([us(f[1]) for f in rows]),
+            "close_us": _spread([us(f[4]) for f in rows]),
+            "before_pass_us": _spread([(f[2] - f[1]) / 1000.0 for f in sampled]),
+            "pass_us": _spread([(f[3] - f[2]) / 1000.0 for f in sampled]),
+            "after_pass_us": _spread([(f[4] - f[3]) / 1000.0 for f in sampled]),
+        }
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("shapes", nargs="*", default=["131072x8192", "262144x8192", "524288x8192",
@@ -76,6 +116,7 @@ def main():
     ap.add_argument("--dtype", default="f32", choices=["f32", "bf16", "e4m3"])
     ap.add_argument("--K", type=int, default=2048)
     ap.add_argument("--reps", type=int, default=5)
+    ap.add_argument("--timeline", action="store_true")
     args = ap.parse_args()
 
     import torch
@@ -88,6 +129,9 @@ def main():
     lib = ets.load_library(path)
     lib.topk_debug_phase_cycles.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), ctypes.c_int]
     lib.topk_debug_phase_cycles.restype = ctypes.c_int
+    lib.topk_debug_timeline.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), ctypes.c_int,
+                                        ctypes.c_int]
+    lib.topk_debug_timeline.restype = ctypes.c_int
     dev = torch.device("cuda", 0)
     K = args.K
     for shape in args.shapes:
@@ -121,6 +165,16 @@ def main():
                           "us_per_row_per_cta": per_row,
                           "refine_rounds_per_row": round(buf[ROUNDS_SLOT] / args.reps / M, 2)}),
               flush=True)
+        if args.timeline:
+            grid = int(ets.plan(M, N, K)["grid"])
+            if lib.topk_debug_timeline(None, 0, 1) < 0:
+                raise RuntimeError("timeline reset failed")
+            ets.topk_ragged(x, d, K, out=out)
+            slots = lib.topk_debug_timeline(None, 0, 0)
+            tl = (ctypes.c_ulonglong * (grid * slots))()
+            if lib.topk_debug_timeline(tl, grid, 0) < 0:
+                raise RuntimeError("timeline read failed")
+            print(json.dumps(timeline_summary(shape, list(tl), grid, slots)), flush=True)
         del x, out
         torch.cuda.empty_cache()
 
