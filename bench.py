@@ -116,6 +116,11 @@ def copy_only_step(h, K, chunk_bytes=1 << 30):
     return step, release
 
 
+def step_gbs(nbytes: float, seconds) -> list:
+    """GB/s of each timed step that moved nbytes (one figure per step)."""
+    return [round(nbytes / t / 1e9, 1) for t in seconds]
+
+
 def job_rows_per_s(ws: int, M: int, steps: int, total_ms: float) -> float:
     """Whole-job throughput: every rank selects its own M-row batch per step
     (weak scaling, no data-path collective), timed by the slowest rank."""
@@ -885,7 +890,9 @@ def run_gb300(args):
                              "h2d_bytes_per_step": M * N * 4 + M * 4,
                              "d2h_bytes_per_step": M * K * 4,
                              "steps": len(ts), "api": "topk_ragged_host (pinned host buffers)",
+                             "h2d_gbs_per_step": step_gbs(M * N * 4, ts),
                              "copy_only": {"value": copy_rate, "unit": UNIT, "h2d_gbs": h2d_gbs,
+                                           "h2d_gbs_per_step": step_gbs(M * N * 4, tc),
                                            "what": "the same host->device and device->host "
                                                    "bytes in the same 1 GiB chunks on two "
                                                    "streams, no selection, timed in steps "

@@ -68,3 +68,9 @@ def test_traffic_only_while_the_capture_matches(tmp_path, monkeypatch):
 def test_whole_job_rate():
     # rows of every rank over the slowest rank's time
     assert bench.job_rows_per_s(4, 8192, 10, 50.0) == pytest.approx(4 * 8192 * 10 / 0.05)
+
+
+def test_step_rates():
+    # one figure per step: 2 GB in 0.01 s is 200 GB/s, in 0.02 s 100 GB/s
+    assert bench.step_gbs(2e9, [0.01, 0.02]) == [200.0, 100.0]
+    assert bench.step_gbs(1e9, []) == []
