@@ -86,6 +86,8 @@ def timeline_summary(shape, tl, grid, slots):
     the first CTA's start)."""
     recs = [tl[i * slots:(i + 1) * slots] for i in range(grid)]
     recs = [r for r in recs if r[0] > 0]
+    if not recs:  # the call ran no persistent launch (direct or KV-split plan)
+        return {"shape": shape, "timeline_ctas": 0}
     t0 = min(r[0] for r in recs)
     us = lambda t: (t - t0) / 1000.0  # noqa: E731
     nrows = [sum(1 for j in range((slots - 2) // 5) if r[2 + 5 * j] > 0) for r in recs]

@@ -51,3 +51,9 @@ def test_timeline_summary_counts_and_spreads():
     assert r1["ctas"] == 1
     assert r1["pass_us"] == [28.0, 28.0, 28.0, 28.0]
     assert "row2" not in s
+
+
+def test_timeline_summary_without_persistent_launch():
+    # a call planned as direct or KV-split leaves every record empty
+    s = phases.timeline_summary("1048576x512", [0] * (3 * SLOTS), 3, SLOTS)
+    assert s == {"shape": "1048576x512", "timeline_ctas": 0}
